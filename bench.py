@@ -1,0 +1,536 @@
+"""Throughput of the FastOCR-shaped decode step on one GB300 (or N independent replicas).
+
+One step = one decode position for 8 sequences through all 28 layers: focal layers 3 and 14 run
+fx_focal_attn_scores over the whole cache (4096 visual + 512 text + t tokens) plus fx_topk_select
+(k = 205 of the 4096 visual tokens, warm-started from the previous step); every other layer runs
+fx_sparse_gqa_decode over the selected visual tokens plus all text tokens (layers 0-2 use the previous
+step's layer-14 set).  Inputs are seeded synthetic tensors (no model weights); each step's K/V token
+is already in the cache and the cache length advances by one per step.  Steps are replayed from
+per-step CUDA graphs.  The KV touched per step (~1 GB across 28 layers) is larger than L2, so no
+flush is needed between steps.
+
+Printed JSON line: value = decoded tokens/s over all ranks (attention only), plus the dominant
+kernel's roofline (fx_sparse_gqa_decode: algorithmic bytes / CUDA-event duration vs the measured HBM
+copy bandwidth), the end-to-end rate through the same API with host buffers, SM clocks sampled during
+the timed region and the fp64 oracle timed on the host as a CPU baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fx|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth.workloads import OcrDecode  # noqa: E402
+
+METRIC = "sparse-decode attn tokens/s/GPU and KV GB/s as % of GB300 HBM peak"
+UNIT = "tokens/s"
+ROW_BYTES = 512          # K + V bytes of one (token, KV head) row
+D = 128
+
+
+# ----------------------------------------------------------------------------------------------
+# distributed helpers (host-side only: barriers and max-over-ranks of timings)
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return rank, local, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------------
+# SM clock sampling through NVML (read-only queries)
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+            0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.ok = False
+        self.period = period_s
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self.h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.nv = nv
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_r = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, ctypes.c_int(1), ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if get_r(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        names = [n for bit, n in _REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------------------------
+def _cudart():
+    """The CUDA runtime PyTorch already loaded (for external event nodes and 2-D copies)."""
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    import glob
+    for p in glob.glob(os.path.join(os.path.dirname(torch.__file__), "..", "nvidia", "*", "lib", "libcudart.so*")):
+        try:
+            return ctypes.CDLL(p)
+        except OSError:
+            continue
+    return None
+
+
+class RawEvent:
+    """A timing CUDA event driven through the runtime directly.  Recorded while a stream is being
+    captured, it becomes an event node of the graph (cudaEventRecordExternal), so each replay stamps
+    it on the device timeline around the kernel it brackets."""
+
+    def __init__(self, rt):
+        self.rt = rt
+        self.h = ctypes.c_void_p()
+        if rt.cudaEventCreate(ctypes.byref(self.h)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+
+    def record(self, stream):
+        flags = 1 if torch.cuda.is_current_stream_capturing() else 0
+        err = self.rt.cudaEventRecordWithFlags(self.h, ctypes.c_void_p(stream.cuda_stream), ctypes.c_uint(flags))
+        if err != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags failed ({err})")
+
+    def elapsed_time(self, end) -> float:
+        ms = ctypes.c_float()
+        err = self.rt.cudaEventElapsedTime(ctypes.byref(ms), self.h, end.h)
+        if err != 0:
+            raise RuntimeError(f"cudaEventElapsedTime failed ({err})")
+        return float(ms.value)
+
+
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class OcrDecodeRun:
+    """Device state of the FastOCR-shaped decode and its per-step CUDA graphs."""
+
+    def __init__(self, w: OcrDecode, device, with_e2e: bool):
+        import kv_cache_token_fx_gb300 as fx
+        self.fx = fx
+        self.w = w
+        self.dev = device
+        L, B, Hkv, Hq, T = w.n_layers, w.B, w.Hkv, w.Hq, w.tcap
+        self.K = torch.empty((L, B, Hkv, T, D), dtype=torch.bfloat16, device=device)
+        self.V = torch.empty_like(self.K)
+        self.Q = torch.empty((w.steps, L, B, Hq, 1, D), dtype=torch.bfloat16, device=device)
+        for l in range(L):
+            tab = w.fourier_table(l)
+            k, v = w.layer_kv(l, device=device, table=tab)
+            self.K[l].copy_(k)
+            self.V[l].copy_(v)
+            del k, v
+            for t in range(w.steps):
+                self.Q[t, l].copy_(w.query(t, l, device=device, table=tab))
+        self.lens = torch.tensor([[w.length_at(t)] * B for t in range(w.steps)], dtype=torch.int32, device=device)
+        self.sets = {l: torch.zeros((2, B, Hkv, w.k_keep), dtype=torch.int32, device=device) for l in w.focal_layers}
+        self.scores = torch.empty((B, Hkv, w.n_vis), dtype=torch.float32, device=device)
+        self.O = torch.empty((L, B, Hq, 1, D), dtype=torch.float32, device=device)
+        nb = max(fx.fx_focal_workspace_bytes(B, Hkv, Hq, 1, T), fx.fx_sparse_workspace_bytes(B, Hkv, Hq, w.k_keep, w.n_vis, T),
+                 fx.fx_sparse_workspace_bytes(B, Hkv, Hq, 0, 0, T))
+        self.ws = fx.Workspace(device, nb)
+        self.with_e2e = with_e2e
+        if with_e2e:
+            # the per-step inputs as a host would hold them: queries of all layers and the new K/V row
+            self.Q_host = self.Q.cpu().pin_memory()
+            pos = [w.n_vis + w.n_text + t for t in range(w.steps)]
+            self.Knew_host = torch.stack([self.K[:, :, :, p] for p in pos]).cpu().pin_memory()
+            self.Vnew_host = torch.stack([self.V[:, :, :, p] for p in pos]).cpu().pin_memory()
+            self.O_host = torch.empty(self.O.shape, dtype=torch.float32).pin_memory()
+        self.rt = _cudart()
+        self.graphs, self.graphs_e2e, self.events = {}, {}, {}
+        self.launches_per_step = 0
+
+    # one decode step; `ev` collects (start, end, bytes) around every sparse-decode launch
+    def step(self, t: int, ev=None):
+        fx, w = self.fx, self.w
+        p = t % 2
+        ln = self.lens[t]
+        launches = 0
+        for l in range(w.n_layers):
+            if l in w.focal_layers:
+                fx.fx_focal_attn_scores(self.K[l], self.V[l], ln, self.Q[t, l], cand=(0, w.n_vis), out=self.O[l],
+                                        scores=self.scores, ws=self.ws)
+                prev = self.sets[l][1 - p] if t > 0 else None
+                fx.fx_topk_select(self.scores, w.k_keep, prev=prev, out=self.sets[l][p])
+                launches += 3
+                continue
+            if l < w.focal_layers[0]:
+                sel = self.sets[w.focal_layers[-1]][1 - p] if t > 0 else None
+            elif l < w.focal_layers[-1]:
+                sel = self.sets[w.focal_layers[0]][p]
+            else:
+                sel = self.sets[w.focal_layers[-1]][p]
+            n_keys = (w.k_keep + w.length_at(t) - w.n_vis) if sel is not None else w.length_at(t)
+            nbytes = (w.B * w.Hkv * n_keys * ROW_BYTES + w.B * w.Hq * D * (2 + 4) +
+                      (w.B * w.Hkv * w.k_keep * 4 if sel is not None else 0))
+            if ev is not None:
+                e0, e1 = RawEvent(self.rt), RawEvent(self.rt)
+                self._record(e0)
+            fx.fx_sparse_gqa_decode(self.K[l], self.V[l], ln, self.Q[t, l], sel, w.n_vis if sel is not None else 0,
+                                    out=self.O[l], ws=self.ws)
+            if ev is not None:
+                self._record(e1)
+                ev.append((e0, e1, nbytes))
+            launches += 1
+        self.launches_per_step = launches
+
+    def _record(self, e):
+        e.record(torch.cuda.current_stream())
+
+    def e2e_inputs(self, t: int):
+        """Copy step t's inputs from pinned host memory (queries, new K/V row) into device memory."""
+        w = self.w
+        self.Q[t].copy_(self.Q_host[t], non_blocking=True)
+        pos = w.n_vis + w.n_text + t
+        # one strided 2-D copy per tensor: 28*8*8 rows of 256 bytes, device pitch = one (l, b, h) cache
+        for dst, src in ((self.K, self.Knew_host), (self.V, self.Vnew_host)):
+            rows = w.n_layers * w.B * w.Hkv
+            dptr = dst.data_ptr() + pos * D * 2
+            err = self.rt.cudaMemcpy2DAsync(ctypes.c_void_p(dptr), ctypes.c_size_t(w.tcap * D * 2),
+                                            ctypes.c_void_p(src[t].data_ptr()), ctypes.c_size_t(D * 2),
+                                            ctypes.c_size_t(D * 2), ctypes.c_size_t(rows), ctypes.c_int(1),
+                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+            if err != 0:
+                raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
+
+    def capture(self, with_events: bool):
+        s = torch.cuda.Stream(self.dev)
+        for t in range(self.w.steps):
+            g = torch.cuda.CUDAGraph()
+            ev = [] if with_events else None
+            with torch.cuda.graph(g, stream=s):
+                self.step(t, ev)
+            self.graphs[t] = g
+            self.events[t] = ev
+            if self.with_e2e:
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g2, stream=s):
+                    self.e2e_inputs(t)
+                    self.step(t)
+                    self.O_host.copy_(self.O, non_blocking=True)
+                self.graphs_e2e[t] = g2
+
+
+def run_fx(args, rank, local, ws):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = OcrDecode()
+    run = OcrDecodeRun(w, dev, with_e2e=not args.no_e2e)
+    # eager warm-up step (sizes the workspace, loads the kernels) then capture every step once
+    for t in range(2):
+        run.step(t)
+    torch.cuda.synchronize()
+    with_events = run.rt is not None
+    try:
+        run.capture(with_events)
+    except RuntimeError:
+        with_events = False
+        run.capture(False)
+    torch.cuda.synchronize()
+    if run.fx.fx_device_errors() != 0:
+        raise RuntimeError("device error flag set during warm-up")
+
+    steps = [(args.warmup + i) % w.steps for i in range(args.steps)]
+    for i in range(args.warmup):
+        run.graphs[i % w.steps].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        e_start.record()
+        for t in steps:
+            run.graphs[t].replay()
+        e_end.record()
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = e_start.elapsed_time(e_end)
+    ms_max = max_over_ranks(ms, ws)
+    tokens = sum_over_ranks(float(w.B * len(steps)), ws)
+    value = tokens / (ms_max / 1e3)
+
+    # dominant kernel: fx_sparse_gqa_decode, timed by the event nodes of the replayed graphs.  The
+    # event nodes of a graph keep the times of its latest replay, so each step's graph is read right
+    # after the timed region for the steps it covered (every step index appears at most once per lap).
+    kern_ms, kern_bytes, n_launch = 0.0, 0, 0
+    if with_events:
+        seen = set()
+        for t in steps[-w.steps:]:
+            if t in seen:
+                continue
+            seen.add(t)
+            for e0, e1, nb in run.events[t]:
+                kern_ms += e0.elapsed_time(e1)
+                kern_bytes += nb
+                n_launch += 1
+    peak, peak_kind = measured_hbm_peak()
+    roofline = None
+    if n_launch:
+        achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+        roofline = {"kernel": "fx_sparse_gqa_decode", "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak_source": peak_kind, "avg_launch_us": round(kern_ms * 1e3 / n_launch, 3),
+                    "avg_bytes_per_launch": int(kern_bytes / n_launch), "launches_timed": n_launch}
+
+    # whole-step KV bytes: focal layers read every row, sparse layers the selected + text rows
+    kv_bytes = 0
+    for t in steps:
+        n_focal = w.length_at(t)
+        n_sparse = w.k_keep + w.length_at(t) - w.n_vis
+        per_layer = [n_focal if l in w.focal_layers else (w.length_at(t) if (t == 0 and l < w.focal_layers[0])
+                                                          else n_sparse) for l in range(w.n_layers)]
+        kv_bytes += w.B * w.Hkv * ROW_BYTES * sum(per_layer)
+    kv_gbs = sum_over_ranks(kv_bytes, ws) / (ms_max / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        for i in range(min(args.warmup, 3)):
+            run.graphs_e2e[i % w.steps].replay()
+        torch.cuda.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for t in steps:
+            run.graphs_e2e[t].replay()
+        b.record()
+        torch.cuda.synchronize()
+        barrier(ws)
+        ems = max_over_ranks(a.elapsed_time(b), ws)
+        h2d = run.Q_host[0].numel() * 2 + run.Knew_host[0].numel() * 2 * 2
+        d2h = run.O_host.numel() * 4
+        e2e = {"value": round(tokens / (ems / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems / len(steps), 4)}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, run, args.cpu_seconds)
+
+    if run.fx.fx_device_errors() != 0:
+        raise RuntimeError("device error flag set during the timed steps")
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": len(steps),
+        "warmup": args.warmup, "ms_per_step": round(ms_max / len(steps), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": "ocr_decode: FastOCR-shaped decode, batch 8, 28 layers, 16 q / 8 kv heads, d 128, "
+                               "4096 visual + 512 text tokens + 1 per step, focal layers 3 and 14, top 205 visual "
+                               "tokens (5%) per KV head, warm start from the previous step",
+                   "batch": w.B, "layers": w.n_layers, "kv_tokens": f"{w.length_at(0)}..{w.length_at(w.steps - 1)}",
+                   "k": w.k_keep, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (about 1 GB of KV touched per step)",
+                   "timing": "per-step CUDA graphs, CUDA events, max over ranks"},
+        "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / ws / peak, 4),
+        "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
+        "gpu_launches": run.launches_per_step * len(steps),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+def _oracle_step(w, orc, kv_host, q_host, t, prev_sets, B):
+    """One decode step of the fp64 oracle for the first B sequences: returns the new focal sets."""
+    length = torch.full((B,), w.length_at(t), dtype=torch.int32)
+    sets = {}
+    for l in range(w.n_layers):
+        k, v = kv_host[l]
+        q = q_host[t][l]
+        if l in w.focal_layers:
+            _, sc = orc.focal(k, v, length, q, cand=(0, w.n_vis))
+            sets[l] = torch.from_numpy(orc.topk(sc, w.k_keep))
+            continue
+        if l < w.focal_layers[0]:
+            sel = prev_sets.get(w.focal_layers[-1])
+        elif l < w.focal_layers[-1]:
+            sel = sets[w.focal_layers[0]]
+        else:
+            sel = sets[w.focal_layers[-1]]
+        if sel is None:
+            orc.sparse_decode(k, v, length, q, None, 0)
+        else:
+            orc.sparse_decode(k, v, length, q, sel, w.n_vis)
+    return sets
+
+
+def _host_inputs(w, run, B, steps):
+    """The first B sequences' caches and the first `steps` steps' queries on the host (copied from the
+    generator's device tensors when a device run exists, else generated on the host)."""
+    kv, qs = [], []
+    for l in range(w.n_layers):
+        if run is not None:
+            kv.append((run.K[l, :B].cpu(), run.V[l, :B].cpu()))
+        else:
+            k, v = w.layer_kv(l, device="cuda" if torch.cuda.is_available() else "cpu")
+            kv.append((k[:B].cpu(), v[:B].cpu()))
+    for t in range(steps):
+        if run is not None:
+            qs.append([run.Q[t, l, :B].cpu().contiguous() for l in range(w.n_layers)])
+        else:
+            dev = "cuda" if torch.cuda.is_available() else "cpu"
+            qs.append([w.query(t, l, device=dev)[:B].cpu().contiguous() for l in range(w.n_layers)])
+    return kv, qs
+
+
+def cpu_baseline(w, run, seconds):
+    import oracle as orc
+    orc.build()
+    B = 2
+    cores = orc.set_threads(min(os.cpu_count() or 1, B * w.Hkv))
+    steps = 64
+    kv, qs = _host_inputs(w, run, B, steps)
+    t0 = time.perf_counter()
+    prev = {}
+    done = 0
+    for t in range(steps):
+        prev = _oracle_step(w, orc, kv, qs, t, prev, B)
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(B * done / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} decode steps x {B} of 8 sequences, all 28 layers (fp64 C oracle, "
+                      f"{cores} threads over (sequence, KV head) rows)"}
+
+
+def run_reference(args, rank, local, ws):
+    """The oracle arm: the fp64 CPU oracle on host cores, same workload and metric (a bounded sample
+    per step: 2 of the 8 sequences)."""
+    if rank != 0:
+        return
+    import oracle as orc
+    orc.build()
+    w = OcrDecode()
+    B = 2
+    cores = orc.set_threads(min(os.cpu_count() or 1, B * w.Hkv))
+    n_q = min(w.steps, args.warmup + args.steps)
+    kv, qs = _host_inputs(w, None, B, n_q)
+    prev = {}
+    for i in range(args.warmup):
+        prev = _oracle_step(w, orc, kv, qs, i % n_q, prev, B)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        prev = _oracle_step(w, orc, kv, qs, (args.warmup + i) % n_q, prev, B)
+    dt = time.perf_counter() - t0
+    value = B * args.steps / dt
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "ocr_decode: FastOCR-shaped decode (oracle sample: 2 of 8 sequences per step)",
+                       "batch": B, "layers": w.n_layers, "k": w.k_keep},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: 2 of 8 sequences, all 28 layers"},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="fx", choices=["fx", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "fx":
+        args.warmup = 3
+    rank, local, ws = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, local, ws)
+    else:
+        run_fx(args, rank, local, ws)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

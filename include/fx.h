@@ -1,0 +1,242 @@
+/*
+ * fx.h -- C ABI of libfx: importance-scored KV-cache token selection feeding sparse GQA decode
+ * attention, for one NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute follows three pages:
+ *   [FastOCR]  "FastOCR: Dynamic Visual Fixation via KV Cache Pruning for Efficient Document Parsing",
+ *              Methodology: Focal-Guided Pruning (focal layers attend over the whole cache and keep
+ *              the top-attended image tokens at a kept ratio; the selection is propagated to the
+ *              non-focal layers, which attend only to the pruned set) and Cross-Step Fixation Reuse
+ *              (the deepest focal layer's set from the previous step warm-starts the next step).
+ *   [FastKV]   "FastKV: Decoupling of Context Reduction and KV Cache Compression for Prefill-Decoding
+ *              Acceleration", 2.A Token-Selective Propagation (saliency = attention weights from a
+ *              recent window of queries to every context token) and 2.B Decoupled KV Retention (a
+ *              chosen subset of KV entries is kept for decoding).
+ *   [HPD]      "HPD-Parsing -- Hierarchical Parallel Document Parsing", method part 2 (branches reuse
+ *              the shared visual + layout prefix KV zero-copy and each attends only to that prefix,
+ *              its own prefix and its own history) and part 3 P-MTP (each branch drafts several
+ *              tokens and verifies them in one step).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library allocates no device
+ *     memory; calls that need scratch take a caller-provided workspace sized by the matching
+ *     fx_*_workspace_bytes() query.  A workspace must be zero-filled once before its first use
+ *     (fx_workspace_init does that); every call leaves it ready for the next one.  A workspace may be
+ *     used by one stream at a time.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls only
+ *     enqueue work; none synchronises the host, so they can be captured into CUDA graphs.
+ *   - bf16 tensors are passed as fx_bf16 (the 16-bit storage of a bfloat16).  Head dimension d must
+ *     be 128.  Rows of 128 bf16 values (256 bytes) must start on 16-byte boundaries: base pointers
+ *     16-byte aligned and every row stride a multiple of 8 elements.
+ *   - GQA grouping: with G = Hq / Hkv, query head g belongs to KV head g / G.
+ *   - q and out tensors are laid out [batch, Hq, Mq, 128] (contiguous).  Outputs are fp32.
+ *   - Host-side argument errors return a status and set a thread-local message (fx_last_error);
+ *     nothing is enqueued then.  Data that only the device can see (lengths, indices, offsets) is
+ *     checked by the kernels: a bad value is clamped or skipped -- never dereferenced -- and a bit is
+ *     set in a per-device error word that fx_device_errors() reads and clears.
+ */
+#ifndef FX_H
+#define FX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FX_API __attribute__((visibility("default")))
+#else
+#define FX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fx_bf16; /* storage of one bfloat16 value */
+
+typedef enum {
+    FX_OK = 0,
+    FX_ERR_INVALID_ARG = 1, /* a null pointer, an out-of-range size or a misaligned pointer/stride */
+    FX_ERR_UNSUPPORTED = 2, /* a shape the kernels do not implement (d != 128, too many query rows) */
+    FX_ERR_WORKSPACE = 3,   /* workspace missing, too small or not 256-byte aligned */
+    FX_ERR_CUDA = 4,        /* a CUDA runtime call failed; fx_last_error() has its message */
+    FX_ERR_DEVICE = 5       /* fx_device_errors(): a kernel saw bad device-side data */
+} fx_status;
+
+/* Bits of the device error word (fx_device_errors). */
+#define FX_DEVERR_LEN 1u      /* a length outside [0, capacity]; it was clamped */
+#define FX_DEVERR_INDEX 2u    /* a token index outside [0, len); that entry was skipped */
+#define FX_DEVERR_OFFSETS 4u  /* branch suffix offsets decreasing or past the suffix rows; branch suffix skipped */
+#define FX_DEVERR_CAPACITY 8u /* a compacted cache would exceed its capacity; extra rows not written */
+
+/*
+ * One layer's KV cache, read-only.  Element (b, h, t, c) of K is at k[b*stride_b + h*stride_h +
+ * t*stride_t + c] (strides in elements), likewise V with the same strides.  Rows t < len[b] are
+ * valid; len is a device array of B int32 values with 0 <= len[b] <= Tcap.
+ */
+typedef struct {
+    const fx_bf16* k;
+    const fx_bf16* v;
+    const int32_t* len;
+    int64_t stride_b, stride_h, stride_t;
+    int32_t B, Hkv, Tcap, d;
+} fx_kv_desc;
+
+/* A writable KV cache (destination of fx_kv_compact); len receives the new lengths. */
+typedef struct {
+    fx_bf16* k;
+    fx_bf16* v;
+    int32_t* len;
+    int64_t stride_b, stride_h, stride_t;
+    int32_t B, Hkv, Tcap, d;
+} fx_kv_out_desc;
+
+/* Last host-side error message of the calling thread ("" if none). */
+FX_API const char* fx_last_error(void);
+
+/* ABI version of this header (incremented on any incompatible change). */
+FX_API int fx_abi_version(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the current device.
+ * *bits receives the FX_DEVERR_* bits seen since the last read.  Returns FX_ERR_DEVICE when any bit
+ * was set, FX_OK otherwise.
+ */
+FX_API fx_status fx_device_errors(unsigned* bits, void* stream);
+
+/* Zero-fills a workspace before its first use (an asynchronous memset on `stream`). */
+FX_API fx_status fx_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* fx_focal_attn_scores -- a focal layer: full attention over the whole cache plus per-token
+ * importance.  [FastOCR] Focal-Guided Pruning; [FastKV] 2.A window saliency.
+ *
+ * For each sequence b, KV head h and query row (gi, i) (query head h*G + gi, query position i):
+ *   p_j = softmax_j(scale * q . k_j) over the visible tokens j < len[b] -- and, when q_pos0 >= 0,
+ *         only j <= q_pos0 + i (query position i sits at token position q_pos0 + i: causal window);
+ *   out[b, h*G+gi, i, :] = sum_j p_j v_j                              (written when out != NULL)
+ *   scores[b, h, j - cand_lo] = sum over the group's G*Mq rows of p_j,  cand_lo <= j < cand_hi
+ *                                                                     (written when scores != NULL)
+ * The softmax always runs over every visible token; the candidate range only selects which token
+ * importances are reported (tokens j >= len[b] report 0).  Scores of one row sum to G*Mq over the
+ * full range.  An empty row (len[b] == 0) gives out = 0.
+ *
+ *   kv      cache, as above                    q      [B, Hq, Mq, 128] bf16
+ *   Hq      query heads (multiple of Hkv)      Mq     query positions per sequence (>= 1)
+ *   q_pos0  -1: no causal limit; >= 0: position of query 0
+ *   scale   logit scale (use 1/sqrt(128) for plain attention)
+ *   out     [B, Hq, Mq, 128] fp32 or NULL      scores [B, Hkv, cand_hi - cand_lo] fp32 or NULL
+ *   G*Mq must be <= 64.  0 <= cand_lo <= cand_hi <= Tcap.
+ * Workspace: fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap) bytes.
+ */
+FX_API size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap);
+FX_API fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,
+                               float scale, int cand_lo, int cand_hi, float* out, float* scores,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* fx_topk_select -- keep the k most important tokens of each row.  [FastOCR] Focal-Guided Pruning
+ * (top-attended tokens at kept ratio tau) and Cross-Step Fixation Reuse (warm start).
+ *
+ * For each of `rows` rows of n fp32 scores (row r at scores + r*n): the k entries that come first in
+ * the order (score descending, index ascending) -- so ties go to the lower index -- written to
+ * idx_out[r*k .. r*k+k) in ascending index order.  Scores are compared as floats (-0.0 < +0.0; NaN
+ * must not occur).
+ * prev_idx (NULL or [rows, k] distinct indices in [0, n)) is the previous step's set: it only speeds
+ * the search up (every score at least the smallest score over prev_idx is a candidate) and never
+ * changes the result.  An index of prev_idx outside [0, n) sets FX_DEVERR_INDEX and that row runs
+ * without the warm start.
+ * 1 <= k <= n.  No workspace.
+ */
+FX_API fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int32_t* prev_idx,
+                         int32_t* idx_out, void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* fx_sparse_gqa_decode -- a non-focal layer: decode attention over the selected tokens only.
+ * [FastOCR] Focal-Guided Pruning (non-focal layers attend only to the pruned set; the full cache
+ * stays intact); [FastKV] 2.B (decoding over the retained entries).
+ *
+ * One query position per sequence.  For each b and query head g (KV head h = g / G):
+ *   S = { idx[b, h, 0..k) } followed by the dense tail { tail_lo .. len[b]-1 }
+ *   out[b, g, 0, :] = sum_{j in S} softmax_S(scale * q . k_j) v_j   (softmax renormalised over S)
+ * idx entries are token positions in [0, len[b]); an entry outside that range sets FX_DEVERR_INDEX
+ * and is skipped.  A listed token that is also in the tail counts twice (callers keep idx < tail_lo).
+ * k = 0 with tail_lo = 0 is plain dense decode over the whole cache; an empty S gives out = 0.
+ *
+ *   q    [B, Hq, 1, 128] bf16         idx  [B, Hkv, k] int32 (NULL when k == 0)
+ *   out  [B, Hq, 1, 128] fp32         G = Hq / Hkv must be <= 64
+ * Workspace: fx_sparse_workspace_bytes(B, Hkv, Hq, k, tail_lo, Tcap) bytes.
+ */
+FX_API size_t fx_sparse_workspace_bytes(int B, int Hkv, int Hq, int k, int tail_lo, int Tcap);
+FX_API fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, const int32_t* idx,
+                               int k, int tail_lo, float scale, float* out, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* fx_kv_compact -- decoupled KV retention: copy the retained rows of n_layers layers into a
+ * contiguous cache, once, after prefill.  [FastKV] 2.B.
+ *
+ * For every layer l < n_layers, b and h, destination row r of
+ *   S = idx[b, h, 0..k) followed by tail_lo .. len[b]-1
+ * receives source row S[r] (K and V, bit-exact copies), so the kept rows stay in the order given
+ * (ascending when idx is ascending and below tail_lo).  dst->len[b] = k + max(0, len[b] - tail_lo).
+ * Layer l of the source starts at element offset l*src_stride_layer from src->k / src->v, layer l of
+ * the destination at l*dst_stride_layer; all layers share src->len.  Rows past the new length are
+ * not touched.  An idx entry outside [0, len[b]) sets FX_DEVERR_INDEX and its row is not written; a
+ * new length above dst->Tcap sets FX_DEVERR_CAPACITY and only dst->Tcap rows are written (dst->len
+ * is then clamped to dst->Tcap).
+ *   idx [B, Hkv, k] int32 (NULL when k == 0).  src and dst must agree on B, Hkv and d.
+ * No workspace.
+ */
+FX_API fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx, int k,
+                        int tail_lo, const fx_kv_out_desc* dst, int64_t dst_stride_layer,
+                        int n_layers, void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* fx_shared_prefix_decode -- parallel draft verification over a shared prefix.  [HPD] parts 2
+ * (shared-prefix KV reuse with context isolation) and 3 (P-MTP parallel verification).
+ *
+ * Br branches share one prefix KV.  Branch b owns suffix rows off[b] .. off[b+1]-1 and Mq draft
+ * rows.  For branch b, KV head h and query row (gi, i) (query head h*G + gi, draft position i):
+ *   S = prefix rows (all P of them, or prefix_idx[b, h, 0..kp) when prefix_idx != NULL)
+ *       ++ the branch's suffix rows ++ the branch's draft rows 0..i         (causal inside the draft)
+ *   out[b, h*G+gi, i, :] = sum_{j in S} softmax_S(scale * q . k_j) v_j
+ *
+ *   prefix      rows (h, t) at k + h*stride_h + t*stride_t, t < P
+ *   suffix      rows (h, t) at suf_k + h*suf_stride_h + t*suf_stride_t, t < suf_rows
+ *   suf_off     device [Br + 1] int32, non-decreasing, suf_off[Br] <= suf_rows; max_suffix bounds
+ *               every suf_off[b+1] - suf_off[b] (longer suffixes set FX_DEVERR_OFFSETS and are cut)
+ *   draft       rows (b, i, h) at draft_k + b*draft_stride_b + i*draft_stride_i + h*draft_stride_h
+ *   q           [Br, Hq, Mq, 128] bf16;  out [Br, Hq, Mq, 128] fp32;  G*Mq <= 64
+ *   prefix_idx  NULL (dense prefix) or [Br, Hkv, kp] int32 prefix positions in [0, P)
+ * Workspace: fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np, max_suffix) bytes, where np is
+ * P (dense) or kp (sparse).
+ */
+typedef struct {
+    const fx_bf16* k;
+    const fx_bf16* v;
+    int64_t stride_h, stride_t;
+    int32_t P, Hkv, d;
+} fx_prefix_desc;
+
+typedef struct {
+    const fx_bf16* suf_k;
+    const fx_bf16* suf_v;
+    int64_t suf_stride_h, suf_stride_t;
+    const int32_t* suf_off;
+    int32_t suf_rows, max_suffix;
+    const fx_bf16* draft_k;
+    const fx_bf16* draft_v;
+    int64_t draft_stride_b, draft_stride_i, draft_stride_h;
+    int32_t Br, Mq;
+} fx_branch_desc;
+
+FX_API size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np, int max_suffix);
+FX_API fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_desc* branches,
+                                  const fx_bf16* q, int Hq, const int32_t* prefix_idx, int kp,
+                                  float scale, float* out, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FX_H */

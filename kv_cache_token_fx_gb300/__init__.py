@@ -1,0 +1,335 @@
+"""Python binding of libfx (include/fx.h): argument marshalling only.
+
+Every function here checks tensor dtypes/devices, allocates outputs and workspaces with PyTorch, and
+calls the C entry point of the same name; all arithmetic runs in the library's CUDA kernels.  There is
+no fallback: if libfx.so has not been built, or a CUDA tensor is missing, the call raises.
+
+Build the library with ``python -m kv_cache_token_fx_gb300.build`` (or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "FxError", "load_library", "library_path", "Workspace", "fx_focal_attn_scores", "fx_topk_select",
+    "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode", "fx_device_errors",
+    "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
+    "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY",
+]
+
+FX_OK, FX_ERR_INVALID_ARG, FX_ERR_UNSUPPORTED, FX_ERR_WORKSPACE, FX_ERR_CUDA, FX_ERR_DEVICE = range(6)
+FX_DEVERR_LEN, FX_DEVERR_INDEX, FX_DEVERR_OFFSETS, FX_DEVERR_CAPACITY = 1, 2, 4, 8
+_STATUS = {0: "FX_OK", 1: "FX_ERR_INVALID_ARG", 2: "FX_ERR_UNSUPPORTED", 3: "FX_ERR_WORKSPACE",
+           4: "FX_ERR_CUDA", 5: "FX_ERR_DEVICE"}
+
+c_vp, c_i64, c_i32, c_int, c_float, c_size = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
+                                              ctypes.c_float, ctypes.c_size_t)
+
+
+class FxError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class KVDesc(ctypes.Structure):
+    _fields_ = [("k", c_vp), ("v", c_vp), ("len", c_vp), ("stride_b", c_i64), ("stride_h", c_i64),
+                ("stride_t", c_i64), ("B", c_i32), ("Hkv", c_i32), ("Tcap", c_i32), ("d", c_i32)]
+
+
+KVOutDesc = type("KVOutDesc", (ctypes.Structure,), {"_fields_": KVDesc._fields_})
+
+
+class PrefixDesc(ctypes.Structure):
+    _fields_ = [("k", c_vp), ("v", c_vp), ("stride_h", c_i64), ("stride_t", c_i64), ("P", c_i32),
+                ("Hkv", c_i32), ("d", c_i32)]
+
+
+class BranchDesc(ctypes.Structure):
+    _fields_ = [("suf_k", c_vp), ("suf_v", c_vp), ("suf_stride_h", c_i64), ("suf_stride_t", c_i64),
+                ("suf_off", c_vp), ("suf_rows", c_i32), ("max_suffix", c_i32), ("draft_k", c_vp),
+                ("draft_v", c_vp), ("draft_stride_b", c_i64), ("draft_stride_i", c_i64),
+                ("draft_stride_h", c_i64), ("Br", c_i32), ("Mq", c_i32)]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libfx.so (must have been built).  Raises FxError if it is missing."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise FxError(FX_ERR_CUDA, f"{path} is not built; run `python -m kv_cache_token_fx_gb300.build`")
+        lib = ctypes.CDLL(path)
+        lib.fx_last_error.restype = ctypes.c_char_p
+        lib.fx_abi_version.restype = c_int
+        lib.fx_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), c_vp]
+        lib.fx_workspace_init.argtypes = [c_vp, c_size, c_vp]
+        lib.fx_focal_workspace_bytes.argtypes = [c_int] * 5
+        lib.fx_focal_workspace_bytes.restype = c_size
+        lib.fx_focal_attn_scores.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_int, c_int, c_float, c_int,
+                                             c_int, c_vp, c_vp, c_vp, c_size, c_vp]
+        lib.fx_topk_select.argtypes = [c_vp, c_int, c_int, c_int, c_vp, c_vp, c_vp]
+        lib.fx_sparse_workspace_bytes.argtypes = [c_int] * 6
+        lib.fx_sparse_workspace_bytes.restype = c_size
+        lib.fx_sparse_gqa_decode.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_vp, c_int, c_int, c_float,
+                                             c_vp, c_vp, c_size, c_vp]
+        lib.fx_kv_compact.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_vp, c_int, c_int, ctypes.POINTER(KVOutDesc),
+                                      c_i64, c_int, c_vp]
+        lib.fx_shared_prefix_workspace_bytes.argtypes = [c_int] * 6
+        lib.fx_shared_prefix_workspace_bytes.restype = c_size
+        lib.fx_shared_prefix_decode.argtypes = [ctypes.POINTER(PrefixDesc), ctypes.POINTER(BranchDesc), c_vp, c_int,
+                                                c_vp, c_int, c_float, c_vp, c_vp, c_size, c_vp]
+        for name in ("fx_device_errors", "fx_workspace_init", "fx_focal_attn_scores", "fx_topk_select",
+                     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode"):
+            getattr(lib, name).restype = c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != FX_OK:
+        msg = load_library().fx_last_error().decode(errors="replace")
+        raise FxError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need_cuda(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise FxError(FX_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise FxError(FX_ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _kv_desc(k, v, length):
+    _need_cuda(k, "k", torch.bfloat16)
+    _need_cuda(v, "v", torch.bfloat16)
+    _need_cuda(length, "len", torch.int32)
+    if k.dim() != 4 or k.shape != v.shape or k.stride() != v.stride() or k.stride(3) != 1:
+        raise FxError(FX_ERR_INVALID_ARG, "k and v must be [B, Hkv, Tcap, d] views with equal strides, unit last stride")
+    B, Hkv, Tcap, d = k.shape
+    return KVDesc(k.data_ptr(), v.data_ptr(), length.data_ptr(), k.stride(0), k.stride(1), k.stride(2), B, Hkv,
+                  Tcap, d)
+
+
+def _default_scale(d):
+    return 1.0 / math.sqrt(d)
+
+
+class Workspace:
+    """A zero-initialised device scratch buffer reused across calls on one stream.
+
+    ``ensure(nbytes)`` grows it (allocating a fresh zeroed buffer) when needed; a buffer that a CUDA
+    graph has captured must not be grown afterwards, so size it before capture.
+    """
+
+    def __init__(self, device=None, nbytes: int = 0):
+        self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.buf = None
+        if nbytes:
+            self.ensure(nbytes)
+
+    def ensure(self, nbytes: int, stream=None):
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=self.device)
+            _check(load_library().fx_workspace_init(_ptr(self.buf), self.buf.numel(), _stream(stream)))
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(ws, nbytes, device, stream):
+    if ws is None:
+        key = device.index if device.index is not None else torch.cuda.current_device()
+        ws = _default_ws.get(key)
+        if ws is None:
+            ws = _default_ws[key] = Workspace(torch.device("cuda", key))
+    buf = ws.ensure(nbytes, stream)
+    return buf
+
+
+def fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap) -> int:
+    return int(load_library().fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap))
+
+
+def fx_sparse_workspace_bytes(B, Hkv, Hq, k, tail_lo, Tcap) -> int:
+    return int(load_library().fx_sparse_workspace_bytes(B, Hkv, Hq, k, tail_lo, Tcap))
+
+
+def fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np_, max_suffix) -> int:
+    return int(load_library().fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np_, max_suffix))
+
+
+def fx_focal_attn_scores(k, v, length, q, *, q_pos0: int = -1, scale=None, cand=None, want_out=True,
+                         want_scores=True, out=None, scores=None, ws=None, stream=None):
+    """Focal layer: full attention + per-token importance.  Returns (out, scores) (None if not wanted).
+
+    k, v [B, Hkv, Tcap, 128] bf16; length int32 [B]; q [B, Hq, Mq, 128] bf16 (contiguous).
+    cand = (lo, hi) candidate range for the scores (default: the whole capacity).
+    """
+    lib = load_library()
+    desc = _kv_desc(k, v, length)
+    _need_cuda(q, "q", torch.bfloat16)
+    if not q.is_contiguous() or q.dim() != 4:
+        raise FxError(FX_ERR_INVALID_ARG, "q must be a contiguous [B, Hq, Mq, 128] tensor")
+    B, Hkv, Tcap, d = k.shape
+    _, Hq, Mq, _ = q.shape
+    lo, hi = cand if cand is not None else (0, Tcap)
+    if want_out and out is None:
+        out = torch.empty((B, Hq, Mq, d), dtype=torch.float32, device=k.device)
+    if want_scores and scores is None:
+        scores = torch.empty((B, Hkv, hi - lo), dtype=torch.float32, device=k.device)
+    if not want_out:
+        out = None
+    if not want_scores:
+        scores = None
+    nbytes = lib.fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap)
+    buf = _workspace(ws, nbytes, k.device, stream)
+    sc = _default_scale(d) if scale is None else float(scale)
+    _check(lib.fx_focal_attn_scores(ctypes.byref(desc), _ptr(q), Hq, Mq, int(q_pos0), sc, int(lo), int(hi),
+                                    _ptr(out), _ptr(scores), _ptr(buf), buf.numel(), _stream(stream)))
+    return out, scores
+
+
+def fx_topk_select(scores, k: int, *, prev=None, out=None, stream=None):
+    """Top-k of each row of ``scores`` [..., n] (fp32, contiguous): int32 [..., k], ascending indices."""
+    lib = load_library()
+    _need_cuda(scores, "scores", torch.float32)
+    if not scores.is_contiguous():
+        raise FxError(FX_ERR_INVALID_ARG, "scores must be contiguous")
+    n = scores.shape[-1]
+    rows = scores.numel() // n if n else 0
+    if out is None:
+        out = torch.empty(scores.shape[:-1] + (k,), dtype=torch.int32, device=scores.device)
+    if prev is not None:
+        _need_cuda(prev, "prev", torch.int32)
+        if prev.numel() != rows * k or not prev.is_contiguous():
+            raise FxError(FX_ERR_INVALID_ARG, "prev must be a contiguous [rows, k] int32 tensor")
+    _check(lib.fx_topk_select(_ptr(scores), rows, n, int(k), _ptr(prev), _ptr(out), _stream(stream)))
+    return out
+
+
+def fx_sparse_gqa_decode(k, v, length, q, idx, tail_lo: int, *, scale=None, out=None, ws=None, stream=None):
+    """Decode attention of q [B, Hq, 1, 128] over idx [B, Hkv, kk] (or None) plus the tail [tail_lo, len)."""
+    lib = load_library()
+    desc = _kv_desc(k, v, length)
+    _need_cuda(q, "q", torch.bfloat16)
+    if not q.is_contiguous() or q.dim() != 4 or q.shape[2] != 1:
+        raise FxError(FX_ERR_INVALID_ARG, "q must be a contiguous [B, Hq, 1, 128] tensor")
+    B, Hkv, Tcap, d = k.shape
+    Hq = q.shape[1]
+    kk = 0
+    if idx is not None:
+        _need_cuda(idx, "idx", torch.int32)
+        if not idx.is_contiguous() or idx.dim() != 3 or tuple(idx.shape[:2]) != (B, Hkv):
+            raise FxError(FX_ERR_INVALID_ARG, "idx must be a contiguous [B, Hkv, k] int32 tensor")
+        kk = idx.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, 1, d), dtype=torch.float32, device=k.device)
+    nbytes = lib.fx_sparse_workspace_bytes(B, Hkv, Hq, kk, int(tail_lo), Tcap)
+    buf = _workspace(ws, nbytes, k.device, stream)
+    sc = _default_scale(d) if scale is None else float(scale)
+    _check(lib.fx_sparse_gqa_decode(ctypes.byref(desc), _ptr(q), Hq, _ptr(idx) if kk else None, kk, int(tail_lo),
+                                    sc, _ptr(out), _ptr(buf), buf.numel(), _stream(stream)))
+    return out
+
+
+def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, stream=None):
+    """Compact the retained rows of one layer ([B, Hkv, T, 128]) or of L layers ([L, B, Hkv, T, 128])."""
+    lib = load_library()
+    if k.dim() == 5:
+        n_layers = k.shape[0]
+        if dst_k.dim() != 5 or dst_k.shape[0] != n_layers:
+            raise FxError(FX_ERR_INVALID_ARG, "dst must have the same number of layers")
+        s_layer, d_layer = k.stride(0), dst_k.stride(0)
+        if v.stride(0) != s_layer or dst_v.stride(0) != d_layer:
+            raise FxError(FX_ERR_INVALID_ARG, "k/v layer strides must match")
+        src = _kv_desc(k[0], v[0], length)
+        dst = _kv_desc(dst_k[0], dst_v[0], dst_len)
+    else:
+        n_layers, s_layer, d_layer = 1, 0, 0
+        src = _kv_desc(k, v, length)
+        dst = _kv_desc(dst_k, dst_v, dst_len)
+    kk = 0
+    if idx is not None:
+        _need_cuda(idx, "idx", torch.int32)
+        if not idx.is_contiguous():
+            raise FxError(FX_ERR_INVALID_ARG, "idx must be contiguous [B, Hkv, k]")
+        kk = idx.shape[-1]
+    dst_out = KVOutDesc(*[getattr(dst, f) for f, _ in KVDesc._fields_])
+    _check(lib.fx_kv_compact(ctypes.byref(src), s_layer, _ptr(idx) if kk else None, kk, int(tail_lo),
+                             ctypes.byref(dst_out), d_layer, n_layers, _stream(stream)))
+    return dst_k, dst_v, dst_len
+
+
+def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, prefix_idx=None, scale=None,
+                            out=None, ws=None, stream=None):
+    """Draft verification of Br branches over one shared prefix.
+
+    pk, pv [Hkv, P, 128]; sk, sv [Hkv, S, 128] (branch b owns rows off[b]..off[b+1]-1);
+    off int32 [Br + 1]; dk, dv [Br, Mq, Hkv, 128]; q [Br, Hq, Mq, 128]; prefix_idx [Br, Hkv, kp] or None.
+    """
+    lib = load_library()
+    for t, n in ((pk, "pk"), (pv, "pv"), (sk, "sk"), (sv, "sv"), (dk, "dk"), (dv, "dv"), (q, "q")):
+        _need_cuda(t, n, torch.bfloat16)
+    _need_cuda(off, "off", torch.int32)
+    if pk.stride() != pv.stride() or sk.stride() != sv.stride() or dk.stride() != dv.stride():
+        raise FxError(FX_ERR_INVALID_ARG, "paired K/V tensors must share strides")
+    if not q.is_contiguous():
+        raise FxError(FX_ERR_INVALID_ARG, "q must be contiguous")
+    Hkv, P, d = pk.shape
+    Br, Hq, Mq, _ = q.shape
+    pre = PrefixDesc(pk.data_ptr(), pv.data_ptr(), pk.stride(0), pk.stride(1), P, Hkv, d)
+    brd = BranchDesc(sk.data_ptr(), sv.data_ptr(), sk.stride(0), sk.stride(1), off.data_ptr(), sk.shape[1],
+                     int(max_suffix), dk.data_ptr(), dv.data_ptr(), dk.stride(0), dk.stride(1), dk.stride(2), Br, Mq)
+    kp = 0
+    if prefix_idx is not None:
+        _need_cuda(prefix_idx, "prefix_idx", torch.int32)
+        if not prefix_idx.is_contiguous():
+            raise FxError(FX_ERR_INVALID_ARG, "prefix_idx must be contiguous [Br, Hkv, kp]")
+        kp = prefix_idx.shape[-1]
+    if out is None:
+        out = torch.empty((Br, Hq, Mq, d), dtype=torch.float32, device=q.device)
+    np_ = kp if prefix_idx is not None else P
+    nbytes = lib.fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np_, int(max_suffix))
+    buf = _workspace(ws, nbytes, q.device, stream)
+    sc = _default_scale(d) if scale is None else float(scale)
+    _check(lib.fx_shared_prefix_decode(ctypes.byref(pre), ctypes.byref(brd), _ptr(q), Hq, _ptr(prefix_idx), kp, sc,
+                                       _ptr(out), _ptr(buf), buf.numel(), _stream(stream)))
+    return out
+
+
+def fx_device_errors(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the FX_DEVERR_* bits of the current device."""
+    bits = ctypes.c_uint(0)
+    st = load_library().fx_device_errors(ctypes.byref(bits), _stream(stream))
+    if st not in (FX_OK, FX_ERR_DEVICE):
+        _check(st)
+    return int(bits.value)

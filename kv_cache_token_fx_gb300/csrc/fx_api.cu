@@ -1,0 +1,528 @@
+// Host side of libfx: argument checks, workspace planning, kernel launches and the device error word.
+// Every entry point is extern "C" and declared in include/fx.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "fx_internal.h"
+
+using namespace fx;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int kMaxDevices = 64;
+constexpr size_t kAlign = 256;
+
+thread_local char g_msg[512] = "";
+
+fx_status fail(fx_status st, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fx_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(FX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+// Per-device error word written by the kernels (atomicOr of FX_DEVERR_* bits).
+__device__ unsigned g_fx_device_error;
+
+namespace {
+
+struct DeviceState {
+    bool ready = false;
+    unsigned* err = nullptr;
+    int sm_count = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+fx_status device_state(DeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FX_ERR_CUDA, "device ordinal %d out of range", dev);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_fx_device_error);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        s.ready = true;
+    }
+    *out = &s;
+    return FX_OK;
+}
+
+int sm_count_or_default()
+{
+    DeviceState* s = nullptr;
+    if (device_state(&s) == FX_OK) return s->sm_count;
+    return 152;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool row_stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0; }
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Split-KV plan: how many query-row groups, how many key splits and how long each split is.
+struct Plan {
+    int rb, nrg, nsplit, split_len;
+};
+
+Plan make_plan(int pairs, int R, int max_keys, int sm_count)
+{
+    Plan pl;
+    pl.rb = rows_per_block(R);
+    pl.nrg = cdiv(R, pl.rb);
+    const int per_split = pairs * pl.nrg;
+    const int target = 4 * sm_count;                  // about 4 resident CTAs per SM in one wave
+    int ns = cdiv(target, per_split);
+    ns = ns > cdiv(max_keys, 4096) ? ns : cdiv(max_keys, 4096);   // at most 4096 keys per split
+    const int cap = max_keys / 64 > 1 ? max_keys / 64 : 1;        // at least ~64 keys per split
+    if (ns > cap) ns = cap;
+    if (ns < 1) ns = 1;
+    int len = cdiv(max_keys > 0 ? max_keys : 1, ns);
+    len = cdiv(len, 16) * 16;
+    pl.split_len = len;
+    pl.nsplit = cdiv(max_keys > 0 ? max_keys : 1, len);
+    return pl;
+}
+
+struct Layout {
+    size_t part_m, part_l, part_o, logits, counters, total;
+};
+
+Layout make_layout(int pairs, int R, const Plan& pl, int tcap_for_logits, bool with_counters)
+{
+    Layout L;
+    const size_t P = (size_t)pairs * R * pl.nsplit;
+    size_t off = 0;
+    L.part_m = off;
+    off += round_up(P * sizeof(float));
+    L.part_l = off;
+    off += round_up(P * sizeof(float));
+    L.part_o = off;
+    off += round_up(P * kHeadDim * sizeof(float));
+    L.logits = off;
+    off += round_up((size_t)pairs * R * (size_t)(tcap_for_logits > 0 ? tcap_for_logits : 0) * sizeof(float));
+    L.counters = off;
+    off += with_counters ? round_up((size_t)pairs * pl.nrg * sizeof(unsigned)) : 0;
+    L.total = off;
+    return L;
+}
+
+fx_status check_kv(const fx_kv_desc* kv, const char* name)
+{
+    if (!kv) return fail(FX_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!kv->k || !kv->v || !kv->len) return fail(FX_ERR_INVALID_ARG, "%s: k, v and len must be non-NULL", name);
+    if (kv->d != kHeadDim) return fail(FX_ERR_UNSUPPORTED, "%s: head dim %d (only 128 is implemented)", name, kv->d);
+    if (kv->B < 1 || kv->Hkv < 1 || kv->Tcap < 0)
+        return fail(FX_ERR_INVALID_ARG, "%s: need B >= 1, Hkv >= 1, Tcap >= 0", name);
+    if (!aligned16(kv->k) || !aligned16(kv->v))
+        return fail(FX_ERR_INVALID_ARG, "%s: k and v must be 16-byte aligned", name);
+    if (!row_stride_ok(kv->stride_b) || !row_stride_ok(kv->stride_h) || !row_stride_ok(kv->stride_t))
+        return fail(FX_ERR_INVALID_ARG, "%s: strides must be non-negative multiples of 8 elements", name);
+    return FX_OK;
+}
+
+fx_status check_heads(int Hq, int Hkv, int Mq)
+{
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+        return fail(FX_ERR_INVALID_ARG, "Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
+    if (Mq < 1) return fail(FX_ERR_INVALID_ARG, "Mq must be >= 1");
+    if ((Hq / Hkv) * Mq > kMaxRows)
+        return fail(FX_ERR_UNSUPPORTED, "G*Mq = %d query rows per KV head (at most %d)", (Hq / Hkv) * Mq, kMaxRows);
+    return FX_OK;
+}
+
+fx_status check_ws(void* ws, size_t ws_bytes, size_t need)
+{
+    if (need == 0) return FX_OK;
+    if (!ws) return fail(FX_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+        return fail(FX_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < need) return fail(FX_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", ws_bytes, need);
+    return FX_OK;
+}
+
+float log2e_scale(float scale) { return scale * 1.4426950408889634f; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fx_last_error(void) { return g_msg; }
+
+int fx_abi_version(void) { return kAbiVersion; }
+
+fx_status fx_device_errors(unsigned* bits, void* stream)
+{
+    if (!bits) return fail(FX_ERR_INVALID_ARG, "bits is NULL");
+    DeviceState* ds = nullptr;
+    fx_status st = device_state(&ds);
+    if (st != FX_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(&v, ds->err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+    e = cudaMemset(ds->err, 0, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    *bits = v;
+    return v ? FX_ERR_DEVICE : FX_OK;
+}
+
+fx_status fx_workspace_init(void* ws, size_t ws_bytes, void* stream)
+{
+    if (ws_bytes == 0) return FX_OK;
+    if (!ws) return fail(FX_ERR_WORKSPACE, "workspace is NULL");
+    cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+    return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap)
+{
+    if (B < 1 || Hkv < 1 || Hq < Hkv || Mq < 1 || Tcap < 0) return 0;
+    const int R = (Hq / Hkv) * Mq;
+    const Plan pl = make_plan(B * Hkv, R, Tcap, sm_count_or_default());
+    return make_layout(B * Hkv, R, pl, Tcap, false).total;
+}
+
+fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,
+                               float scale, int cand_lo, int cand_hi, float* out, float* scores,
+                               void* ws, size_t ws_bytes, void* stream)
+{
+    fx_status st = check_kv(kv, "kv");
+    if (st != FX_OK) return st;
+    if ((st = check_heads(Hq, kv->Hkv, Mq)) != FX_OK) return st;
+    if (!q || !aligned16(q)) return fail(FX_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+    if (!out && !scores) return fail(FX_ERR_INVALID_ARG, "out and scores are both NULL");
+    if (q_pos0 < -1) return fail(FX_ERR_INVALID_ARG, "q_pos0 must be -1 or >= 0");
+    if (!isfinite(scale)) return fail(FX_ERR_INVALID_ARG, "scale must be finite");
+    if (scores && (cand_lo < 0 || cand_lo > cand_hi || cand_hi > kv->Tcap))
+        return fail(FX_ERR_INVALID_ARG, "candidate range [%d, %d) not inside [0, Tcap=%d]", cand_lo, cand_hi, kv->Tcap);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
+
+    const int pairs = kv->B * kv->Hkv;
+    const int G = Hq / kv->Hkv;
+    const int R = G * Mq;
+    const Plan pl = make_plan(pairs, R, kv->Tcap, ds->sm_count);
+    const Layout L = make_layout(pairs, R, pl, kv->Tcap, false);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
+    if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
+
+    char* w = static_cast<char*>(ws);
+    AttnParams p;
+    memset(&p, 0, sizeof p);
+    p.k = kv->k;
+    p.v = kv->v;
+    p.len = kv->len;
+    p.sb = kv->stride_b;
+    p.sh = kv->stride_h;
+    p.st = kv->stride_t;
+    p.B = kv->B;
+    p.Hkv = kv->Hkv;
+    p.Tcap = kv->Tcap;
+    p.q = q;
+    p.Hq = Hq;
+    p.G = G;
+    p.Mq = Mq;
+    p.R = R;
+    p.q_pos0 = q_pos0;
+    p.qscale = log2e_scale(scale);
+    p.nsplit = pl.nsplit;
+    p.split_len = pl.split_len;
+    p.nrg = pl.nrg;
+    p.part_m = reinterpret_cast<float*>(w + L.part_m);
+    p.part_l = reinterpret_cast<float*>(w + L.part_l);
+    p.part_o = reinterpret_cast<float*>(w + L.part_o);
+    p.logits = scores ? reinterpret_cast<float*>(w + L.logits) : nullptr;
+    p.err = ds->err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_attn_partial(p, kModeFocal, pl.rb, s);
+    if (e != cudaSuccess) return cuda_fail(e, "focal attention launch");
+
+    FocalCombineParams c;
+    c.part_m = p.part_m;
+    c.part_l = p.part_l;
+    c.part_o = p.part_o;
+    c.logits = p.logits;
+    c.len = kv->len;
+    c.B = kv->B;
+    c.Hkv = kv->Hkv;
+    c.Tcap = kv->Tcap;
+    c.Hq = Hq;
+    c.G = G;
+    c.Mq = Mq;
+    c.R = R;
+    c.nsplit = pl.nsplit;
+    c.cand_lo = cand_lo;
+    c.cand_hi = cand_hi;
+    c.out = out;
+    c.scores = scores;
+    c.err = ds->err;
+    e = launch_focal_combine(c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "focal combine launch");
+    return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int32_t* prev_idx,
+                         int32_t* idx_out, void* stream)
+{
+    if (!scores || !idx_out) return fail(FX_ERR_INVALID_ARG, "scores and idx_out must be non-NULL");
+    if (rows < 1) return fail(FX_ERR_INVALID_ARG, "rows must be >= 1");
+    if (k < 1 || k > n) return fail(FX_ERR_INVALID_ARG, "need 1 <= k (%d) <= n (%d)", k, n);
+    DeviceState* ds = nullptr;
+    fx_status st = device_state(&ds);
+    if (st != FX_OK) return st;
+    TopkParams p;
+    p.scores = scores;
+    p.rows = rows;
+    p.n = n;
+    p.k = k;
+    p.prev = prev_idx;
+    p.out = idx_out;
+    p.err = ds->err;
+    cudaError_t e = launch_topk(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+size_t fx_sparse_workspace_bytes(int B, int Hkv, int Hq, int k, int tail_lo, int Tcap)
+{
+    if (B < 1 || Hkv < 1 || Hq < Hkv || k < 0 || tail_lo < 0 || Tcap < 0) return 0;
+    const int R = Hq / Hkv;
+    const int max_keys = k + (Tcap > tail_lo ? Tcap - tail_lo : 0);
+    const Plan pl = make_plan(B * Hkv, R, max_keys, sm_count_or_default());
+    return make_layout(B * Hkv, R, pl, 0, true).total;
+}
+
+fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, const int32_t* idx,
+                               int k, int tail_lo, float scale, float* out, void* ws,
+                               size_t ws_bytes, void* stream)
+{
+    fx_status st = check_kv(kv, "kv");
+    if (st != FX_OK) return st;
+    if ((st = check_heads(Hq, kv->Hkv, 1)) != FX_OK) return st;
+    if (!q || !aligned16(q)) return fail(FX_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+    if (!out) return fail(FX_ERR_INVALID_ARG, "out is NULL");
+    if (k < 0 || (k > 0 && !idx)) return fail(FX_ERR_INVALID_ARG, "need k >= 0 and idx when k > 0");
+    if (tail_lo < 0) return fail(FX_ERR_INVALID_ARG, "tail_lo must be >= 0");
+    if (!isfinite(scale)) return fail(FX_ERR_INVALID_ARG, "scale must be finite");
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
+
+    const int pairs = kv->B * kv->Hkv;
+    const int G = Hq / kv->Hkv;
+    const int R = G;
+    const int max_keys = k + (kv->Tcap > tail_lo ? kv->Tcap - tail_lo : 0);
+    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count);
+    const Layout L = make_layout(pairs, R, pl, 0, true);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
+    if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
+
+    char* w = static_cast<char*>(ws);
+    AttnParams p;
+    memset(&p, 0, sizeof p);
+    p.k = kv->k;
+    p.v = kv->v;
+    p.len = kv->len;
+    p.sb = kv->stride_b;
+    p.sh = kv->stride_h;
+    p.st = kv->stride_t;
+    p.B = kv->B;
+    p.Hkv = kv->Hkv;
+    p.Tcap = kv->Tcap;
+    p.q = q;
+    p.Hq = Hq;
+    p.G = G;
+    p.Mq = 1;
+    p.R = R;
+    p.q_pos0 = -1;
+    p.qscale = log2e_scale(scale);
+    p.idx = k > 0 ? idx : nullptr;
+    p.kk = k;
+    p.tail_lo = tail_lo;
+    p.nsplit = pl.nsplit;
+    p.split_len = pl.split_len;
+    p.nrg = pl.nrg;
+    p.part_m = reinterpret_cast<float*>(w + L.part_m);
+    p.part_l = reinterpret_cast<float*>(w + L.part_l);
+    p.part_o = reinterpret_cast<float*>(w + L.part_o);
+    p.counters = reinterpret_cast<unsigned*>(w + L.counters);
+    p.out = out;
+    p.err = ds->err;
+    cudaError_t e = launch_attn_partial(p, kModeSparse, pl.rb, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse decode launch");
+    return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx, int k,
+                        int tail_lo, const fx_kv_out_desc* dst, int64_t dst_stride_layer,
+                        int n_layers, void* stream)
+{
+    fx_status st = check_kv(src, "src");
+    if (st != FX_OK) return st;
+    if (!dst) return fail(FX_ERR_INVALID_ARG, "dst is NULL");
+    fx_kv_desc dview = {dst->k, dst->v, dst->len, dst->stride_b, dst->stride_h, dst->stride_t,
+                        dst->B, dst->Hkv, dst->Tcap, dst->d};
+    if ((st = check_kv(&dview, "dst")) != FX_OK) return st;
+    if (dst->B != src->B || dst->Hkv != src->Hkv)
+        return fail(FX_ERR_INVALID_ARG, "src and dst must have the same B and Hkv");
+    if (n_layers < 1) return fail(FX_ERR_INVALID_ARG, "n_layers must be >= 1");
+    if (k < 0 || (k > 0 && !idx)) return fail(FX_ERR_INVALID_ARG, "need k >= 0 and idx when k > 0");
+    if (tail_lo < 0) return fail(FX_ERR_INVALID_ARG, "tail_lo must be >= 0");
+    if (!row_stride_ok(src_stride_layer) || !row_stride_ok(dst_stride_layer))
+        return fail(FX_ERR_INVALID_ARG, "layer strides must be non-negative multiples of 8 elements");
+    if ((int64_t)src->B * n_layers > 65535 || src->Hkv > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
+
+    CompactParams p;
+    p.sk = src->k;
+    p.sv = src->v;
+    p.len = src->len;
+    p.sb = src->stride_b;
+    p.sh = src->stride_h;
+    p.st = src->stride_t;
+    p.s_layer = src_stride_layer;
+    p.B = src->B;
+    p.Hkv = src->Hkv;
+    p.Tcap = src->Tcap;
+    p.idx = k > 0 ? idx : nullptr;
+    p.kk = k;
+    p.tail_lo = tail_lo;
+    p.dk = dst->k;
+    p.dv = dst->v;
+    p.dlen = dst->len;
+    p.db = dst->stride_b;
+    p.dh = dst->stride_h;
+    p.dt = dst->stride_t;
+    p.d_layer = dst_stride_layer;
+    p.dcap = dst->Tcap;
+    p.n_layers = n_layers;
+    const int max_rows = k + (src->Tcap > tail_lo ? src->Tcap - tail_lo : 0);
+    p.max_rows = max_rows < dst->Tcap ? max_rows : dst->Tcap;
+    p.err = ds->err;
+    cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "compaction launch");
+    return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np, int max_suffix)
+{
+    if (Br < 1 || Hkv < 1 || Hq < Hkv || Mq < 1 || np < 0 || max_suffix < 0) return 0;
+    const int R = (Hq / Hkv) * Mq;
+    const int max_keys = np + max_suffix + Mq;
+    const Plan pl = make_plan(Br * Hkv, R, max_keys, sm_count_or_default());
+    return make_layout(Br * Hkv, R, pl, 0, true).total;
+}
+
+fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_desc* br,
+                                  const fx_bf16* q, int Hq, const int32_t* prefix_idx, int kp,
+                                  float scale, float* out, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!prefix || !br) return fail(FX_ERR_INVALID_ARG, "prefix and branches must be non-NULL");
+    if (prefix->d != kHeadDim) return fail(FX_ERR_UNSUPPORTED, "head dim %d (only 128 is implemented)", prefix->d);
+    if (prefix->P < 0 || prefix->Hkv < 1) return fail(FX_ERR_INVALID_ARG, "need P >= 0 and Hkv >= 1");
+    if (prefix->P > 0 && (!prefix->k || !prefix->v)) return fail(FX_ERR_INVALID_ARG, "prefix k/v are NULL");
+    if (!aligned16(prefix->k) || !aligned16(prefix->v) || !row_stride_ok(prefix->stride_h) ||
+        !row_stride_ok(prefix->stride_t))
+        return fail(FX_ERR_INVALID_ARG, "prefix rows must be 16-byte aligned (strides multiples of 8)");
+    if (br->Br < 1 || br->Mq < 1) return fail(FX_ERR_INVALID_ARG, "need Br >= 1 and Mq >= 1");
+    if (!br->suf_off) return fail(FX_ERR_INVALID_ARG, "suf_off is NULL");
+    if (br->suf_rows < 0 || br->max_suffix < 0) return fail(FX_ERR_INVALID_ARG, "need suf_rows, max_suffix >= 0");
+    if (br->suf_rows > 0 && (!br->suf_k || !br->suf_v)) return fail(FX_ERR_INVALID_ARG, "suffix k/v are NULL");
+    if (!aligned16(br->suf_k) || !aligned16(br->suf_v) || !row_stride_ok(br->suf_stride_h) ||
+        !row_stride_ok(br->suf_stride_t))
+        return fail(FX_ERR_INVALID_ARG, "suffix rows must be 16-byte aligned (strides multiples of 8)");
+    if (!br->draft_k || !br->draft_v || !aligned16(br->draft_k) || !aligned16(br->draft_v) ||
+        !row_stride_ok(br->draft_stride_b) || !row_stride_ok(br->draft_stride_i) || !row_stride_ok(br->draft_stride_h))
+        return fail(FX_ERR_INVALID_ARG, "draft rows must be non-NULL and 16-byte aligned");
+    fx_status st = check_heads(Hq, prefix->Hkv, br->Mq);
+    if (st != FX_OK) return st;
+    if (!q || !aligned16(q)) return fail(FX_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+    if (!out) return fail(FX_ERR_INVALID_ARG, "out is NULL");
+    if (prefix_idx && kp < 0) return fail(FX_ERR_INVALID_ARG, "kp must be >= 0");
+    if (!isfinite(scale)) return fail(FX_ERR_INVALID_ARG, "scale must be finite");
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
+
+    const int Hkv = prefix->Hkv;
+    const int pairs = br->Br * Hkv;
+    const int G = Hq / Hkv;
+    const int R = G * br->Mq;
+    const int np = prefix_idx ? kp : prefix->P;
+    const int max_keys = np + br->max_suffix + br->Mq;
+    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count);
+    const Layout L = make_layout(pairs, R, pl, 0, true);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
+    if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
+
+    char* w = static_cast<char*>(ws);
+    AttnParams p;
+    memset(&p, 0, sizeof p);
+    p.k = prefix->k;
+    p.v = prefix->v;
+    p.sb = 0;
+    p.sh = prefix->stride_h;
+    p.st = prefix->stride_t;
+    p.B = br->Br;
+    p.Hkv = Hkv;
+    p.Tcap = prefix->P;
+    p.q = q;
+    p.Hq = Hq;
+    p.G = G;
+    p.Mq = br->Mq;
+    p.R = R;
+    p.q_pos0 = -1;
+    p.qscale = log2e_scale(scale);
+    p.idx = prefix_idx;
+    p.kk = prefix_idx ? kp : 0;
+    p.P = prefix->P;
+    p.suf_k = br->suf_k;
+    p.suf_v = br->suf_v;
+    p.suf_sh = br->suf_stride_h;
+    p.suf_st = br->suf_stride_t;
+    p.suf_off = br->suf_off;
+    p.suf_rows = br->suf_rows;
+    p.max_suffix = br->max_suffix;
+    p.dr_k = br->draft_k;
+    p.dr_v = br->draft_v;
+    p.dr_sb = br->draft_stride_b;
+    p.dr_si = br->draft_stride_i;
+    p.dr_sh = br->draft_stride_h;
+    p.nsplit = pl.nsplit;
+    p.split_len = pl.split_len;
+    p.nrg = pl.nrg;
+    p.part_m = reinterpret_cast<float*>(w + L.part_m);
+    p.part_l = reinterpret_cast<float*>(w + L.part_l);
+    p.part_o = reinterpret_cast<float*>(w + L.part_o);
+    p.counters = reinterpret_cast<unsigned*>(w + L.counters);
+    p.out = out;
+    p.err = ds->err;
+    cudaError_t e = launch_attn_partial(p, kModePrefix, pl.rb, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix decode launch");
+    return FX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,251 @@
+// Deterministic top-k per row for sm_103a: one CTA per row, radix select on the float bits.
+//
+// Order: score descending, index ascending (FastOCR, Focal-Guided Pruning: the top-attended tokens;
+// ties go to the lower index).  Each fp32 score maps to a uint32 key that orders like the float.
+// Four 8-bit radix passes find K*, the k-th largest key, and how many keys equal to K* must be taken
+// (need_eq).  A final ordered pass -- tiles of 1024 scores, one per thread, with a block-wide
+// exclusive scan of (greater, equal) counts -- writes every index with key > K* and the first need_eq
+// indices with key == K*, in ascending index order.  No atomics decide the output, so the result is
+// bit-reproducible.
+//
+// Warm start (FastOCR, Cross-Step Fixation Reuse): with the previous set S_prev, the threshold
+// T = min over S_prev of the current scores is exceeded-or-met by at least k entries, so the top-k
+// lies in {score >= T}; the radix passes only count those candidates.  The result is unchanged.
+//
+// Rows up to kSmemKeys long are held in shared memory as keys; longer rows are re-read from global
+// memory (L2) on each pass.
+#include <stdint.h>
+
+#include "fx_internal.h"
+
+namespace fx {
+namespace {
+
+constexpr int kTkThreads = 1024;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kSmemKeys = 48 * 1024;   // 192 KB of keys
+
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <bool SMEM>
+__device__ __forceinline__ uint32_t get_key(const uint32_t* skeys, const float* src, int j)
+{
+    if (SMEM) return skeys[j];
+    return order_key(__ldg(src + j));
+}
+
+// Block-wide exclusive scan of one uint32 per thread; returns the exclusive prefix, *total = sum.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* swarp, uint32_t* total)
+{
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) swarp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = lane < kTkWarps ? swarp[lane] : 0u;
+        uint32_t winc = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, winc, o);
+            if (lane >= o) winc += t;
+        }
+        if (lane < kTkWarps) swarp[lane] = winc - w;   // exclusive warp offsets
+        if (lane == kTkWarps - 1) swarp[32] = winc;    // block total
+    }
+    __syncthreads();
+    const uint32_t res = swarp[warp] + inc - v;
+    *total = swarp[32];
+    __syncthreads();
+    return res;
+}
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
+{
+    extern __shared__ uint32_t skeys[];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t swarp[33];
+    __shared__ uint32_t s_digit, s_gt, s_thr, s_bad;
+
+    const int row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int n = p.n;
+    const float* src = p.scores + (int64_t)row * n;
+
+    if (SMEM) {
+        for (int j = tid; j < n; j += kTkThreads) skeys[j] = order_key(src[j]);
+    }
+    if (tid == 0) {
+        s_thr = p.prev != nullptr ? 0xffffffffu : 0u;
+        s_bad = 0u;
+    }
+    __syncthreads();
+
+    // ---- warm-start threshold ----------------------------------------------------------------
+    uint32_t thr = 0u;
+    if (p.prev != nullptr) {
+        uint32_t kmin = 0xffffffffu;
+        const int32_t* prow = p.prev + (int64_t)row * p.k;
+        for (int i = tid; i < p.k; i += kTkThreads) {
+            const int t = prow[i];
+            if (t < 0 || t >= n)
+                s_bad = 1u;
+            else
+                kmin = min(kmin, get_key<SMEM>(skeys, src, t));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        if (lane == 0) atomicMin(&s_thr, kmin);
+        __syncthreads();
+        if (s_bad) {
+            if (tid == 0) atomicOr(p.err, FX_DEVERR_INDEX);
+        } else {
+            thr = s_thr;
+        }
+    }
+
+    // ---- radix select: K* and the number of equal keys to take --------------------------------
+    uint32_t prefix = 0u, pmask = 0u;
+    uint32_t krem = (uint32_t)p.k;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
+            __syncthreads();
+            for (int j0 = 0; j0 < n; j0 += kTkThreads) {
+                const int j = j0 + tid;   // whole warps iterate together (ballot/match below)
+                const uint32_t key = j < n ? get_key<SMEM>(skeys, src, j) : 0u;
+                const bool take = j < n && key >= thr && (key & pmask) == prefix;
+                const unsigned active = __ballot_sync(0xffffffffu, take);
+                if (take) {
+                    const uint32_t digit = (key >> shift) & 255u;
+                    const unsigned peers = __match_any_sync(active, digit);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+                }
+            }
+            __syncthreads();
+            if (tid < 32) {
+                uint32_t loc[8];
+                uint32_t tot = 0u;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    loc[e] = hist[8 * tid + e];
+                    tot += loc[e];
+                }
+                uint32_t inc = tot;   // inclusive suffix sum over lanes >= tid
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t t = __shfl_down_sync(0xffffffffu, inc, o);
+                    if (tid + o < 32) inc += t;
+                }
+                const uint32_t all = __shfl_sync(0xffffffffu, inc, 0);
+                uint32_t run = inc - tot;   // count of digits above this lane's bins
+                int found = -1;
+                uint32_t gt = 0u;
+#pragma unroll
+                for (int e = 7; e >= 0; --e) {
+                    const uint32_t before = run;
+                    run += loc[e];
+                    if (found < 0 && run >= krem && before < krem) {
+                        found = 8 * tid + e;
+                        gt = before;
+                    }
+                }
+                if (found >= 0) {
+                    s_digit = (uint32_t)found;
+                    s_gt = gt;
+                }
+                if (tid == 0 && all < krem) s_digit = 0xffffffffu;  // fewer candidates than needed
+            }
+            __syncthreads();
+            if (s_digit == 0xffffffffu && thr != 0u) {
+                // only possible in pass 0 with a warm-start threshold built from repeated indices:
+                // drop the threshold and count again
+                thr = 0u;
+                __syncthreads();
+                continue;
+            }
+            break;
+        }
+        const bool missing = (s_digit == 0xffffffffu);
+        __syncthreads();
+        if (missing) {
+            // unreachable for 1 <= k <= n (checked on the host); keep the kernel finite anyway
+            if (tid == 0) {
+                atomicOr(p.err, FX_DEVERR_INDEX);
+                s_digit = 0u;
+                s_gt = 0u;
+            }
+            __syncthreads();
+        }
+        prefix |= s_digit << shift;
+        pmask |= 255u << shift;
+        krem -= s_gt;
+        __syncthreads();
+    }
+    const uint32_t kstar = prefix;
+    const uint32_t need_eq = krem;
+
+    // ---- ordered output -------------------------------------------------------------------------
+    int32_t* orow = p.out + (int64_t)row * p.k;
+    uint32_t base_g = 0u, base_e = 0u;
+    for (int t0 = 0; t0 < n; t0 += kTkThreads) {
+        const int j = t0 + tid;
+        uint32_t key = 0u;
+        uint32_t g = 0u, e = 0u;
+        if (j < n) {
+            key = get_key<SMEM>(skeys, src, j);
+            g = key > kstar ? 1u : 0u;
+            e = key == kstar ? 1u : 0u;
+        }
+        uint32_t total;
+        const uint32_t ex = block_exclusive_scan(g | (e << 16), swarp, &total);
+        const uint32_t gc = base_g + (ex & 0xffffu);
+        const uint32_t ec = base_e + (ex >> 16);
+        // positions are < k by construction; the bound check keeps a logic slip from writing past the row
+        if (g) {
+            const uint32_t pos = gc + min(ec, need_eq);
+            if (pos < (uint32_t)p.k) orow[pos] = j;
+        } else if (e && ec < need_eq) {
+            const uint32_t pos = gc + ec;
+            if (pos < (uint32_t)p.k) orow[pos] = j;
+        }
+        base_g += total & 0xffffu;
+        base_e += total >> 16;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s)
+{
+    if (p.n <= kSmemKeys) {
+        const size_t smem = (size_t)p.n * sizeof(uint32_t);
+        static int configured_device = -1;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (configured_device != dev) {
+            cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemKeys * (int)sizeof(uint32_t));
+            if (e != cudaSuccess) return e;
+            configured_device = dev;
+        }
+        topk_kernel<true><<<p.rows, kTkThreads, smem, s>>>(p);
+    } else {
+        topk_kernel<false><<<p.rows, kTkThreads, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fx

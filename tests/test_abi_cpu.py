@@ -1,0 +1,80 @@
+"""The C ABI library builds, loads and exports every entry point declared in include/fx.h; host-side
+argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fx.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^FX_API\s+[\w\s\*]+?\b(fx_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from kv_cache_token_fx_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("fx_focal_attn_scores", "fx_topk_select", "fx_sparse_gqa_decode", "fx_kv_compact",
+              "fx_shared_prefix_decode"):
+        assert n in names
+    assert len(names) >= 12
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_argument_checks_without_gpu(lib):
+    lib.fx_last_error.restype = ctypes.c_char_p
+    lib.fx_abi_version.restype = ctypes.c_int
+    assert lib.fx_abi_version() == 1
+    lib.fx_topk_select.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.fx_topk_select(None, 1, 4, 2, None, None, None) == 1
+    assert b"non-NULL" in lib.fx_last_error()
+    fake = ctypes.c_void_p(256)
+    assert lib.fx_topk_select(fake, 1, 4, 5, None, fake, None) == 1       # k > n
+    assert b"k (5) <= n (4)" in lib.fx_last_error()
+    lib.fx_focal_attn_scores.restype = ctypes.c_int
+    assert lib.fx_focal_attn_scores(None, None, 1, 1, -1, ctypes.c_float(1.0), 0, 0, None, None, None,
+                                    ctypes.c_size_t(0), None) == 1
+    lib.fx_sparse_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) > 0
+    assert lib.fx_sparse_workspace_bytes(0, 8, 16, 205, 4096, 4864) == 0
+    lib.fx_focal_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.fx_focal_workspace_bytes(8, 8, 16, 1, 4864) >= 8 * 8 * 2 * 4864 * 4
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import kv_cache_token_fx_gb300 as fx
+    try:
+        fx.load_library()
+    except fx.FxError:
+        pytest.skip("library not built")
+    with pytest.raises(fx.FxError):
+        fx.fx_topk_select(torch.zeros((2, 8)), 3)
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "kv_cache_token_fx_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cuh", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\boracle\b", text.replace("oracle-free", "")) or f.endswith(".md"), \
+                    f"{f} mentions the oracle"
