@@ -201,7 +201,7 @@ FX_API fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, 
  *       ++ the branch's suffix rows ++ the branch's draft rows 0..i         (causal inside the draft)
  *   out[b, h*G+gi, i, :] = sum_{j in S} softmax_S(scale * q . k_j) v_j
  *
- *   prefix      rows (h, t) at k + h*stride_h + t*stride_t, t < P
+ *   prefix      rows (h, t) at k + h*stride_h + t*stride_t, t < P (k and v non-NULL even when P == 0)
  *   suffix      rows (h, t) at suf_k + h*suf_stride_h + t*suf_stride_t, t < suf_rows
  *   suf_off     device [Br + 1] int32, non-decreasing, suf_off[Br] <= suf_rows; max_suffix bounds
  *               every suf_off[b+1] - suf_off[b] (longer suffixes set FX_DEVERR_OFFSETS and are cut)

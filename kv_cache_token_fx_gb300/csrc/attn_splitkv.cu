@@ -1,17 +1,21 @@
 // Split-KV decode attention on CUDA cores for sm_103a.
 //
 // One CTA = (row group of up to RB query rows, one split of the key sequence, one (b, KV head)).
-// Each warp walks chunks of 2*TPC keys; within a chunk a half-warp owns one key per step: lane
-// `sub` (0..15) loads 16 bytes (8 bf16 of the 128-wide row) of K and of V with one vectorised
-// load each, so a warp instruction moves two full 256-byte rows.  Logits are reduced over the 16
-// lanes with xor shuffles, the softmax is kept online in base-2 units (q is pre-scaled by
-// scale*log2(e)), and V is accumulated straight from registers: K/V bytes are touched exactly once
-// and never staged.  Partial (max, sum, unnormalised output) triples per split go to the
-// workspace; the sparse/prefix modes merge them in the last-arriving CTA of each (b, h, row group),
-// the focal mode in a separate combine kernel that also forms the per-token importance.
+// The split is walked in tiles of 64 keys.  Each tile's K and V rows (256 bytes each) are copied
+// into shared memory with 16-byte cp.async operations -- contiguous rows for the focal mode,
+// gathered rows for the sparse and prefix modes -- two tiles in flight at once, so every byte a CTA
+// needs is requested before the first one is used.  Rows that must not be read (past the split, or a
+// rejected index) are zero-filled by the copy itself.  Each warp then takes 16 keys of the tile: a
+// half-warp owns one key per step, lane `sub` holding dims [8*sub, 8*sub+8) (conflict-free 16-byte
+// shared loads), the dot products are reduced over the 16 lanes with xor shuffles, and the softmax
+// is kept online in base-2 units (q is pre-scaled by scale*log2(e)).  Partial (max, sum,
+// unnormalised output) triples per split go to the workspace; the sparse/prefix modes merge them in
+// the last-arriving CTA of each (b, h, row group), the focal mode in a separate combine kernel that
+// also forms the per-token importance from the stored logits.
 //
 // Attention and importance follow FastOCR (Methodology: Focal-Guided Pruning): focal layers attend
-// over the full cache, the rest over the selected set; FastKV (2.A) for the causal query window.
+// over the full cache, the rest over the selected set; FastKV (2.A) for the causal query window;
+// HPD-Parsing (parts 2 and 3) for the shared prefix + private suffix + causal draft sequence.
 #include <math.h>
 
 #include "fx_internal.h"
@@ -20,15 +24,6 @@ namespace fx {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ uint4 ld_stream16(const uint16_t* ptr)
-{
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(ptr));
-    return r;
-}
 
 __device__ __forceinline__ void unpack8(const uint4& w, float f[8])
 {
@@ -43,16 +38,89 @@ __device__ __forceinline__ void unpack8(const uint4& w, float f[8])
     f[7] = __uint_as_float(w.w & 0xffff0000u);
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 __device__ __forceinline__ void flag(unsigned* err, unsigned bit) { atomicOr(err, bit); }
 
-template <int MODE, int RB>
-__global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams p)
-{
-    constexpr int TPC = (RB >= 8) ? 4 : 8;  // keys per half-warp per chunk
-    constexpr int CH = 2 * TPC;             // keys per warp per chunk
+// Where the rows of one (b, h) key sequence live.  Position pos of the sequence maps to one K row
+// and the V row at the same offset from the V base.
+template <int MODE>
+struct KeySource {
+    const uint16_t* kb;   // main cache / prefix base for this (b, h)
+    const uint16_t* vb;
+    int64_t st;
+    int kk;               // gathered positions (sparse idx / prefix idx)
+    int tail_lo;          // sparse: tail start token
+    int np, L;            // prefix: prefix rows, suffix rows
+    const uint16_t* suf_k;
+    const uint16_t* suf_v;
+    int64_t suf_st;
+    const uint16_t* dr_k;
+    const uint16_t* dr_v;
+    int64_t dr_si;
+    bool gathered;        // prefix positions come from s_tok
+    int s0;
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    // element offset of the row of sequence position `pos` relative to the matching base, and which
+    // base to use (0: main, 1: suffix, 2: draft); returns false when the row must not be read.
+    __device__ __forceinline__ bool row(int pos, const int* s_tok, const uint16_t*& kp, const uint16_t*& vp) const
+    {
+        if (MODE == kModeFocal) {
+            kp = kb + (int64_t)pos * st;
+            vp = vb + (int64_t)pos * st;
+            return true;
+        }
+        if (MODE == kModeSparse) {
+            int t;
+            if (pos < kk) {
+                t = s_tok[pos - s0];
+                if (t < 0) return false;
+            } else {
+                t = tail_lo + (pos - kk);
+            }
+            kp = kb + (int64_t)t * st;
+            vp = vb + (int64_t)t * st;
+            return true;
+        }
+        if (pos < np) {
+            int t = pos;
+            if (gathered) {
+                t = s_tok[pos - s0];
+                if (t < 0) return false;
+            }
+            kp = kb + (int64_t)t * st;
+            vp = vb + (int64_t)t * st;
+        } else if (pos < np + L) {
+            const int64_t o = (int64_t)(pos - np) * suf_st;
+            kp = suf_k + o;
+            vp = suf_v + o;
+        } else {
+            const int64_t o = (int64_t)(pos - np - L) * dr_si;
+            kp = dr_k + o;
+            vp = dr_v + o;
+        }
+        return true;
+    }
+};
+
+template <int MODE, int RB>
+__global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
+{
+    constexpr int TPC = kTile / (2 * kWarps);   // keys per half-warp per tile (8)
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint16_t* sdata = reinterpret_cast<uint16_t*>(smem_raw);
+    int* s_tok = reinterpret_cast<int*>(smem_raw + kStageBytes * kStages);
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
     const int hw = lane >> 4;
     const int sub = lane & 15;
     const int rg = blockIdx.x;
@@ -63,35 +131,86 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
     const int r0 = rg * RB;
 
     // ---- key sequence of this (b, h) ----------------------------------------------------------
+    KeySource<MODE> src;
     int n_keys;
-    int lenb = 0, np = 0, L = 0, soff = 0;
+    src.kb = p.k + (int64_t)b * p.sb + (int64_t)h * p.sh;
+    src.vb = p.v + (int64_t)b * p.sb + (int64_t)h * p.sh;
+    src.st = p.st;
+    src.kk = p.kk;
+    src.tail_lo = p.tail_lo;
+    src.gathered = p.idx != nullptr;
+    src.np = 0;
+    src.L = 0;
     if (MODE == kModeFocal || MODE == kModeSparse) {
         int l = p.len[b];
         if (l < 0 || l > p.Tcap) {
-            if (threadIdx.x == 0) flag(p.err, FX_DEVERR_LEN);
+            if (tid == 0) flag(p.err, FX_DEVERR_LEN);
             l = l < 0 ? 0 : p.Tcap;
         }
-        lenb = l;
-        n_keys = (MODE == kModeFocal) ? lenb : p.kk + max(0, lenb - p.tail_lo);
+        n_keys = (MODE == kModeFocal) ? l : p.kk + max(0, l - p.tail_lo);
+        src.np = l;   // sparse: valid token range [0, len) for the gathered indices
     } else {
-        np = p.idx ? p.kk : p.P;
+        src.np = p.idx ? p.kk : p.P;
         const int o0 = p.suf_off[b];
         const int o1 = p.suf_off[b + 1];
+        int L = 0;
         if (o0 < 0 || o1 < o0 || o1 > p.suf_rows) {
-            if (threadIdx.x == 0) flag(p.err, FX_DEVERR_OFFSETS);
-            L = 0;
+            if (tid == 0) flag(p.err, FX_DEVERR_OFFSETS);
         } else {
             L = o1 - o0;
             if (L > p.max_suffix) {
-                if (threadIdx.x == 0) flag(p.err, FX_DEVERR_OFFSETS);
+                if (tid == 0) flag(p.err, FX_DEVERR_OFFSETS);
                 L = p.max_suffix;
             }
         }
-        soff = o0;
-        n_keys = np + L + p.Mq;
+        src.L = L;
+        src.suf_k = p.suf_k + (int64_t)h * p.suf_sh + (int64_t)(L > 0 ? o0 : 0) * p.suf_st;
+        src.suf_v = p.suf_v + (int64_t)h * p.suf_sh + (int64_t)(L > 0 ? o0 : 0) * p.suf_st;
+        src.suf_st = p.suf_st;
+        src.dr_k = p.dr_k + (int64_t)b * p.dr_sb + (int64_t)h * p.dr_sh;
+        src.dr_v = p.dr_v + (int64_t)b * p.dr_sb + (int64_t)h * p.dr_sh;
+        src.dr_si = p.dr_si;
+        n_keys = src.np + L + p.Mq;
     }
     const int s0 = split * p.split_len;
     const int s1 = min(n_keys, s0 + p.split_len);
+    src.s0 = s0;
+    const int ntiles = s1 > s0 ? (s1 - s0 + kTile - 1) / kTile : 0;
+
+    // gathered token positions of this split, checked once
+    if (MODE != kModeFocal && p.idx != nullptr) {
+        const int32_t* irow = p.idx + (int64_t)bh * p.kk;
+        const int lim_tok = (MODE == kModeSparse) ? src.np : p.P;
+        const int hi = min(s1, p.kk);
+        for (int pos = s0 + tid; pos < hi; pos += kThreads) {
+            int t = __ldg(irow + pos);
+            if (t < 0 || t >= lim_tok) {
+                flag(p.err, FX_DEVERR_INDEX);
+                t = -1;
+            }
+            s_tok[pos - s0] = t;
+        }
+        __syncthreads();
+    }
+
+    // ---- tile loader: thread copies 16-byte chunk `sub` of rows (tid >> 4) + 8u, K and V ----------
+    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sdata);
+    auto issue = [&](int tile, int stage) {
+        const int base = s0 + tile * kTile;
+#pragma unroll
+        for (int u = 0; u < kTile / 8; ++u) {
+            const int r = (tid >> 4) + 8 * u;
+            const int pos = base + r;
+            const uint16_t* kp = src.kb;
+            const uint16_t* vp = src.vb;
+            const bool ok = pos < s1 && src.row(pos, s_tok, kp, vp);
+            const uint32_t dk = sbase + (uint32_t)(((stage * 2 + 0) * kTile + r) * kRowBytes + sub * 16);
+            const uint32_t dv = sbase + (uint32_t)(((stage * 2 + 1) * kTile + r) * kRowBytes + sub * 16);
+            cp_async16(dk, ok ? (const void*)(kp + sub * 8) : (const void*)src.kb, ok ? 16 : 0);
+            cp_async16(dv, ok ? (const void*)(vp + sub * 8) : (const void*)src.vb, ok ? 16 : 0);
+        }
+        cp_async_commit();
+    };
 
     // ---- query rows: lane `sub` holds dims [8*sub, 8*sub+8) of each row ------------------------
     float qf[RB][8];
@@ -102,8 +221,7 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
         if (row < p.R) {
             const int gi = row / p.Mq;
             const int i = row - gi * p.Mq;
-            const uint16_t* qp =
-                p.q + ((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + sub * 8;
+            const uint16_t* qp = p.q + ((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + sub * 8;
             const uint4 w = *reinterpret_cast<const uint4*>(qp);
             unpack8(w, qf[r]);
 #pragma unroll
@@ -111,19 +229,15 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
             if (MODE == kModeFocal)
                 lim[r] = p.q_pos0 >= 0 ? p.q_pos0 + i : 0x7fffffff;
             else if (MODE == kModePrefix)
-                lim[r] = np + L + i;   // draft row j is visible iff j <= i
+                lim[r] = src.np + src.L + i;   // draft row j is visible iff j <= i
             else
                 lim[r] = 0x7fffffff;
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[r][e] = 0.f;
-            lim[r] = -1;                // padding row: sees nothing
+            lim[r] = -1;   // padding row: sees nothing
         }
     }
-
-    const uint16_t* kb = p.k + (int64_t)b * p.sb + (int64_t)h * p.sh;
-    const uint16_t* vb = p.v + (int64_t)b * p.sb + (int64_t)h * p.sh;
-    const int32_t* idxrow = p.idx ? p.idx + (int64_t)bh * p.kk : nullptr;
 
     float m[RB], l[RB], o[RB][8];
 #pragma unroll
@@ -134,75 +248,34 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
         for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
     }
 
-    for (int cbase = s0 + warp * CH; cbase < s1; cbase += kWarps * CH) {
-        // gathered token positions of this chunk, one per lane, broadcast below
-        int myidx = 0;
-        if (MODE != kModeFocal && idxrow != nullptr) {
-            const int pp = cbase + lane;
-            if (lane < CH && pp < s1 && pp < p.kk) myidx = __ldg(idxrow + pp);
-        }
+    if (ntiles > 0) issue(0, 0);
+    if (ntiles > 1) issue(1, 1);
 
-        uint4 kr[TPC], vr[TPC];
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int stage = tile & 1;
+        if (tile + 1 < ntiles)
+            cp_async_wait_all_but_one();
+        else
+            cp_async_wait_all();
+        __syncthreads();
+
+        const int base = s0 + tile * kTile;
+        const uint16_t* sK = sdata + (size_t)(stage * 2 + 0) * kTile * kHeadDim;
+        const uint16_t* sV = sdata + (size_t)(stage * 2 + 1) * kTile * kHeadDim;
+
+        float lg[TPC][RB];
         bool valid[TPC];
         int pos[TPC];
 #pragma unroll
         for (int i = 0; i < TPC; ++i) {
-            pos[i] = cbase + 2 * i + hw;
-            const int tsrc = __shfl_sync(kFull, myidx, 2 * i + hw);
+            const int row = warp * (2 * TPC) + 2 * i + hw;
+            pos[i] = base + row;
             bool ok = pos[i] < s1;
-            const uint16_t* kp = kb;
-            const uint16_t* vp = vb;
-            if (MODE == kModeFocal) {
-                kp = kb + (int64_t)pos[i] * p.st;
-                vp = vb + (int64_t)pos[i] * p.st;
-            } else if (MODE == kModeSparse) {
-                int t;
-                if (pos[i] < p.kk) {
-                    t = tsrc;
-                    if (ok && (t < 0 || t >= lenb)) {
-                        flag(p.err, FX_DEVERR_INDEX);
-                        ok = false;
-                    }
-                } else {
-                    t = p.tail_lo + (pos[i] - p.kk);
-                }
-                kp = kb + (int64_t)t * p.st;
-                vp = vb + (int64_t)t * p.st;
-            } else {
-                if (pos[i] < np) {
-                    int t = idxrow ? tsrc : pos[i];
-                    if (ok && idxrow && (t < 0 || t >= p.P)) {
-                        flag(p.err, FX_DEVERR_INDEX);
-                        ok = false;
-                    }
-                    kp = kb + (int64_t)t * p.st;
-                    vp = vb + (int64_t)t * p.st;
-                } else if (pos[i] < np + L) {
-                    const int64_t t = soff + (pos[i] - np);
-                    kp = p.suf_k + (int64_t)h * p.suf_sh + t * p.suf_st;
-                    vp = p.suf_v + (int64_t)h * p.suf_sh + t * p.suf_st;
-                } else {
-                    const int64_t j = pos[i] - np - L;
-                    kp = p.dr_k + (int64_t)b * p.dr_sb + j * p.dr_si + (int64_t)h * p.dr_sh;
-                    vp = p.dr_v + (int64_t)b * p.dr_sb + j * p.dr_si + (int64_t)h * p.dr_sh;
-                }
-            }
+            if (MODE == kModeSparse && ok && pos[i] < p.kk) ok = s_tok[pos[i] - s0] >= 0;
+            if (MODE == kModePrefix && ok && src.gathered && pos[i] < src.np) ok = s_tok[pos[i] - s0] >= 0;
             valid[i] = ok;
-            if (ok) {
-                kr[i] = ld_stream16(kp + sub * 8);
-                vr[i] = ld_stream16(vp + sub * 8);
-            } else {
-                kr[i] = make_uint4(0u, 0u, 0u, 0u);
-                vr[i] = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-
-        // logits (base 2), reduced over the 16 lanes of each half-warp
-        float lg[TPC][RB];
-#pragma unroll
-        for (int i = 0; i < TPC; ++i) {
             float kf[8];
-            unpack8(kr[i], kf);
+            unpack8(*reinterpret_cast<const uint4*>(sK + row * kHeadDim + sub * 8), kf);
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
                 float s = 0.f;
@@ -212,12 +285,12 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
                 s += __shfl_xor_sync(kFull, s, 4);
                 s += __shfl_xor_sync(kFull, s, 2);
                 s += __shfl_xor_sync(kFull, s, 1);
-                lg[i][r] = (valid[i] && pos[i] <= lim[r]) ? s : -INFINITY;
+                lg[i][r] = (ok && pos[i] <= lim[r]) ? s : -INFINITY;
             }
         }
 
         if (MODE == kModeFocal && p.logits != nullptr) {
-            const int pp = cbase + 2 * sub + hw;
+            const int pp = base + warp * (2 * TPC) + 2 * sub + hw;
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
                 if (r0 + r < p.R) {
@@ -225,8 +298,7 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
 #pragma unroll
                     for (int i = 1; i < TPC; ++i)
                         if (sub == i) mine = lg[i][r];
-                    if (sub < TPC && pp < s1)
-                        p.logits[(int64_t)(bh * p.R + r0 + r) * p.Tcap + pp] = mine;
+                    if (sub < TPC && pp < s1) p.logits[(int64_t)(bh * p.R + r0 + r) * p.Tcap + pp] = mine;
                 }
             }
         }
@@ -253,13 +325,16 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
         }
 #pragma unroll
         for (int i = 0; i < TPC; ++i) {
+            const int row = warp * (2 * TPC) + 2 * i + hw;
             float vf[8];
-            unpack8(vr[i], vf);
+            unpack8(*reinterpret_cast<const uint4*>(sV + row * kHeadDim + sub * 8), vf);
 #pragma unroll
             for (int r = 0; r < RB; ++r)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[r][e] = fmaf(lg[i][r], vf[e], o[r][e]);
         }
+        __syncthreads();                       // every warp is done with this stage
+        if (tile + 2 < ntiles) issue(tile + 2, stage);
     }
 
     // the two half-warps hold the same dims for different keys
@@ -270,14 +345,14 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
         for (int e = 0; e < 8; ++e) o[r][e] += __shfl_xor_sync(kFull, o[r][e], 16);
     }
 
-    // ---- combine the warps of this CTA into one partial per row -------------------------------
+    // ---- combine the warps of this CTA into one partial per row (tile buffers are free now) ----
     __shared__ float sm_m[kWarps][RB];
     __shared__ float sm_l[kWarps][RB];
-    __shared__ __align__(16) float sm_o[kWarps][RB][kHeadDim];
+    float* sm_o = reinterpret_cast<float*>(smem_raw);   // [kWarps][RB][128]
     if (lane < 16) {
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
-            float4* dst = reinterpret_cast<float4*>(&sm_o[warp][r][sub * 8]);
+            float4* dst = reinterpret_cast<float4*>(sm_o + (warp * RB + r) * kHeadDim + sub * 8);
             dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
             dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
         }
@@ -291,7 +366,6 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
     }
     __syncthreads();
 
-    const int tid = threadIdx.x;  // == output dim
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
         const int row = r0 + r;
@@ -305,7 +379,7 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(const AttnParams
         for (int w = 0; w < kWarps; ++w) {
             const float sc = exp2f(sm_m[w][r] - Ms);
             Ls = fmaf(sm_l[w][r], sc, Ls);
-            O = fmaf(sm_o[w][r][tid], sc, O);
+            O = fmaf(sm_o[(w * RB + r) * kHeadDim + tid], sc, O);
         }
         const int64_t pi = (int64_t)(bh * p.R + row) * p.nsplit + split;
         p.part_o[pi * kHeadDim + tid] = O;
@@ -402,17 +476,33 @@ __global__ void __launch_bounds__(256) focal_combine_kernel(const FocalCombinePa
     }
 }
 
+template <int MODE, int RB>
+cudaError_t launch_one(const AttnParams& p, size_t smem, cudaStream_t s)
+{
+    static int configured = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured != dev) {
+        cudaError_t e = cudaFuncSetAttribute(attn_tile_kernel<MODE, RB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)attn_smem_bytes(kMaxSplitTokens));
+        if (e != cudaSuccess) return e;
+        configured = dev;
+    }
+    dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
+    attn_tile_kernel<MODE, RB><<<grid, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
 template <int MODE>
 cudaError_t launch_mode(const AttnParams& p, int rb, cudaStream_t s)
 {
-    dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
+    const size_t smem = attn_smem_bytes((MODE != kModeFocal && p.idx != nullptr) ? p.split_len : 0);
     switch (rb) {
-    case 1: attn_partial_kernel<MODE, 1><<<grid, kThreads, 0, s>>>(p); break;
-    case 2: attn_partial_kernel<MODE, 2><<<grid, kThreads, 0, s>>>(p); break;
-    case 4: attn_partial_kernel<MODE, 4><<<grid, kThreads, 0, s>>>(p); break;
-    default: attn_partial_kernel<MODE, 8><<<grid, kThreads, 0, s>>>(p); break;
+    case 1: return launch_one<MODE, 1>(p, smem, s);
+    case 2: return launch_one<MODE, 2>(p, smem, s);
+    case 4: return launch_one<MODE, 4>(p, smem, s);
+    default: return launch_one<MODE, 8>(p, smem, s);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

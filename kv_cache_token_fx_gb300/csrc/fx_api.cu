@@ -86,11 +86,12 @@ Plan make_plan(int pairs, int R, int max_keys, int sm_count)
     pl.rb = rows_per_block(R);
     pl.nrg = cdiv(R, pl.rb);
     const int per_split = pairs * pl.nrg;
-    const int target = 4 * sm_count;                  // about 4 resident CTAs per SM in one wave
-    int ns = cdiv(target, per_split);
-    ns = ns > cdiv(max_keys, 4096) ? ns : cdiv(max_keys, 4096);   // at most 4096 keys per split
-    const int cap = max_keys / 64 > 1 ? max_keys / 64 : 1;        // at least ~64 keys per split
-    if (ns > cap) ns = cap;
+    const int resident = kCtasPerSm * sm_count;           // one full wave of attention CTAs
+    int ns = per_split >= resident ? 1 : resident / per_split;
+    const int min_ns = cdiv(max_keys > 0 ? max_keys : 1, kMaxSplitTokens);
+    if (ns < min_ns) ns = min_ns;
+    const int max_ns = cdiv(max_keys > 0 ? max_keys : 1, 16);   // at least 16 keys per split
+    if (ns > max_ns) ns = max_ns;
     if (ns < 1) ns = 1;
     int len = cdiv(max_keys > 0 ? max_keys : 1, ns);
     len = cdiv(len, 16) * 16;
@@ -107,7 +108,11 @@ Layout make_layout(int pairs, int R, const Plan& pl, int tcap_for_logits, bool w
 {
     Layout L;
     const size_t P = (size_t)pairs * R * pl.nsplit;
-    size_t off = 0;
+    // every layout (even one that needs no counters) starts after the counter region, so a focal
+    // call sharing the workspace can never overwrite the sparse/prefix arrival counters
+    (void)with_counters;
+    L.counters = 0;
+    size_t off = kCounterBytes;
     L.part_m = off;
     off += round_up(P * sizeof(float));
     L.part_l = off;
@@ -116,8 +121,6 @@ Layout make_layout(int pairs, int R, const Plan& pl, int tcap_for_logits, bool w
     off += round_up(P * kHeadDim * sizeof(float));
     L.logits = off;
     off += round_up((size_t)pairs * R * (size_t)(tcap_for_logits > 0 ? tcap_for_logits : 0) * sizeof(float));
-    L.counters = off;
-    off += with_counters ? round_up((size_t)pairs * pl.nrg * sizeof(unsigned)) : 0;
     L.total = off;
     return L;
 }
@@ -444,7 +447,7 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     if (!prefix || !br) return fail(FX_ERR_INVALID_ARG, "prefix and branches must be non-NULL");
     if (prefix->d != kHeadDim) return fail(FX_ERR_UNSUPPORTED, "head dim %d (only 128 is implemented)", prefix->d);
     if (prefix->P < 0 || prefix->Hkv < 1) return fail(FX_ERR_INVALID_ARG, "need P >= 0 and Hkv >= 1");
-    if (prefix->P > 0 && (!prefix->k || !prefix->v)) return fail(FX_ERR_INVALID_ARG, "prefix k/v are NULL");
+    if (!prefix->k || !prefix->v) return fail(FX_ERR_INVALID_ARG, "prefix k/v are NULL");
     if (!aligned16(prefix->k) || !aligned16(prefix->v) || !row_stride_ok(prefix->stride_h) ||
         !row_stride_ok(prefix->stride_t))
         return fail(FX_ERR_INVALID_ARG, "prefix rows must be 16-byte aligned (strides multiples of 8)");

@@ -12,6 +12,22 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxRows = 64;   // G * Mq limit per KV head
 constexpr int kWarps = 4;      // warps per attention CTA
 constexpr int kThreads = 32 * kWarps;
+constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row
+constexpr int kTile = 64;                               // keys per shared-memory tile
+constexpr int kStages = 2;                              // tiles in flight per CTA
+constexpr int kStageBytes = 2 * kTile * kRowBytes;      // K and V of one tile (32 KB)
+constexpr int kMaxSplitTokens = 4096;                   // longest split (bounds the index table)
+constexpr int kCtasPerSm = 3;                           // resident attention CTAs per SM (smem-bound)
+// Arrival counters of the last-CTA merge live in a fixed region at the start of every workspace
+// (one slot per (b, h, row group); grid.z <= 65535 and at most 8 row groups), so no other data of
+// any call ever overlaps them and they stay zero between calls.
+constexpr size_t kCounterSlots = 65536u * 8u;
+constexpr size_t kCounterBytes = kCounterSlots * sizeof(unsigned);
+
+inline size_t attn_smem_bytes(int gathered_split_len)
+{
+    return (size_t)kStages * kStageBytes + (size_t)(gathered_split_len > 0 ? gathered_split_len : 0) * sizeof(int);
+}
 
 // Which key sequence an attention CTA walks.
 enum AttnMode : int {
