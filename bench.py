@@ -153,31 +153,6 @@ def _cudart():
     return None
 
 
-class RawEvent:
-    """A timing CUDA event driven through the runtime directly.  Recorded while a stream is being
-    captured, it becomes an event node of the graph (cudaEventRecordExternal), so each replay stamps
-    it on the device timeline around the kernel it brackets."""
-
-    def __init__(self, rt):
-        self.rt = rt
-        self.h = ctypes.c_void_p()
-        if rt.cudaEventCreate(ctypes.byref(self.h)) != 0:
-            raise RuntimeError("cudaEventCreate failed")
-
-    def record(self, stream):
-        flags = 1 if torch.cuda.is_current_stream_capturing() else 0
-        err = self.rt.cudaEventRecordWithFlags(self.h, ctypes.c_void_p(stream.cuda_stream), ctypes.c_uint(flags))
-        if err != 0:
-            raise RuntimeError(f"cudaEventRecordWithFlags failed ({err})")
-
-    def elapsed_time(self, end) -> float:
-        ms = ctypes.c_float()
-        err = self.rt.cudaEventElapsedTime(ctypes.byref(ms), self.h, end.h)
-        if err != 0:
-            raise RuntimeError(f"cudaEventElapsedTime failed ({err})")
-        return float(ms.value)
-
-
 def measured_hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -222,17 +197,20 @@ class OcrDecodeRun:
             self.Vnew_host = torch.stack([self.V[:, :, :, p] for p in pos]).cpu().pin_memory()
             self.O_host = torch.empty(self.O.shape, dtype=torch.float32).pin_memory()
         self.rt = _cudart()
-        self.graphs, self.graphs_e2e, self.events = {}, {}, {}
+        self.graphs, self.graphs_e2e, self.graphs_sparse, self.sparse_bytes = {}, {}, {}, {}
         self.launches_per_step = 0
 
-    # one decode step; `ev` collects (start, end, bytes) around every sparse-decode launch
-    def step(self, t: int, ev=None):
+    # one decode step; `only_sparse` replays just the sparse-decode launches of the step (used to time
+    # the dominant kernel on its own); `nbytes_out` collects the algorithmic bytes of each sparse launch
+    def step(self, t: int, only_sparse: bool = False, nbytes_out=None):
         fx, w = self.fx, self.w
         p = t % 2
         ln = self.lens[t]
         launches = 0
         for l in range(w.n_layers):
             if l in w.focal_layers:
+                if only_sparse:
+                    continue
                 fx.fx_focal_attn_scores(self.K[l], self.V[l], ln, self.Q[t, l], cand=(0, w.n_vis), out=self.O[l],
                                         scores=self.scores, ws=self.ws)
                 prev = self.sets[l][1 - p] if t > 0 else None
@@ -248,19 +226,13 @@ class OcrDecodeRun:
             n_keys = (w.k_keep + w.length_at(t) - w.n_vis) if sel is not None else w.length_at(t)
             nbytes = (w.B * w.Hkv * n_keys * ROW_BYTES + w.B * w.Hq * D * (2 + 4) +
                       (w.B * w.Hkv * w.k_keep * 4 if sel is not None else 0))
-            if ev is not None:
-                e0, e1 = RawEvent(self.rt), RawEvent(self.rt)
-                self._record(e0)
             fx.fx_sparse_gqa_decode(self.K[l], self.V[l], ln, self.Q[t, l], sel, w.n_vis if sel is not None else 0,
                                     out=self.O[l], ws=self.ws)
-            if ev is not None:
-                self._record(e1)
-                ev.append((e0, e1, nbytes))
+            if nbytes_out is not None:
+                nbytes_out.append(nbytes)
             launches += 1
-        self.launches_per_step = launches
-
-    def _record(self, e):
-        e.record(torch.cuda.current_stream())
+        if not only_sparse:
+            self.launches_per_step = launches
 
     def e2e_inputs(self, t: int):
         """Copy step t's inputs from pinned host memory (queries, new K/V row) into device memory."""
@@ -278,15 +250,19 @@ class OcrDecodeRun:
             if err != 0:
                 raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
 
-    def capture(self, with_events: bool):
+    def capture(self):
         s = torch.cuda.Stream(self.dev)
         for t in range(self.w.steps):
             g = torch.cuda.CUDAGraph()
-            ev = [] if with_events else None
             with torch.cuda.graph(g, stream=s):
-                self.step(t, ev)
+                self.step(t)
             self.graphs[t] = g
-            self.events[t] = ev
+            gs = torch.cuda.CUDAGraph()
+            nb = []
+            with torch.cuda.graph(gs, stream=s):
+                self.step(t, only_sparse=True, nbytes_out=nb)
+            self.graphs_sparse[t] = gs
+            self.sparse_bytes[t] = nb
             if self.with_e2e:
                 g2 = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g2, stream=s):
@@ -305,12 +281,7 @@ def run_fx(args, rank, local, ws):
     for t in range(2):
         run.step(t)
     torch.cuda.synchronize()
-    with_events = run.rt is not None
-    try:
-        run.capture(with_events)
-    except RuntimeError:
-        with_events = False
-        run.capture(False)
+    run.capture()
     torch.cuda.synchronize()
     if run.fx.fx_device_errors() != 0:
         raise RuntimeError("device error flag set during warm-up")
@@ -336,20 +307,21 @@ def run_fx(args, rank, local, ws):
     tokens = sum_over_ranks(float(w.B * len(steps)), ws)
     value = tokens / (ms_max / 1e3)
 
-    # dominant kernel: fx_sparse_gqa_decode, timed by the event nodes of the replayed graphs.  The
-    # event nodes of a graph keep the times of its latest replay, so each step's graph is read right
-    # after the timed region for the steps it covered (every step index appears at most once per lap).
-    kern_ms, kern_bytes, n_launch = 0.0, 0, 0
-    if with_events:
-        seen = set()
-        for t in steps[-w.steps:]:
-            if t in seen:
-                continue
-            seen.add(t)
-            for e0, e1, nb in run.events[t]:
-                kern_ms += e0.elapsed_time(e1)
-                kern_bytes += nb
-                n_launch += 1
+    # dominant kernel: fx_sparse_gqa_decode.  Its average launch duration comes from CUDA events around
+    # the replay of graphs that hold only the step's 26 sparse-decode launches (same pointers, same
+    # order), over the same steps as the timed region; inter-kernel gaps count against it.
+    for t in steps[:3]:
+        run.graphs_sparse[t].replay()
+    torch.cuda.synchronize()
+    ks, ke = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ks.record()
+    for t in steps:
+        run.graphs_sparse[t].replay()
+    ke.record()
+    torch.cuda.synchronize()
+    kern_ms = ks.elapsed_time(ke)
+    kern_bytes = sum(sum(run.sparse_bytes[t]) for t in steps)
+    n_launch = sum(len(run.sparse_bytes[t]) for t in steps)
     peak, peak_kind = measured_hbm_peak()
     roofline = None
     if n_launch:
@@ -357,7 +329,8 @@ def run_fx(args, rank, local, ws):
         roofline = {"kernel": "fx_sparse_gqa_decode", "bound": "hbm", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
                     "peak_source": peak_kind, "avg_launch_us": round(kern_ms * 1e3 / n_launch, 3),
-                    "avg_bytes_per_launch": int(kern_bytes / n_launch), "launches_timed": n_launch}
+                    "avg_bytes_per_launch": int(kern_bytes / n_launch), "launches_timed": n_launch,
+                    "timing": "CUDA events around graphs of the 26 sparse launches per step"}
 
     # whole-step KV bytes: focal layers read every row, sparse layers the selected + text rows
     kv_bytes = 0
@@ -510,6 +483,43 @@ def run_reference(args, rank, local, ws):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel_case(args):
+    """A small, fixed case of one kernel for profiler captures: the decode-shaped call on `--layers`
+    distinct layers (each layer's KV is 160 MB, so even one layer exceeds L2), `--reps` passes."""
+    import kv_cache_token_fx_gb300 as fx
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = OcrDecode()
+    B, Hkv, Hq, T = w.B, w.Hkv, w.Hq, w.tcap
+    t = w.steps - 1
+    ln = torch.full((B,), w.length_at(t), dtype=torch.int32, device=dev)
+    layers = []
+    for l in range(args.layers):
+        k, v = w.layer_kv(l, device=dev)
+        layers.append((k, v, w.query(t, l, device=dev)))
+    ws = fx.Workspace(dev, max(fx.fx_focal_workspace_bytes(B, Hkv, Hq, 1, T),
+                               fx.fx_sparse_workspace_bytes(B, Hkv, Hq, w.k_keep, w.n_vis, T)))
+    scores = torch.empty((B, Hkv, w.n_vis), dtype=torch.float32, device=dev)
+    out = torch.empty((B, Hq, 1, D), dtype=torch.float32, device=dev)
+    idx = torch.empty((B, Hkv, w.k_keep), dtype=torch.int32, device=dev)
+    k0, v0, q0 = layers[0]
+    fx.fx_focal_attn_scores(k0, v0, ln, q0, cand=(0, w.n_vis), out=out, scores=scores, ws=ws)
+    fx.fx_topk_select(scores, w.k_keep, out=idx)
+    for _ in range(args.reps):
+        for k, v, q in layers:
+            if args.kernel_case == "sparse":
+                fx.fx_sparse_gqa_decode(k, v, ln, q, idx, w.n_vis, out=out, ws=ws)
+            elif args.kernel_case == "focal":
+                fx.fx_focal_attn_scores(k, v, ln, q, cand=(0, w.n_vis), out=out, scores=scores, ws=ws)
+            else:
+                fx.fx_topk_select(scores, w.k_keep, prev=idx, out=idx)
+    torch.cuda.synchronize()
+    bits = fx.fx_device_errors()
+    print(json.dumps({"kernel_case": args.kernel_case, "layers": args.layers, "reps": args.reps, "device_errors": bits}))
+    if bits:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -519,7 +529,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk"], default=None,
+                    help="run a small fixed case of one kernel (for profiler captures) instead of the bench")
+    ap.add_argument("--layers", type=int, default=2)
+    ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
+    if args.kernel_case:
+        run_kernel_case(args)
+        return
     if args.warmup < 3 and args.impl == "fx":
         args.warmup = 3
     rank, local, ws = dist_setup()
