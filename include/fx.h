@@ -67,6 +67,7 @@ typedef enum {
 #define FX_DEVERR_INDEX 2u    /* a token index outside [0, len); that entry was skipped */
 #define FX_DEVERR_OFFSETS 4u  /* branch suffix offsets decreasing or past the suffix rows; branch suffix skipped */
 #define FX_DEVERR_CAPACITY 8u /* a compacted cache would exceed its capacity; extra rows not written */
+#define FX_DEVERR_TIMEOUT 16u /* a bounded wait for an asynchronous copy gave up; that call's output is invalid */
 
 /*
  * One layer's KV cache, read-only.  Element (b, h, t, c) of K is at k[b*stride_b + h*stride_h +

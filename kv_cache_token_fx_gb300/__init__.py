@@ -21,11 +21,11 @@ __all__ = [
     "FxError", "load_library", "library_path", "Workspace", "fx_focal_attn_scores", "fx_topk_select",
     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode", "fx_device_errors",
     "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
-    "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY",
+    "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
 ]
 
 FX_OK, FX_ERR_INVALID_ARG, FX_ERR_UNSUPPORTED, FX_ERR_WORKSPACE, FX_ERR_CUDA, FX_ERR_DEVICE = range(6)
-FX_DEVERR_LEN, FX_DEVERR_INDEX, FX_DEVERR_OFFSETS, FX_DEVERR_CAPACITY = 1, 2, 4, 8
+FX_DEVERR_LEN, FX_DEVERR_INDEX, FX_DEVERR_OFFSETS, FX_DEVERR_CAPACITY, FX_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 _STATUS = {0: "FX_OK", 1: "FX_ERR_INVALID_ARG", 2: "FX_ERR_UNSUPPORTED", 3: "FX_ERR_WORKSPACE",
            4: "FX_ERR_CUDA", 5: "FX_ERR_DEVICE"}
 

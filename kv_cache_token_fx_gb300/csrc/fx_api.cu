@@ -75,28 +75,50 @@ bool row_stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0; }
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Split-KV plan: how many query-row groups, how many key splits and how long each split is.
+// Split-KV plan: how many query-row groups, how many key splits, how long each split is and how
+// many staged K tiles each CTA keeps in flight.
 struct Plan {
-    int rb, nrg, nsplit, split_len;
+    int rb, nrg, nsplit, split_len, stages;
 };
 
-Plan make_plan(int pairs, int R, int max_keys, int sm_count)
+// Resident attention CTAs per SM (64 threads each; ~19 KB of shared memory with one staged tile,
+// ~36 KB with two; registers allow about 8).
+constexpr int kResidentOneStage = 8;
+constexpr int kResidentTwoStage = 6;
+
+// `merge_in_cluster`: the splits of one (b, h, row group) are merged inside a thread-block cluster
+// (sparse and prefix calls), which needs at most kMaxClusterSplits splits; the focal call merges in
+// its combine kernel and may use any number of splits.
+Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_cluster = false)
 {
     Plan pl;
     pl.rb = rows_per_block(R);
     pl.nrg = cdiv(R, pl.rb);
+    const int keys = max_keys > 0 ? max_keys : 1;
     const int per_split = pairs * pl.nrg;
-    const int resident = kCtasPerSm * sm_count;           // one full wave of attention CTAs
-    int ns = per_split >= resident ? 1 : resident / per_split;
-    const int min_ns = cdiv(max_keys > 0 ? max_keys : 1, kMaxSplitTokens);
-    if (ns < min_ns) ns = min_ns;
-    const int max_ns = cdiv(max_keys > 0 ? max_keys : 1, 16);   // at least 16 keys per split
-    if (ns > max_ns) ns = max_ns;
+    const int tiles = cdiv(keys, kTile);
+    if (merge_in_cluster && cdiv(tiles, kMaxClusterSplits) * kTile <= kMaxSplitTokens) {
+        const int ns = tiles < kMaxClusterSplits ? tiles : kMaxClusterSplits;
+        pl.split_len = cdiv(cdiv(keys, ns), kTile) * kTile;
+        pl.nsplit = cdiv(keys, pl.split_len);
+        pl.stages = pl.split_len > kTile ? 2 : 1;
+        return pl;
+    }
+    if ((int64_t)per_split * tiles <= (int64_t)kResidentOneStage * sm_count) {
+        // every tile gets its own CTA and the whole call fits in one wave
+        pl.nsplit = tiles;
+        pl.split_len = kTile;
+        pl.stages = 1;
+        return pl;
+    }
+    int ns = kResidentTwoStage * sm_count / per_split;
     if (ns < 1) ns = 1;
-    int len = cdiv(max_keys > 0 ? max_keys : 1, ns);
-    len = cdiv(len, 16) * 16;
-    pl.split_len = len;
-    pl.nsplit = cdiv(max_keys > 0 ? max_keys : 1, len);
+    const int min_ns = cdiv(keys, kMaxSplitTokens);
+    if (ns < min_ns) ns = min_ns;
+    if (ns > tiles) ns = tiles;
+    pl.split_len = cdiv(cdiv(keys, ns), kTile) * kTile;
+    pl.nsplit = cdiv(keys, pl.split_len);
+    pl.stages = pl.split_len > kTile ? 2 : 1;
     return pl;
 }
 
@@ -251,6 +273,7 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     p.nsplit = pl.nsplit;
     p.split_len = pl.split_len;
     p.nrg = pl.nrg;
+    p.stages = pl.stages;
     p.part_m = reinterpret_cast<float*>(w + L.part_m);
     p.part_l = reinterpret_cast<float*>(w + L.part_l);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
@@ -313,7 +336,7 @@ size_t fx_sparse_workspace_bytes(int B, int Hkv, int Hq, int k, int tail_lo, int
     if (B < 1 || Hkv < 1 || Hq < Hkv || k < 0 || tail_lo < 0 || Tcap < 0) return 0;
     const int R = Hq / Hkv;
     const int max_keys = k + (Tcap > tail_lo ? Tcap - tail_lo : 0);
-    const Plan pl = make_plan(B * Hkv, R, max_keys, sm_count_or_default());
+    const Plan pl = make_plan(B * Hkv, R, max_keys, sm_count_or_default(), true);
     return make_layout(B * Hkv, R, pl, 0, true).total;
 }
 
@@ -336,7 +359,7 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     const int G = Hq / kv->Hkv;
     const int R = G;
     const int max_keys = k + (kv->Tcap > tail_lo ? kv->Tcap - tail_lo : 0);
-    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count);
+    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true);
     const Layout L = make_layout(pairs, R, pl, 0, true);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
     if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
@@ -366,6 +389,7 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     p.nsplit = pl.nsplit;
     p.split_len = pl.split_len;
     p.nrg = pl.nrg;
+    p.stages = pl.stages;
     p.part_m = reinterpret_cast<float*>(w + L.part_m);
     p.part_l = reinterpret_cast<float*>(w + L.part_l);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
@@ -436,7 +460,7 @@ size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np,
     if (Br < 1 || Hkv < 1 || Hq < Hkv || Mq < 1 || np < 0 || max_suffix < 0) return 0;
     const int R = (Hq / Hkv) * Mq;
     const int max_keys = np + max_suffix + Mq;
-    const Plan pl = make_plan(Br * Hkv, R, max_keys, sm_count_or_default());
+    const Plan pl = make_plan(Br * Hkv, R, max_keys, sm_count_or_default(), true);
     return make_layout(Br * Hkv, R, pl, 0, true).total;
 }
 
@@ -476,7 +500,7 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     const int R = G * br->Mq;
     const int np = prefix_idx ? kp : prefix->P;
     const int max_keys = np + br->max_suffix + br->Mq;
-    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count);
+    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true);
     const Layout L = make_layout(pairs, R, pl, 0, true);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
     if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
@@ -517,6 +541,7 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     p.nsplit = pl.nsplit;
     p.split_len = pl.split_len;
     p.nrg = pl.nrg;
+    p.stages = pl.stages;
     p.part_m = reinterpret_cast<float*>(w + L.part_m);
     p.part_l = reinterpret_cast<float*>(w + L.part_l);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);

@@ -10,23 +10,28 @@ namespace fx {
 
 constexpr int kHeadDim = 128;
 constexpr int kMaxRows = 64;   // G * Mq limit per KV head
-constexpr int kWarps = 4;      // warps per attention CTA
+constexpr int kWarps = 2;                               // warps per attention CTA
 constexpr int kThreads = 32 * kWarps;
-constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row
-constexpr int kTile = 64;                               // keys per shared-memory tile
-constexpr int kStages = 2;                              // tiles in flight per CTA
-constexpr int kStageBytes = 2 * kTile * kRowBytes;      // K and V of one tile (32 KB)
+constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row (256 bytes)
+constexpr int kTile = 32 * kWarps;                      // keys per tile: one key per thread
+constexpr int kKPitch = kRowBytes + 16;                 // staged K row pitch: 16-byte pad keeps the
+                                                        // lane-per-row 16-byte reads conflict-free
+constexpr int kKStageBytes = kTile * kKPitch;           // 17 KB per staged tile of K
 constexpr int kMaxSplitTokens = 4096;                   // longest split (bounds the index table)
-constexpr int kCtasPerSm = 3;                           // resident attention CTAs per SM (smem-bound)
+constexpr unsigned kSpinLimit = 1u << 22;               // bounded mbarrier waits
+constexpr int kMaxClusterSplits = 16;                   // splits merged inside one thread-block cluster
 // Arrival counters of the last-CTA merge live in a fixed region at the start of every workspace
 // (one slot per (b, h, row group); grid.z <= 65535 and at most 8 row groups), so no other data of
 // any call ever overlaps them and they stay zero between calls.
 constexpr size_t kCounterSlots = 65536u * 8u;
 constexpr size_t kCounterBytes = kCounterSlots * sizeof(unsigned);
 
-inline size_t attn_smem_bytes(int gathered_split_len)
+// Dynamic shared memory of one attention CTA: mbarriers, `stages` K tiles, the query rows (fp32)
+// and the gathered-index table of its split.
+inline size_t attn_smem_bytes(int stages, int rb, int gathered_split_len)
 {
-    return (size_t)kStages * kStageBytes + (size_t)(gathered_split_len > 0 ? gathered_split_len : 0) * sizeof(int);
+    return 128 + (size_t)stages * kKStageBytes + (size_t)rb * kHeadDim * sizeof(float) +
+           (size_t)(gathered_split_len > 0 ? gathered_split_len : 0) * sizeof(int);
 }
 
 // Which key sequence an attention CTA walks.
@@ -63,7 +68,7 @@ struct AttnParams {
     const uint16_t* dr_v;
     int64_t dr_sb, dr_si, dr_sh;
     // split geometry
-    int nsplit, split_len, nrg;
+    int nsplit, split_len, nrg, stages;
     // outputs / scratch
     float* part_m;        // [B*Hkv*R*nsplit]
     float* part_l;        // [B*Hkv*R*nsplit]

@@ -289,3 +289,31 @@ def test_shared_prefix_matches_oracle(fx, sparse):
     assert fx.fx_device_errors() == 0
     vmax = max(float(t.float().abs().max()) for t in (pv, sv, dv))
     pu.assert_out_close(out, ref, vmax)
+
+
+def test_sparse_long_dense_tail_uses_global_merge(fx):
+    """More than 16 x 4096 keys in one row: the splits are merged through the workspace (not inside a
+    thread-block cluster)."""
+    B, Hkv, G, T = 1, 1, 2, 70000
+    k, v = kv_case(B, Hkv, T, 81)
+    q = rnd((B, Hkv * G, 1, D), 81, 3)
+    length = torch.tensor([T - 5], dtype=torch.int32)
+    idx = torch.tensor([[[3, 17, 40000]]], dtype=torch.int32)
+    ref = oracle.sparse_decode(k, v, length, q, idx, 50)
+    out = fx.fx_sparse_gqa_decode(dev(k), dev(v), dev(length), dev(q), dev(idx), 50)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    pu.assert_out_close(out, ref, float(v.float().abs().max()))
+
+
+@pytest.mark.parametrize("n_keys", [1, 63, 64, 65, 130, 1000, 1023, 1025])
+def test_sparse_split_counts(fx, n_keys):
+    """Key counts around tile and cluster boundaries (1 to 16 splits of one cluster)."""
+    B, Hkv, G = 2, 2, 2
+    T = n_keys + 3
+    k, v = kv_case(B, Hkv, T, 90 + n_keys % 7)
+    q = rnd((B, Hkv * G, 1, D), 91, 3)
+    length = torch.tensor([n_keys, max(1, n_keys // 2)], dtype=torch.int32)
+    ref = oracle.sparse_decode(k, v, length, q, None, 0)
+    out = fx.fx_sparse_gqa_decode(dev(k), dev(v), dev(length), dev(q), None, 0)
+    pu.assert_out_close(out, ref, float(v.float().abs().max()))
