@@ -164,7 +164,7 @@ def measured_hbm_peak():
 class OcrDecodeRun:
     """Device state of the FastOCR-shaped decode and its per-step CUDA graphs."""
 
-    def __init__(self, w: OcrDecode, device, with_e2e: bool):
+    def __init__(self, w: OcrDecode, device, with_e2e: bool, pdl: bool = True):
         import kv_cache_token_fx_gb300 as fx
         self.fx = fx
         self.w = w
@@ -189,6 +189,7 @@ class OcrDecodeRun:
                  fx.fx_sparse_workspace_bytes(B, Hkv, Hq, 0, 0, T))
         self.ws = fx.Workspace(device, nb)
         self.with_e2e = with_e2e
+        self.pdl = pdl
         if with_e2e:
             # the per-step inputs as a host would hold them: queries of all layers and the new K/V row
             self.Q_host = self.Q.cpu().pin_memory()
@@ -201,21 +202,27 @@ class OcrDecodeRun:
         self.launches_per_step = 0
 
     # one decode step; `only_sparse` replays just the sparse-decode launches of the step (used to time
-    # the dominant kernel on its own); `nbytes_out` collects the algorithmic bytes of each sparse launch
+    # the dominant kernel on its own); `nbytes_out` collects the algorithmic bytes of each sparse launch.
+    # Every call is a programmatic dependent launch; a call whose lengths / indices / K-V rows were
+    # written two or more launches earlier also prefetches them before the previous kernel ends.
     def step(self, t: int, only_sparse: bool = False, nbytes_out=None):
         fx, w = self.fx, self.w
+        pdl = fx.FX_LAUNCH_PDL if self.pdl else 0
+        ready = fx.FX_LAUNCH_INPUTS_READY if self.pdl else 0
         p = t % 2
         ln = self.lens[t]
         launches = 0
+        after_topk = False
         for l in range(w.n_layers):
             if l in w.focal_layers:
                 if only_sparse:
                     continue
                 fx.fx_focal_attn_scores(self.K[l], self.V[l], ln, self.Q[t, l], cand=(0, w.n_vis), out=self.O[l],
-                                        scores=self.scores, ws=self.ws)
+                                        scores=self.scores, ws=self.ws, flags=pdl | ready)
                 prev = self.sets[l][1 - p] if t > 0 else None
-                fx.fx_topk_select(self.scores, w.k_keep, prev=prev, out=self.sets[l][p])
+                fx.fx_topk_select(self.scores, w.k_keep, prev=prev, out=self.sets[l][p], flags=pdl)
                 launches += 3
+                after_topk = True
                 continue
             if l < w.focal_layers[0]:
                 sel = self.sets[w.focal_layers[-1]][1 - p] if t > 0 else None
@@ -226,8 +233,11 @@ class OcrDecodeRun:
             n_keys = (w.k_keep + w.length_at(t) - w.n_vis) if sel is not None else w.length_at(t)
             nbytes = (w.B * w.Hkv * n_keys * ROW_BYTES + w.B * w.Hq * D * (2 + 4) +
                       (w.B * w.Hkv * w.k_keep * 4 if sel is not None else 0))
+            # the set made by the top-k launched just before is not ready before that kernel ends
+            fl = pdl | (0 if (after_topk and not only_sparse) else ready)
             fx.fx_sparse_gqa_decode(self.K[l], self.V[l], ln, self.Q[t, l], sel, w.n_vis if sel is not None else 0,
-                                    out=self.O[l], ws=self.ws)
+                                    out=self.O[l], ws=self.ws, flags=fl)
+            after_topk = False
             if nbytes_out is not None:
                 nbytes_out.append(nbytes)
             launches += 1
@@ -276,7 +286,7 @@ def run_fx(args, rank, local, ws):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = OcrDecode()
-    run = OcrDecodeRun(w, dev, with_e2e=not args.no_e2e)
+    run = OcrDecodeRun(w, dev, with_e2e=not args.no_e2e, pdl=not args.no_pdl)
     # eager warm-up step (sizes the workspace, loads the kernels) then capture every step once
     for t in range(2):
         run.step(t)
@@ -378,7 +388,8 @@ def run_fx(args, rank, local, ws):
                    "batch": w.B, "layers": w.n_layers, "kv_tokens": f"{w.length_at(0)}..{w.length_at(w.steps - 1)}",
                    "k": w.k_keep, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (about 1 GB of KV touched per step)",
-                   "timing": "per-step CUDA graphs, CUDA events, max over ranks"},
+                   "timing": "per-step CUDA graphs, CUDA events, max over ranks",
+                   "launch": "plain" if args.no_pdl else "programmatic dependent launch between the step's kernels"},
         "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / ws / peak, 4),
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": run.launches_per_step * len(steps),
@@ -528,6 +539,7 @@ def main():
     ap.add_argument("--impl", default="fx", choices=["fx", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk"], default=None,
                     help="run a small fixed case of one kernel (for profiler captures) instead of the bench")

@@ -30,6 +30,19 @@
  *     16-byte aligned and every row stride a multiple of 8 elements.
  *   - GQA grouping: with G = Hq / Hkv, query head g belongs to KV head g / G.
  *   - q and out tensors are laid out [batch, Hq, Mq, 128] (contiguous).  Outputs are fp32.
+ *   - `flags` (the argument before `stream` of every compute call) is a bit set of FX_LAUNCH_*:
+ *       FX_LAUNCH_PDL            launch as a programmatic dependent of the kernel enqueued just before
+ *                                it on the same stream: the call's kernels may start while that kernel
+ *                                is still running and wait for it on the device before reading or
+ *                                writing anything it could have produced.  Back-to-back calls (layer
+ *                                after layer) then overlap one call's start with the previous one's end.
+ *       FX_LAUNCH_INPUTS_READY   (with FX_LAUNCH_PDL) the caller guarantees that the lengths, the index
+ *                                lists and the K/V rows the call reads were written by the host or by
+ *                                a kernel enqueued two or more launches earlier -- not by the kernel
+ *                                immediately before.  The call may then read them, and start its K/V
+ *                                loads, before that kernel finishes.  Queries, outputs and workspace
+ *                                are still touched only after it finishes.
+ *     0 gives ordinary stream-ordered launches.
  *   - Host-side argument errors return a status and set a thread-local message (fx_last_error);
  *     nothing is enqueued then.  Data that only the device can see (lengths, indices, offsets) is
  *     checked by the kernels: a bad value is clamped or skipped -- never dereferenced -- and a bit is
@@ -61,6 +74,10 @@ typedef enum {
     FX_ERR_CUDA = 4,        /* a CUDA runtime call failed; fx_last_error() has its message */
     FX_ERR_DEVICE = 5       /* fx_device_errors(): a kernel saw bad device-side data */
 } fx_status;
+
+/* Launch flags (see the conventions above). */
+#define FX_LAUNCH_PDL 1u
+#define FX_LAUNCH_INPUTS_READY 2u
 
 /* Bits of the device error word (fx_device_errors). */
 #define FX_DEVERR_LEN 1u      /* a length outside [0, capacity]; it was clamped */
@@ -132,7 +149,7 @@ FX_API fx_status fx_workspace_init(void* ws, size_t ws_bytes, void* stream);
 FX_API size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap);
 FX_API fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,
                                float scale, int cand_lo, int cand_hi, float* out, float* scores,
-                               void* ws, size_t ws_bytes, void* stream);
+                               void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------------------------- */
 /* fx_topk_select -- keep the k most important tokens of each row.  [FastOCR] Focal-Guided Pruning
@@ -149,7 +166,7 @@ FX_API fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, in
  * 1 <= k <= n.  No workspace.
  */
 FX_API fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int32_t* prev_idx,
-                         int32_t* idx_out, void* stream);
+                         int32_t* idx_out, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------------------------- */
 /* fx_sparse_gqa_decode -- a non-focal layer: decode attention over the selected tokens only.
@@ -170,7 +187,7 @@ FX_API fx_status fx_topk_select(const float* scores, int rows, int n, int k, con
 FX_API size_t fx_sparse_workspace_bytes(int B, int Hkv, int Hq, int k, int tail_lo, int Tcap);
 FX_API fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, const int32_t* idx,
                                int k, int tail_lo, float scale, float* out, void* ws,
-                               size_t ws_bytes, void* stream);
+                               size_t ws_bytes, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------------------------- */
 /* fx_kv_compact -- decoupled KV retention: copy the retained rows of n_layers layers into a
@@ -190,7 +207,7 @@ FX_API fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, in
  */
 FX_API fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx, int k,
                         int tail_lo, const fx_kv_out_desc* dst, int64_t dst_stride_layer,
-                        int n_layers, void* stream);
+                        int n_layers, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------------------------- */
 /* fx_shared_prefix_decode -- parallel draft verification over a shared prefix.  [HPD] parts 2
@@ -234,7 +251,8 @@ typedef struct {
 FX_API size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np, int max_suffix);
 FX_API fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_desc* branches,
                                   const fx_bf16* q, int Hq, const int32_t* prefix_idx, int kp,
-                                  float scale, float* out, void* ws, size_t ws_bytes, void* stream);
+                                  float scale, float* out, void* ws, size_t ws_bytes, unsigned flags,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

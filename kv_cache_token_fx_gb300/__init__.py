@@ -22,10 +22,12 @@ __all__ = [
     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode", "fx_device_errors",
     "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
     "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
+    "FX_LAUNCH_PDL", "FX_LAUNCH_INPUTS_READY",
 ]
 
 FX_OK, FX_ERR_INVALID_ARG, FX_ERR_UNSUPPORTED, FX_ERR_WORKSPACE, FX_ERR_CUDA, FX_ERR_DEVICE = range(6)
 FX_DEVERR_LEN, FX_DEVERR_INDEX, FX_DEVERR_OFFSETS, FX_DEVERR_CAPACITY, FX_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+FX_LAUNCH_PDL, FX_LAUNCH_INPUTS_READY = 1, 2
 _STATUS = {0: "FX_OK", 1: "FX_ERR_INVALID_ARG", 2: "FX_ERR_UNSUPPORTED", 3: "FX_ERR_WORKSPACE",
            4: "FX_ERR_CUDA", 5: "FX_ERR_DEVICE"}
 
@@ -84,19 +86,20 @@ def load_library():
         lib.fx_workspace_init.argtypes = [c_vp, c_size, c_vp]
         lib.fx_focal_workspace_bytes.argtypes = [c_int] * 5
         lib.fx_focal_workspace_bytes.restype = c_size
+        c_uint = ctypes.c_uint
         lib.fx_focal_attn_scores.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_int, c_int, c_float, c_int,
-                                             c_int, c_vp, c_vp, c_vp, c_size, c_vp]
-        lib.fx_topk_select.argtypes = [c_vp, c_int, c_int, c_int, c_vp, c_vp, c_vp]
+                                             c_int, c_vp, c_vp, c_vp, c_size, c_uint, c_vp]
+        lib.fx_topk_select.argtypes = [c_vp, c_int, c_int, c_int, c_vp, c_vp, c_uint, c_vp]
         lib.fx_sparse_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_sparse_workspace_bytes.restype = c_size
         lib.fx_sparse_gqa_decode.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_vp, c_int, c_int, c_float,
-                                             c_vp, c_vp, c_size, c_vp]
+                                             c_vp, c_vp, c_size, c_uint, c_vp]
         lib.fx_kv_compact.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_vp, c_int, c_int, ctypes.POINTER(KVOutDesc),
-                                      c_i64, c_int, c_vp]
+                                      c_i64, c_int, c_uint, c_vp]
         lib.fx_shared_prefix_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_shared_prefix_workspace_bytes.restype = c_size
         lib.fx_shared_prefix_decode.argtypes = [ctypes.POINTER(PrefixDesc), ctypes.POINTER(BranchDesc), c_vp, c_int,
-                                                c_vp, c_int, c_float, c_vp, c_vp, c_size, c_vp]
+                                                c_vp, c_int, c_float, c_vp, c_vp, c_size, c_uint, c_vp]
         for name in ("fx_device_errors", "fx_workspace_init", "fx_focal_attn_scores", "fx_topk_select",
                      "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode"):
             getattr(lib, name).restype = c_int
@@ -188,7 +191,7 @@ def fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np_, max_suffix) -> int:
 
 
 def fx_focal_attn_scores(k, v, length, q, *, q_pos0: int = -1, scale=None, cand=None, want_out=True,
-                         want_scores=True, out=None, scores=None, ws=None, stream=None):
+                         want_scores=True, out=None, scores=None, ws=None, stream=None, flags: int = 0):
     """Focal layer: full attention + per-token importance.  Returns (out, scores) (None if not wanted).
 
     k, v [B, Hkv, Tcap, 128] bf16; length int32 [B]; q [B, Hq, Mq, 128] bf16 (contiguous).
@@ -214,11 +217,11 @@ def fx_focal_attn_scores(k, v, length, q, *, q_pos0: int = -1, scale=None, cand=
     buf = _workspace(ws, nbytes, k.device, stream)
     sc = _default_scale(d) if scale is None else float(scale)
     _check(lib.fx_focal_attn_scores(ctypes.byref(desc), _ptr(q), Hq, Mq, int(q_pos0), sc, int(lo), int(hi),
-                                    _ptr(out), _ptr(scores), _ptr(buf), buf.numel(), _stream(stream)))
+                                    _ptr(out), _ptr(scores), _ptr(buf), buf.numel(), int(flags), _stream(stream)))
     return out, scores
 
 
-def fx_topk_select(scores, k: int, *, prev=None, out=None, stream=None):
+def fx_topk_select(scores, k: int, *, prev=None, out=None, stream=None, flags: int = 0):
     """Top-k of each row of ``scores`` [..., n] (fp32, contiguous): int32 [..., k], ascending indices."""
     lib = load_library()
     _need_cuda(scores, "scores", torch.float32)
@@ -232,11 +235,12 @@ def fx_topk_select(scores, k: int, *, prev=None, out=None, stream=None):
         _need_cuda(prev, "prev", torch.int32)
         if prev.numel() != rows * k or not prev.is_contiguous():
             raise FxError(FX_ERR_INVALID_ARG, "prev must be a contiguous [rows, k] int32 tensor")
-    _check(lib.fx_topk_select(_ptr(scores), rows, n, int(k), _ptr(prev), _ptr(out), _stream(stream)))
+    _check(lib.fx_topk_select(_ptr(scores), rows, n, int(k), _ptr(prev), _ptr(out), int(flags), _stream(stream)))
     return out
 
 
-def fx_sparse_gqa_decode(k, v, length, q, idx, tail_lo: int, *, scale=None, out=None, ws=None, stream=None):
+def fx_sparse_gqa_decode(k, v, length, q, idx, tail_lo: int, *, scale=None, out=None, ws=None, stream=None,
+                         flags: int = 0):
     """Decode attention of q [B, Hq, 1, 128] over idx [B, Hkv, kk] (or None) plus the tail [tail_lo, len)."""
     lib = load_library()
     desc = _kv_desc(k, v, length)
@@ -257,11 +261,11 @@ def fx_sparse_gqa_decode(k, v, length, q, idx, tail_lo: int, *, scale=None, out=
     buf = _workspace(ws, nbytes, k.device, stream)
     sc = _default_scale(d) if scale is None else float(scale)
     _check(lib.fx_sparse_gqa_decode(ctypes.byref(desc), _ptr(q), Hq, _ptr(idx) if kk else None, kk, int(tail_lo),
-                                    sc, _ptr(out), _ptr(buf), buf.numel(), _stream(stream)))
+                                    sc, _ptr(out), _ptr(buf), buf.numel(), int(flags), _stream(stream)))
     return out
 
 
-def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, stream=None):
+def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, stream=None, flags: int = 0):
     """Compact the retained rows of one layer ([B, Hkv, T, 128]) or of L layers ([L, B, Hkv, T, 128])."""
     lib = load_library()
     if k.dim() == 5:
@@ -285,12 +289,12 @@ def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, str
         kk = idx.shape[-1]
     dst_out = KVOutDesc(*[getattr(dst, f) for f, _ in KVDesc._fields_])
     _check(lib.fx_kv_compact(ctypes.byref(src), s_layer, _ptr(idx) if kk else None, kk, int(tail_lo),
-                             ctypes.byref(dst_out), d_layer, n_layers, _stream(stream)))
+                             ctypes.byref(dst_out), d_layer, n_layers, int(flags), _stream(stream)))
     return dst_k, dst_v, dst_len
 
 
 def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, prefix_idx=None, scale=None,
-                            out=None, ws=None, stream=None):
+                            out=None, ws=None, stream=None, flags: int = 0):
     """Draft verification of Br branches over one shared prefix.
 
     pk, pv [Hkv, P, 128]; sk, sv [Hkv, S, 128] (branch b owns rows off[b]..off[b+1]-1);
@@ -322,7 +326,7 @@ def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, 
     buf = _workspace(ws, nbytes, q.device, stream)
     sc = _default_scale(d) if scale is None else float(scale)
     _check(lib.fx_shared_prefix_decode(ctypes.byref(pre), ctypes.byref(brd), _ptr(q), Hq, _ptr(prefix_idx), kp, sc,
-                                       _ptr(out), _ptr(buf), buf.numel(), _stream(stream)))
+                                       _ptr(out), _ptr(buf), buf.numel(), int(flags), _stream(stream)))
     return out
 
 

@@ -1,27 +1,28 @@
-// Split-KV decode attention on CUDA cores for sm_103a.
+// Split-KV decode / verify attention for sm_103a.
 //
-// One CTA (2 warps, 64 threads) = (row group of up to RB query rows, one split of the key sequence,
-// one (b, KV head)).  The split is walked in tiles of 64 keys, one key per thread:
-//   * K rows reach shared memory through the TMA engine: thread r issues one 256-byte
-//     cp.async.bulk copy for key r of the tile (contiguous rows for the focal mode, gathered rows for
-//     the sparse/prefix modes) into a row padded to 272 bytes, completing on an mbarrier.  With two
-//     stages the next tile's rows are in flight while the current one is used.
-//   * V rows go straight to registers: before waiting on K, each half-warp issues coalesced 16-byte
-//     loads for its keys' V rows (lane `sub` holds dims [8*sub, 8*sub+8)).
-//   * q.k is computed lane-per-key: each thread reads its own staged K row (the pad keeps the 32
-//     rows of a warp on distinct banks) against the pre-scaled fp32 query rows broadcast from shared
-//     memory -- no cross-lane reduction.  The softmax is kept online in base-2 units.
-//   * p.v: half-warps take alternate keys, p is broadcast with one shuffle per (key, row).
-// Partial (max, sum, unnormalised output) triples per split go to the workspace; the sparse/prefix
-// modes merge them in the last-arriving CTA of each (b, h, row group), the focal mode in a separate
-// combine kernel that also forms the per-token importance from the stored logits.
-//
-// Every mbarrier wait is bounded: on timeout the kernel sets FX_DEVERR_TIMEOUT, waits once more
-// (bounded) for its own copies, and finishes without hanging.
+// One CTA (4 warps) = (group of up to 16 query rows of one KV head, one split of that head's key
+// sequence, one (b, KV head)).  The split is walked in tiles of 64 keys:
+//   * Data movement: the K and V rows of a tile (256 bytes each; contiguous rows for the focal mode,
+//     gathered rows for the sparse/prefix modes) are copied into shared memory with 16-byte cp.async
+//     operations, each warp instruction moving two whole rows, one commit group per tile.  Rows are padded to 272 bytes so
+//     that the 8-row ldmatrix reads below hit 8 different bank groups.  Two stages: tile i+1 is in
+//     flight while tile i is used.  Rows that must not be read (past the split, rejected index) are
+//     zero-filled instead.  (Per-row cp.async.bulk TMA copies were measured slower here: 256-byte
+//     requests keep the TMA engine, not HBM, busy.)
+//   * Math: each warp takes 16 keys of the tile.  S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32
+//     accumulate; the query rows sit in one 16-row A tile, rows past R are zero), then an online
+//     softmax on the accumulator fragments in base-2 units, then O += P V with the same MMA, where P
+//     is split into bf16 hi + lo parts (two MMAs) so that the probabilities keep ~16 bits.
+// Partial (max, sum, unnormalised output) triples per split are merged either inside a thread-block
+// cluster -- all splits of one (b, h, row group) form one cluster and read each other's partials
+// from distributed shared memory -- or, for the focal call and for very long rows, through the
+// workspace (the focal call's combine kernel also forms the per-token importance from the logits
+// this kernel stores).
 //
 // Attention and importance follow FastOCR (Methodology: Focal-Guided Pruning): focal layers attend
 // over the full cache, the rest over the selected set; FastKV (2.A) for the causal query window;
 // HPD-Parsing (parts 2 and 3) for the shared prefix + private suffix + causal draft sequence.
+#include <cuda_bf16.h>
 #include <math.h>
 
 #include "fx_internal.h"
@@ -31,30 +32,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ void unpack8(const uint4& w, float f[8])
-{
-    // bf16 -> fp32 is a 16-bit left shift of the pattern; element 2i is the low half of word i.
-    f[0] = __uint_as_float(w.x << 16);
-    f[1] = __uint_as_float(w.x & 0xffff0000u);
-    f[2] = __uint_as_float(w.y << 16);
-    f[3] = __uint_as_float(w.y & 0xffff0000u);
-    f[4] = __uint_as_float(w.z << 16);
-    f[5] = __uint_as_float(w.z & 0xffff0000u);
-    f[6] = __uint_as_float(w.w << 16);
-    f[7] = __uint_as_float(w.w & 0xffff0000u);
-}
-
-__device__ __forceinline__ uint4 ld_stream16(const uint16_t* ptr)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(ptr));
-    return r;
-}
-
-// 2^x with the hardware approximation (relative error about 2^-22, far inside the tolerances).
-__device__ __forceinline__ float fast_exp2(float x)
+// ---- PTX wrappers -------------------------------------------------------------------------------
+__device__ __forceinline__ float fast_exp2(float x)   // hardware 2^x (relative error about 2^-22)
 {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -63,47 +42,48 @@ __device__ __forceinline__ float fast_exp2(float x)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
 {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_none_pending() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
 {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
 {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D (fp32)
+__device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1)
 {
-    uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Bounded wait for phase `parity` of an mbarrier: never spins forever.
-__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, unsigned* err)
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
-    for (unsigned it = 0; it < kSpinLimit; ++it)
-        if (mbar_try_wait(bar, parity)) return;
-    atomicOr(err, FX_DEVERR_TIMEOUT);
-    for (unsigned it = 0; it < kSpinLimit; ++it)   // give this CTA's own copies one more bounded chance
-        if (mbar_try_wait(bar, parity)) return;
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), for a pair of values
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
+    hi = *reinterpret_cast<uint32_t*>(&hv);
+    lo = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
 }
 
 __device__ __forceinline__ void flag(unsigned* err, unsigned bit) { atomicOr(err, bit); }
@@ -138,6 +118,7 @@ __device__ __forceinline__ float ld_cluster(uint32_t addr)
     return v;
 }
 
+// ---- key sequences --------------------------------------------------------------------------------
 // Where the rows of one (b, h) key sequence live: sequence position -> K row and V row.
 template <int MODE>
 struct KeySource {
@@ -196,29 +177,35 @@ struct KeySource {
     }
 };
 
-template <int MODE, int RB, bool CLUSTER>
-__global__ void __launch_bounds__(kThreads) attn_decode_kernel(const AttnParams p)
+// ---- the kernel -----------------------------------------------------------------------------------
+template <int MODE, bool CLUSTER>
+__global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int nst = p.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    unsigned char* sK = smem + 128;
-    float* q_s = reinterpret_cast<float*>(sK + (size_t)nst * kKStageBytes);
-    int* s_tok = reinterpret_cast<int*>(q_s + RB * kHeadDim);
+    unsigned char* sQ = smem + 128;                                          // [16][kPitch] bf16
+    unsigned char* sKV = sQ + kQTileBytes;                                   // [nst][K tile, V tile]
+    int* s_tok = reinterpret_cast<int*>(sKV + (size_t)nst * kKVStageBytes);  // [split_len]
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int hw = lane >> 4;
-    const int sub = lane & 15;
+    const int g = lane >> 2;      // accumulator row within the 16-row tile (and row + 8)
+    const int t4 = lane & 3;      // accumulator column pair
     const int rg = blockIdx.x;
     const int split = blockIdx.y;
     const int bh = blockIdx.z;
     const int b = bh / p.Hkv;
     const int h = bh - b * p.Hkv;
-    const int r0 = rg * RB;
+    const int r0 = rg * kRowsPerCta;
 
-    // ---- key sequence of this (b, h) ----------------------------------------------------------
+    // ---- stage A: what depends only on the caller's lengths, indices and K/V rows.  With
+    // FX_LAUNCH_INPUTS_READY it runs before the preceding kernel on the stream has finished, so the
+    // first tiles are already in flight when that kernel ends.
+    const bool early = p.prefetch != 0;
+    if (!early) griddep_wait();
+
+    // key sequence of this (b, h)
     KeySource<MODE> src;
     int n_keys;
     src.kb = p.k + (int64_t)b * p.sb + (int64_t)h * p.sh;
@@ -266,25 +253,6 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const AttnParams 
     src.s0 = s0;
     const int ntiles = s1 > s0 ? (s1 - s0 + kTile - 1) / kTile : 0;
 
-    if (tid == 0) {
-        mbar_init(smem_addr(&bars[0]), kThreads);
-        mbar_init(smem_addr(&bars[1]), kThreads);
-        mbar_init_fence();
-    }
-    // query rows, pre-scaled to base-2 logits
-    for (int e = tid; e < RB * kHeadDim; e += kThreads) {
-        const int r = e >> 7;
-        const int c = e & (kHeadDim - 1);
-        const int row = r0 + r;
-        float v = 0.f;
-        if (row < p.R) {
-            const int gi = row / p.Mq;
-            const int i = row - gi * p.Mq;
-            const uint16_t qb = p.q[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c];
-            v = __uint_as_float((uint32_t)qb << 16) * p.qscale;
-        }
-        q_s[e] = v;
-    }
     // gathered token positions of this split, checked once
     if (MODE != kModeFocal && p.idx != nullptr) {
         const int32_t* irow = p.idx + (int64_t)bh * p.kk;
@@ -300,205 +268,246 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const AttnParams 
     }
     __syncthreads();
 
-    int lim[RB];
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-        const int row = r0 + r;
-        const int i = row - (row / p.Mq) * p.Mq;
-        if (row >= p.R)
-            lim[r] = -1;   // padding row: sees nothing
-        else if (MODE == kModeFocal)
-            lim[r] = p.q_pos0 >= 0 ? p.q_pos0 + i : 0x7fffffff;
-        else if (MODE == kModePrefix)
-            lim[r] = src.np + src.L + i;   // draft row j is visible iff j <= i
-        else
-            lim[r] = 0x7fffffff;
-    }
-
-    // thread r stages K row r of a tile (one 256-byte bulk copy) or zero-fills it
+    // a tile is copied with 16-byte cp.async operations, one commit group per tile; each warp
+    // instruction moves two whole rows (lanes 0-15 one row, lanes 16-31 the next), so the copies are
+    // fully coalesced.  Rows that must not be read are zero-filled instead.
     auto issue = [&](int tile, int stage) {
-        const int pos = s0 + tile * kTile + tid;
-        const uint16_t* kp = src.kb;
-        const uint16_t* vp = src.vb;
-        const bool ok = pos < s1 && src.row(pos, s_tok, kp, vp);
-        unsigned char* dst = sK + (size_t)stage * kKStageBytes + (size_t)tid * kKPitch;
-        const uint32_t bar = smem_addr(&bars[stage]);
-        fence_proxy_async();
-        if (ok) {
-            mbar_arrive_expect_tx(bar, kRowBytes);
-            bulk_g2s(smem_addr(dst), kp, kRowBytes, bar);
-        } else {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+        const int c16 = lane & 15;
 #pragma unroll
-            for (int c = 0; c < kRowBytes / 16; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
-            mbar_arrive(bar);
+        for (int u = 0; u < kTile / (2 * kWarps); ++u) {
+            const int r = 2 * (warp + kWarps * u) + (lane >> 4);
+            const int pos = s0 + tile * kTile + r;
+            const uint16_t* kp = src.kb;
+            const uint16_t* vp = src.vb;
+            const bool ok = pos < s1 && src.row(pos, s_tok, kp, vp);
+            unsigned char* dk = sKV + (size_t)stage * kKVStageBytes + (size_t)r * kPitch + 16 * c16;
+            unsigned char* dv = dk + kTile * kPitch;
+            if (ok) {
+                cp_async16(smem_addr(dk), kp + 8 * c16);
+                cp_async16(smem_addr(dv), vp + 8 * c16);
+            } else {
+                *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
+        cp_async_commit();
     };
-
-    float m[RB], lsum[RB], o[RB][8];
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-        m[r] = -INFINITY;
-        lsum[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[r][e] = 0.f;
-    }
-    uint32_t phase_bits = 0u;   // bit s: parity of the next completion of stage s
 
     if (ntiles > 0) issue(0, 0);
     if (ntiles > 1 && nst > 1) issue(1, 1);
 
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int stage = nst > 1 ? (tile & 1) : 0;
-        const int base = s0 + tile * kTile;
+    // ---- stage B: after the preceding kernel -- the query rows, then everything that writes ------
+    if (early) griddep_wait();
+    griddep_launch();
 
-        // V rows of this warp's 32 keys, straight to registers (half-warp per key)
-        uint4 vr[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int pos = base + warp * 32 + 2 * i + hw;
-            const uint16_t* kp;
-            const uint16_t* vp;
-            const bool ok = pos < s1 && src.row(pos, s_tok, kp, vp);
-            vr[i] = ok ? ld_stream16(vp + sub * 8) : make_uint4(0u, 0u, 0u, 0u);
+    // the query rows of this group as one bf16 16-row tile (rows past R are zero)
+    for (int e = tid; e < kRowsPerCta * (kHeadDim / 8); e += kThreads) {
+        const int rr = e >> 4;
+        const int c8 = e & 15;
+        const int row = r0 + rr;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < p.R) {
+            const int gi = row / p.Mq;
+            const int i = row - gi * p.Mq;
+            v = *reinterpret_cast<const uint4*>(p.q + ((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c8 * 8);
         }
-
-        mbar_wait(smem_addr(&bars[stage]), (phase_bits >> stage) & 1u, p.err);
-        phase_bits ^= 1u << stage;
-
-        // q.k, one key per lane
-        const int kpos = base + tid;
-        bool kval = kpos < s1;
-        if (MODE == kModeSparse && kval && kpos < p.kk) kval = s_tok[kpos - s0] >= 0;
-        if (MODE == kModePrefix && kval && src.gathered && kpos < src.np) kval = s_tok[kpos - s0] >= 0;
-        const unsigned char* krow = sK + (size_t)stage * kKStageBytes + (size_t)tid * kKPitch;
-        float acc[RB][4];   // four independent FMA chains per row
-#pragma unroll
-        for (int r = 0; r < RB; ++r)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[r][j] = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < kHeadDim / 8; ++c) {
-            float kf[8];
-            unpack8(*reinterpret_cast<const uint4*>(krow + c * 16), kf);
-#pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                const float4 qa = *reinterpret_cast<const float4*>(q_s + r * kHeadDim + c * 8);
-                const float4 qb = *reinterpret_cast<const float4*>(q_s + r * kHeadDim + c * 8 + 4);
-                acc[r][0] = fmaf(qa.x, kf[0], acc[r][0]);
-                acc[r][1] = fmaf(qa.y, kf[1], acc[r][1]);
-                acc[r][2] = fmaf(qa.z, kf[2], acc[r][2]);
-                acc[r][3] = fmaf(qa.w, kf[3], acc[r][3]);
-                acc[r][0] = fmaf(qb.x, kf[4], acc[r][0]);
-                acc[r][1] = fmaf(qb.y, kf[5], acc[r][1]);
-                acc[r][2] = fmaf(qb.z, kf[6], acc[r][2]);
-                acc[r][3] = fmaf(qb.w, kf[7], acc[r][3]);
-            }
-        }
-        float pr[RB];
-#pragma unroll
-        for (int r = 0; r < RB; ++r)
-            pr[r] = (kval && kpos <= lim[r]) ? (acc[r][0] + acc[r][1]) + (acc[r][2] + acc[r][3]) : -INFINITY;
-
-        if (MODE == kModeFocal && p.logits != nullptr && kpos < s1) {
-#pragma unroll
-            for (int r = 0; r < RB; ++r)
-                if (r0 + r < p.R) p.logits[(int64_t)(bh * p.R + r0 + r) * p.Tcap + kpos] = pr[r];
-        }
-
-        // online softmax (warp-uniform running max)
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            float cm = pr[r];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, off));
-            const float mn = fmaxf(m[r], cm);
-            const float ms = (mn == -INFINITY) ? 0.f : mn;
-            const float alpha = fast_exp2(m[r] - ms);
-            m[r] = mn;
-            lsum[r] *= alpha;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[r][e] *= alpha;
-            pr[r] = fast_exp2(pr[r] - ms);
-            lsum[r] += pr[r];
-        }
-
-        // p.v: half-warp hw takes keys 2i + hw of this warp
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float vf[8];
-            unpack8(vr[i], vf);
-#pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                const float pk = __shfl_sync(kFull, pr[r], 2 * i + hw);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[r][e] = fmaf(pk, vf[e], o[r][e]);
-            }
-        }
-
-        __syncthreads();   // both warps are done with this K stage
-        if (tile + nst < ntiles) issue(tile + nst, stage);
-    }
-
-    // reduce within the warp: lsum over all lanes, o over the two half-warps
-#pragma unroll
-    for (int r = 0; r < RB; ++r) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) lsum[r] += __shfl_xor_sync(kFull, lsum[r], off);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[r][e] += __shfl_xor_sync(kFull, o[r][e], 16);
-    }
-
-    // ---- combine the two warps into one partial per row (the K stages are free now) -----------
-    __shared__ float sm_m[kWarps][RB];
-    __shared__ float sm_l[kWarps][RB];
-    float* sm_o = reinterpret_cast<float*>(sK);   // [kWarps][RB][128]
-    if (lane < 16) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            float4* dst = reinterpret_cast<float4*>(sm_o + (warp * RB + r) * kHeadDim + sub * 8);
-            dst[0] = make_float4(o[r][0], o[r][1], o[r][2], o[r][3]);
-            dst[1] = make_float4(o[r][4], o[r][5], o[r][6], o[r][7]);
-        }
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            sm_m[warp][r] = m[r];
-            sm_l[warp][r] = lsum[r];
-        }
+        *reinterpret_cast<uint4*>(sQ + rr * kPitch + c8 * 16) = v;
     }
     __syncthreads();
 
-    // this CTA's partial: c_m / c_l / c_o (also read by the other CTAs of the cluster)
-    __shared__ float c_m[RB];
-    __shared__ float c_l[RB];
-    __shared__ __align__(16) float c_o[RB][kHeadDim];
+    // causal / draft limits of the two accumulator rows this thread holds (g and g + 8)
+    int lim[2];
 #pragma unroll
-    for (int r = 0; r < RB; ++r) {
+    for (int hr = 0; hr < 2; ++hr) {
+        const int row = r0 + g + 8 * hr;
+        const int i = row - (row / p.Mq) * p.Mq;
+        if (row >= p.R)
+            lim[hr] = -1;   // padding row: sees nothing
+        else if (MODE == kModeFocal)
+            lim[hr] = p.q_pos0 >= 0 ? p.q_pos0 + i : 0x7fffffff;
+        else if (MODE == kModePrefix)
+            lim[hr] = src.np + src.L + i;   // draft row j is visible iff j <= i
+        else
+            lim[hr] = 0x7fffffff;
+    }
+
+    // Q fragments for the 8 k-steps of the 128-wide head
+    uint32_t qa[8][4];
+    {
+        const int qrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int qcol = 8 * (lane >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            ldsm_x4(smem_addr(sQ + qrow * kPitch + (16 * ks + qcol) * 2), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    for (int tile = 0; tile < ntiles; ++tile) {
+        const int stage = nst > 1 ? (tile & 1) : 0;
+        const int base = s0 + tile * kTile + warp * kKeysPerWarp;   // first key of this warp
+        if (nst > 1 && tile + 1 < ntiles)
+            cp_async_wait_one_pending();
+        else
+            cp_async_wait_none_pending();
+        __syncthreads();
+        const unsigned char* sk = sKV + (size_t)stage * kKVStageBytes + (size_t)(warp * kKeysPerWarp) * kPitch;
+        const unsigned char* sv = sk + kTile * kPitch;
+
+        // S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys)
+        float s[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
+            const int krow = 8 * j + (lane & 7);
+            const int kcol = 8 * (lane >> 3);   // matrices: dims +0, +8, +16, +24 of a 32-dim slice
+#pragma unroll
+            for (int kp = 0; kp < 4; ++kp) {     // pairs of k-steps
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(smem_addr(sk + krow * kPitch + (32 * kp + kcol) * 2), b0, b1, b2, b3);
+                mma_bf16(s[j], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+                mma_bf16(s[j], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+            }
+        }
+
+        // scale to base 2, mask, store logits (focal), online softmax
+        float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hr = e >> 1;
+                const int pos = base + 8 * j + 2 * t4 + (e & 1);
+                bool ok = pos < s1 && pos <= lim[hr];
+                if (MODE == kModeSparse && ok && pos < p.kk) ok = s_tok[pos - s0] >= 0;
+                if (MODE == kModePrefix && ok && src.gathered && pos < src.np) ok = s_tok[pos - s0] >= 0;
+                const float x = ok ? s[j][e] * p.qscale : -INFINITY;
+                s[j][e] = x;
+                mx[hr] = fmaxf(mx[hr], x);
+            }
+        }
+        if (MODE == kModeFocal && p.logits != nullptr) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int row = r0 + g + 8 * hr;
+                if (row < p.R) {
+                    float* lrow = p.logits + (int64_t)(bh * p.R + row) * p.Tcap;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int pos = base + 8 * j + 2 * t4;
+                        if (pos < s1) lrow[pos] = s[j][2 * hr];
+                        if (pos + 1 < s1) lrow[pos + 1] = s[j][2 * hr + 1];
+                    }
+                }
+            }
+        }
+        float alpha[2], ms[2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 1));
+            mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 2));
+            const float mn = fmaxf(m_run[hr], mx[hr]);
+            ms[hr] = (mn == -INFINITY) ? 0.f : mn;
+            alpha[hr] = fast_exp2(m_run[hr] - ms[hr]);
+            m_run[hr] = mn;
+            l_run[hr] *= alpha[hr];
+        }
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            o[n][0] *= alpha[0];
+            o[n][1] *= alpha[0];
+            o[n][2] *= alpha[1];
+            o[n][3] *= alpha[1];
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float pe = fast_exp2(s[j][e] - ms[e >> 1]);
+                s[j][e] = pe;
+                l_run[e >> 1] += pe;
+            }
+        }
+
+        // O += P V over this warp's 16 keys (one k-step); P = hi + lo in bf16
+        {
+            uint32_t ph[4], pl[4];
+            split_bf16(s[0][0], s[0][1], ph[0], pl[0]);
+            split_bf16(s[0][2], s[0][3], ph[1], pl[1]);
+            split_bf16(s[1][0], s[1][1], ph[2], pl[2]);
+            split_bf16(s[1][2], s[1][3], ph[3], pl[3]);
+            const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int vcol = 8 * (lane >> 4);
+#pragma unroll
+            for (int np2 = 0; np2 < 8; ++np2) {   // pairs of 8-dim n-tiles
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * np2 + vcol) * 2), b0, b1, b2, b3);
+                mma_bf16(o[2 * np2], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                mma_bf16(o[2 * np2], pl[0], pl[1], pl[2], pl[3], b0, b1);
+                mma_bf16(o[2 * np2 + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+                mma_bf16(o[2 * np2 + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+            }
+        }
+
+        __syncthreads();   // every warp is done with this stage
+        if (tile + nst < ntiles) issue(tile + nst, stage);
+    }
+
+    // row sums over the quad
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        l_run[hr] += __shfl_xor_sync(kFull, l_run[hr], 1);
+        l_run[hr] += __shfl_xor_sync(kFull, l_run[hr], 2);
+    }
+
+    // ---- combine the warps into this CTA's partial (the stage buffers are free now) -------------
+    __shared__ float sm_m[kWarps][kRowsPerCta];
+    __shared__ float sm_l[kWarps][kRowsPerCta];
+    float* sm_o = reinterpret_cast<float*>(sKV);   // [kWarps][16][128]
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+        const int c = 8 * n + 2 * t4;
+        *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kHeadDim + c) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kHeadDim + c) = make_float2(o[n][2], o[n][3]);
+    }
+    if (t4 == 0) {
+        sm_m[warp][g] = m_run[0];
+        sm_m[warp][g + 8] = m_run[1];
+        sm_l[warp][g] = l_run[0];
+        sm_l[warp][g + 8] = l_run[1];
+    }
+    __syncthreads();
+
+    __shared__ float c_m[kRowsPerCta];
+    __shared__ float c_l[kRowsPerCta];
+    float* c_o = sm_o;   // [16][128]: combined in place over warp 0's slice (each element by its own thread)
+    const int nr = min(kRowsPerCta, p.R - r0);   // rows of this group that exist
+    for (int e = tid; e < nr * kHeadDim; e += kThreads) {
+        const int r = e >> 7;
+        const int c = e & (kHeadDim - 1);
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][r]);
         const float Ms = (M == -INFINITY) ? 0.f : M;
-        float sc[kWarps];
-        float Ls = 0.f;
+        float O = 0.f, Ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            sc[w] = fast_exp2(sm_m[w][r] - Ms);
-            Ls = fmaf(sm_l[w][r], sc[w], Ls);
+            const float sc = fast_exp2(sm_m[w][r] - Ms);
+            O = fmaf(sm_o[(w * kRowsPerCta + r) * kHeadDim + c], sc, O);
+            Ls = fmaf(sm_l[w][r], sc, Ls);
         }
-        for (int c = tid; c < kHeadDim; c += kThreads) {
-            float O = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) O = fmaf(sm_o[(w * RB + r) * kHeadDim + c], sc[w], O);
-            c_o[r][c] = O;
-        }
-        if (tid == 0) {
+        c_o[r * kHeadDim + c] = O;
+        if (c == 0) {
             c_m[r] = M;
             c_l[r] = Ls;
         }
     }
-    const int nr = min(RB, p.R - r0);   // rows of this row group that exist
 
     if (CLUSTER) {
         // every split of this (b, h, row group) is one CTA of the cluster: merge through distributed
@@ -509,14 +518,22 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const AttnParams 
         for (int e = (int)me * kThreads + tid; e < nr * kHeadDim; e += (int)cs * kThreads) {
             const int r = e >> 7;
             const int c = e & (kHeadDim - 1);
+            float mq[kMaxClusterSplits];
             float M = -INFINITY;
-            for (unsigned q = 0; q < cs; ++q) M = fmaxf(M, ld_cluster(cluster_map(&c_m[r], q)));
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q) {
+                mq[q] = (unsigned)q < cs ? ld_cluster(cluster_map(&c_m[r], q)) : -INFINITY;
+                M = fmaxf(M, mq[q]);
+            }
             const float Ms = (M == -INFINITY) ? 0.f : M;
             float Ls = 0.f, O = 0.f;
-            for (unsigned q = 0; q < cs; ++q) {
-                const float w = fast_exp2(ld_cluster(cluster_map(&c_m[r], q)) - Ms);
-                Ls = fmaf(ld_cluster(cluster_map(&c_l[r], q)), w, Ls);
-                O = fmaf(ld_cluster(cluster_map(&c_o[r][c], q)), w, O);
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q) {
+                if ((unsigned)q < cs) {
+                    const float w = fast_exp2(mq[q] - Ms);
+                    Ls = fmaf(ld_cluster(cluster_map(&c_l[r], q)), w, Ls);
+                    O = fmaf(ld_cluster(cluster_map(&c_o[r * kHeadDim + c], q)), w, O);
+                }
             }
             const int row = r0 + r;
             const int gi = row / p.Mq;
@@ -530,7 +547,7 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const AttnParams 
     __syncthreads();
     for (int r = 0; r < nr; ++r) {
         const int64_t pi = (int64_t)(bh * p.R + r0 + r) * p.nsplit + split;
-        for (int c = tid; c < kHeadDim; c += kThreads) p.part_o[pi * kHeadDim + c] = c_o[r][c];
+        for (int c = tid; c < kHeadDim; c += kThreads) p.part_o[pi * kHeadDim + c] = c_o[r * kHeadDim + c];
         if (tid == 0) {
             p.part_m[pi] = c_m[r];
             p.part_l[pi] = c_l[r];
@@ -576,6 +593,8 @@ __global__ void __launch_bounds__(kThreads) attn_decode_kernel(const AttnParams 
 //   s_j = sum_r exp2(t_rj - M_r) / Z_r   over the group's rows r, for cand_lo <= j < cand_hi.
 __global__ void __launch_bounds__(256) focal_combine_kernel(const FocalCombineParams p)
 {
+    griddep_wait();   // the partials and logits come from the kernel just before
+    griddep_launch();
     const int bh = blockIdx.y;
     const int b = bh / p.Hkv;
     const int h = bh - b * p.Hkv;
@@ -625,16 +644,16 @@ __global__ void __launch_bounds__(256) focal_combine_kernel(const FocalCombinePa
     }
 }
 
-template <int MODE, int RB, bool CLUSTER>
-cudaError_t launch_one(const AttnParams& p, cudaStream_t s)
+template <int MODE, bool CLUSTER>
+cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
 {
     static int configured = -1;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = attn_decode_kernel<MODE, RB, CLUSTER>;
+    auto kern = attn_tile_kernel<MODE, CLUSTER>;
     if (configured != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_smem_bytes(2, RB, kMaxSplitTokens));
+                                             (int)attn_smem_bytes(2, kMaxSplitTokens));
         if (e != cudaSuccess) return e;
         if (CLUSTER) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -642,58 +661,31 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t s)
         }
         configured = dev;
     }
-    const size_t smem = attn_smem_bytes(p.stages, RB, (MODE != kModeFocal && p.idx != nullptr) ? p.split_len : 0);
+    const size_t smem = attn_smem_bytes(p.stages, (MODE != kModeFocal && p.idx != nullptr) ? p.split_len : 0);
     dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
-    if (!CLUSTER) {
-        kern<<<grid, kThreads, smem, s>>>(p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)p.nsplit;   // every split of one (b, h, row group)
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
-}
-
-template <int MODE, bool CLUSTER>
-cudaError_t launch_mode(const AttnParams& p, int rb, cudaStream_t s)
-{
-    switch (rb) {
-    case 1: return launch_one<MODE, 1, CLUSTER>(p, s);
-    case 2: return launch_one<MODE, 2, CLUSTER>(p, s);
-    case 4: return launch_one<MODE, 4, CLUSTER>(p, s);
-    default: return launch_one<MODE, 8, CLUSTER>(p, s);
-    }
+    // with CLUSTER, every split of one (b, h, row group) is one CTA of a (1, nsplit, 1) cluster
+    return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, CLUSTER ? (unsigned)p.nsplit : 0u, p);
 }
 
 }  // namespace
 
-cudaError_t launch_attn_partial(const AttnParams& p, int mode, int rb, cudaStream_t s)
+cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s)
 {
-    if (mode == kModeFocal) return launch_mode<kModeFocal, false>(p, rb, s);
+    if (mode == kModeFocal) return launch_one<kModeFocal, false>(p, pdl, s);
     const bool cl = p.nsplit <= kMaxClusterSplits;
     if (mode == kModeSparse)
-        return cl ? launch_mode<kModeSparse, true>(p, rb, s) : launch_mode<kModeSparse, false>(p, rb, s);
-    return cl ? launch_mode<kModePrefix, true>(p, rb, s) : launch_mode<kModePrefix, false>(p, rb, s);
+        return cl ? launch_one<kModeSparse, true>(p, pdl, s) : launch_one<kModeSparse, false>(p, pdl, s);
+    return cl ? launch_one<kModePrefix, true>(p, pdl, s) : launch_one<kModePrefix, false>(p, pdl, s);
 }
 
-cudaError_t launch_focal_combine(const FocalCombineParams& p, cudaStream_t s)
+cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s)
 {
     const int ncand = p.scores ? (p.cand_hi - p.cand_lo) : 0;
     int gx = (ncand + 1023) / 1024;
     if (gx < 1) gx = 1;
     if (gx > 256) gx = 256;
     dim3 grid(gx, p.B * p.Hkv);
-    focal_combine_kernel<<<grid, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(focal_combine_kernel, grid, dim3(256), 0, s, pdl, 0u, p);
 }
 
 }  // namespace fx

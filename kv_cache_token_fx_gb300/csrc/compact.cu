@@ -26,6 +26,8 @@ __device__ __forceinline__ uint4 ld_nc16(const uint16_t* ptr)
 
 __global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams p)
 {
+    griddep_wait();
+    griddep_launch();
     const int h = blockIdx.y;
     const int b = blockIdx.z % p.B;
     const int layer = blockIdx.z / p.B;
@@ -82,13 +84,12 @@ __global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams
 
 }  // namespace
 
-cudaError_t launch_compact(const CompactParams& p, cudaStream_t s)
+cudaError_t launch_compact(const CompactParams& p, bool pdl, cudaStream_t s)
 {
     const int rows_per_cta = kRowsPerIter * kRowsPerThread;
     dim3 grid((p.max_rows + rows_per_cta - 1) / rows_per_cta, p.Hkv, p.B * p.n_layers);
     if (grid.x == 0) grid.x = 1;
-    compact_kernel<<<grid, kCpThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(compact_kernel, grid, dim3(kCpThreads), 0, s, pdl, 0u, p);
 }
 
 }  // namespace fx

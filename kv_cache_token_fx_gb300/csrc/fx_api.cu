@@ -11,7 +11,7 @@ using namespace fx;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;
 
@@ -81,42 +81,27 @@ struct Plan {
     int rb, nrg, nsplit, split_len, stages;
 };
 
-// Resident attention CTAs per SM (64 threads each; ~19 KB of shared memory with one staged tile,
-// ~36 KB with two; registers allow about 8).
-constexpr int kResidentOneStage = 8;
-constexpr int kResidentTwoStage = 6;
-
 // `merge_in_cluster`: the splits of one (b, h, row group) are merged inside a thread-block cluster
-// (sparse and prefix calls), which needs at most kMaxClusterSplits splits; the focal call merges in
-// its combine kernel and may use any number of splits.
-Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_cluster = false)
+// (sparse and prefix calls), which needs at most kMaxClusterSplits splits.  Gathered modes also keep
+// each split within kMaxSplitTokens keys (the index table lives in shared memory).  Small calls get
+// about two CTAs per SM in a single wave; large ones at least four full waves.
+Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_cluster = false, bool gathered = false)
 {
     Plan pl;
     pl.rb = rows_per_block(R);
     pl.nrg = cdiv(R, pl.rb);
     const int keys = max_keys > 0 ? max_keys : 1;
     const int per_split = pairs * pl.nrg;
-    const int tiles = cdiv(keys, kTile);
-    if (merge_in_cluster && cdiv(tiles, kMaxClusterSplits) * kTile <= kMaxSplitTokens) {
-        const int ns = tiles < kMaxClusterSplits ? tiles : kMaxClusterSplits;
-        pl.split_len = cdiv(cdiv(keys, ns), kTile) * kTile;
-        pl.nsplit = cdiv(keys, pl.split_len);
-        pl.stages = pl.split_len > kTile ? 2 : 1;
-        return pl;
-    }
-    if ((int64_t)per_split * tiles <= (int64_t)kResidentOneStage * sm_count) {
-        // every tile gets its own CTA and the whole call fits in one wave
-        pl.nsplit = tiles;
-        pl.split_len = kTile;
-        pl.stages = 1;
-        return pl;
-    }
-    int ns = kResidentTwoStage * sm_count / per_split;
-    if (ns < 1) ns = 1;
-    const int min_ns = cdiv(keys, kMaxSplitTokens);
+    // Small calls: as many splits as fill one wave of resident CTAs (every SM gets the same number of
+    // CTAs, so no SM carries extra work).  Large calls: at least four waves.
+    const int resident = kResidentPerSm * sm_count;
+    int ns = per_split >= resident ? cdiv(4 * resident, per_split) : resident / per_split;
+    const int min_ns = gathered ? cdiv(keys, kMaxSplitTokens) : 1;
     if (ns < min_ns) ns = min_ns;
-    if (ns > tiles) ns = tiles;
-    pl.split_len = cdiv(cdiv(keys, ns), kTile) * kTile;
+    if (ns > cdiv(keys, 16)) ns = cdiv(keys, 16);
+    if (merge_in_cluster && ns > kMaxClusterSplits && min_ns <= kMaxClusterSplits) ns = kMaxClusterSplits;
+    if (ns < 1) ns = 1;
+    pl.split_len = cdiv(cdiv(keys, ns), 16) * 16;   // the last tile of a split may be partial
     pl.nsplit = cdiv(keys, pl.split_len);
     pl.stages = pl.split_len > kTile ? 2 : 1;
     return pl;
@@ -183,6 +168,12 @@ fx_status check_ws(void* ws, size_t ws_bytes, size_t need)
 
 float log2e_scale(float scale) { return scale * 1.4426950408889634f; }
 
+fx_status check_flags(unsigned flags)
+{
+    if (flags & ~(FX_LAUNCH_PDL | FX_LAUNCH_INPUTS_READY)) return fail(FX_ERR_INVALID_ARG, "unknown launch flags 0x%x", flags);
+    return FX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,10 +220,11 @@ size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap)
 
 fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,
                                float scale, int cand_lo, int cand_hi, float* out, float* scores,
-                               void* ws, size_t ws_bytes, void* stream)
+                               void* ws, size_t ws_bytes, unsigned flags, void* stream)
 {
     fx_status st = check_kv(kv, "kv");
     if (st != FX_OK) return st;
+    if ((st = check_flags(flags)) != FX_OK) return st;
     if ((st = check_heads(Hq, kv->Hkv, Mq)) != FX_OK) return st;
     if (!q || !aligned16(q)) return fail(FX_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
     if (!out && !scores) return fail(FX_ERR_INVALID_ARG, "out and scores are both NULL");
@@ -280,7 +272,9 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     p.logits = scores ? reinterpret_cast<float*>(w + L.logits) : nullptr;
     p.err = ds->err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_attn_partial(p, kModeFocal, pl.rb, s);
+    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+    p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
+    cudaError_t e = launch_attn_partial(p, kModeFocal, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e, "focal attention launch");
 
     FocalCombineParams c;
@@ -302,18 +296,19 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     c.out = out;
     c.scores = scores;
     c.err = ds->err;
-    e = launch_focal_combine(c, s);
+    e = launch_focal_combine(c, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e, "focal combine launch");
     return FX_OK;
 }
 
 // ---------------------------------------------------------------------------------------------
 fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int32_t* prev_idx,
-                         int32_t* idx_out, void* stream)
+                         int32_t* idx_out, unsigned flags, void* stream)
 {
     if (!scores || !idx_out) return fail(FX_ERR_INVALID_ARG, "scores and idx_out must be non-NULL");
     if (rows < 1) return fail(FX_ERR_INVALID_ARG, "rows must be >= 1");
     if (k < 1 || k > n) return fail(FX_ERR_INVALID_ARG, "need 1 <= k (%d) <= n (%d)", k, n);
+    if (check_flags(flags) != FX_OK) return FX_ERR_INVALID_ARG;
     DeviceState* ds = nullptr;
     fx_status st = device_state(&ds);
     if (st != FX_OK) return st;
@@ -325,7 +320,7 @@ fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int3
     p.prev = prev_idx;
     p.out = idx_out;
     p.err = ds->err;
-    cudaError_t e = launch_topk(p, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_topk(p, (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
     return FX_OK;
 }
@@ -336,16 +331,17 @@ size_t fx_sparse_workspace_bytes(int B, int Hkv, int Hq, int k, int tail_lo, int
     if (B < 1 || Hkv < 1 || Hq < Hkv || k < 0 || tail_lo < 0 || Tcap < 0) return 0;
     const int R = Hq / Hkv;
     const int max_keys = k + (Tcap > tail_lo ? Tcap - tail_lo : 0);
-    const Plan pl = make_plan(B * Hkv, R, max_keys, sm_count_or_default(), true);
+    const Plan pl = make_plan(B * Hkv, R, max_keys, sm_count_or_default(), true, k > 0);
     return make_layout(B * Hkv, R, pl, 0, true).total;
 }
 
 fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, const int32_t* idx,
                                int k, int tail_lo, float scale, float* out, void* ws,
-                               size_t ws_bytes, void* stream)
+                               size_t ws_bytes, unsigned flags, void* stream)
 {
     fx_status st = check_kv(kv, "kv");
     if (st != FX_OK) return st;
+    if ((st = check_flags(flags)) != FX_OK) return st;
     if ((st = check_heads(Hq, kv->Hkv, 1)) != FX_OK) return st;
     if (!q || !aligned16(q)) return fail(FX_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
     if (!out) return fail(FX_ERR_INVALID_ARG, "out is NULL");
@@ -359,7 +355,7 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     const int G = Hq / kv->Hkv;
     const int R = G;
     const int max_keys = k + (kv->Tcap > tail_lo ? kv->Tcap - tail_lo : 0);
-    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true);
+    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true, k > 0);
     const Layout L = make_layout(pairs, R, pl, 0, true);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
     if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
@@ -396,7 +392,9 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     p.counters = reinterpret_cast<unsigned*>(w + L.counters);
     p.out = out;
     p.err = ds->err;
-    cudaError_t e = launch_attn_partial(p, kModeSparse, pl.rb, static_cast<cudaStream_t>(stream));
+    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+    p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
+    cudaError_t e = launch_attn_partial(p, kModeSparse, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse decode launch");
     return FX_OK;
 }
@@ -404,10 +402,11 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
 // ---------------------------------------------------------------------------------------------
 fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx, int k,
                         int tail_lo, const fx_kv_out_desc* dst, int64_t dst_stride_layer,
-                        int n_layers, void* stream)
+                        int n_layers, unsigned flags, void* stream)
 {
     fx_status st = check_kv(src, "src");
     if (st != FX_OK) return st;
+    if ((st = check_flags(flags)) != FX_OK) return st;
     if (!dst) return fail(FX_ERR_INVALID_ARG, "dst is NULL");
     fx_kv_desc dview = {dst->k, dst->v, dst->len, dst->stride_b, dst->stride_h, dst->stride_t,
                         dst->B, dst->Hkv, dst->Tcap, dst->d};
@@ -449,7 +448,7 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
     const int max_rows = k + (src->Tcap > tail_lo ? src->Tcap - tail_lo : 0);
     p.max_rows = max_rows < dst->Tcap ? max_rows : dst->Tcap;
     p.err = ds->err;
-    cudaError_t e = launch_compact(p, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_compact(p, (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "compaction launch");
     return FX_OK;
 }
@@ -460,15 +459,17 @@ size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np,
     if (Br < 1 || Hkv < 1 || Hq < Hkv || Mq < 1 || np < 0 || max_suffix < 0) return 0;
     const int R = (Hq / Hkv) * Mq;
     const int max_keys = np + max_suffix + Mq;
-    const Plan pl = make_plan(Br * Hkv, R, max_keys, sm_count_or_default(), true);
+    const Plan pl = make_plan(Br * Hkv, R, max_keys, sm_count_or_default(), true, np > 0);
     return make_layout(Br * Hkv, R, pl, 0, true).total;
 }
 
 fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_desc* br,
                                   const fx_bf16* q, int Hq, const int32_t* prefix_idx, int kp,
-                                  float scale, float* out, void* ws, size_t ws_bytes, void* stream)
+                                  float scale, float* out, void* ws, size_t ws_bytes, unsigned flags,
+                                  void* stream)
 {
     if (!prefix || !br) return fail(FX_ERR_INVALID_ARG, "prefix and branches must be non-NULL");
+    if (check_flags(flags) != FX_OK) return FX_ERR_INVALID_ARG;
     if (prefix->d != kHeadDim) return fail(FX_ERR_UNSUPPORTED, "head dim %d (only 128 is implemented)", prefix->d);
     if (prefix->P < 0 || prefix->Hkv < 1) return fail(FX_ERR_INVALID_ARG, "need P >= 0 and Hkv >= 1");
     if (!prefix->k || !prefix->v) return fail(FX_ERR_INVALID_ARG, "prefix k/v are NULL");
@@ -500,7 +501,7 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     const int R = G * br->Mq;
     const int np = prefix_idx ? kp : prefix->P;
     const int max_keys = np + br->max_suffix + br->Mq;
-    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true);
+    const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true, prefix_idx != nullptr);
     const Layout L = make_layout(pairs, R, pl, 0, true);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
     if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
@@ -548,7 +549,9 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     p.counters = reinterpret_cast<unsigned*>(w + L.counters);
     p.out = out;
     p.err = ds->err;
-    cudaError_t e = launch_attn_partial(p, kModePrefix, pl.rb, static_cast<cudaStream_t>(stream));
+    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+    p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
+    cudaError_t e = launch_attn_partial(p, kModePrefix, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix decode launch");
     return FX_OK;
 }

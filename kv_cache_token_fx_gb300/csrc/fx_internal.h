@@ -4,33 +4,39 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "fx.h"
 
 namespace fx {
 
 constexpr int kHeadDim = 128;
 constexpr int kMaxRows = 64;   // G * Mq limit per KV head
-constexpr int kWarps = 2;                               // warps per attention CTA
+constexpr int kWarps = 4;                               // warps per attention CTA
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row (256 bytes)
-constexpr int kTile = 32 * kWarps;                      // keys per tile: one key per thread
-constexpr int kKPitch = kRowBytes + 16;                 // staged K row pitch: 16-byte pad keeps the
-                                                        // lane-per-row 16-byte reads conflict-free
-constexpr int kKStageBytes = kTile * kKPitch;           // 17 KB per staged tile of K
-constexpr int kMaxSplitTokens = 4096;                   // longest split (bounds the index table)
+constexpr int kTile = 64;                               // keys per staged tile
+constexpr int kKeysPerWarp = kTile / kWarps;            // 16: two n-tiles of the S = Q K^T MMA
+constexpr int kRowsPerCta = 16;                         // query rows per CTA: one m16 MMA tile
+constexpr int kPitch = kRowBytes + 16;                  // staged row pitch: the 16-byte pad puts the 8
+                                                        // rows of an ldmatrix on 8 distinct bank groups
+constexpr int kQTileBytes = kRowsPerCta * kPitch;       // bf16 query tile
+constexpr int kKVStageBytes = 2 * kTile * kPitch;       // K and V rows of one tile (34 KB)
+constexpr int kMaxSplitTokens = 4096;                   // longest gathered split (bounds the index table)
 constexpr unsigned kSpinLimit = 1u << 22;               // bounded mbarrier waits
 constexpr int kMaxClusterSplits = 16;                   // splits merged inside one thread-block cluster
+constexpr int kResidentPerSm = 3;                       // attention CTAs that fit one SM (shared memory)
 // Arrival counters of the last-CTA merge live in a fixed region at the start of every workspace
-// (one slot per (b, h, row group); grid.z <= 65535 and at most 8 row groups), so no other data of
+// (one slot per (b, h, row group); grid.z <= 65535 and at most 4 row groups), so no other data of
 // any call ever overlaps them and they stay zero between calls.
-constexpr size_t kCounterSlots = 65536u * 8u;
+constexpr size_t kCounterSlots = 65536u * 4u;
 constexpr size_t kCounterBytes = kCounterSlots * sizeof(unsigned);
 
-// Dynamic shared memory of one attention CTA: mbarriers, `stages` K tiles, the query rows (fp32)
-// and the gathered-index table of its split.
-inline size_t attn_smem_bytes(int stages, int rb, int gathered_split_len)
+// Dynamic shared memory of one attention CTA: mbarriers, the query tile, `stages` K+V tiles and the
+// gathered-index table of its split.
+inline size_t attn_smem_bytes(int stages, int gathered_split_len)
 {
-    return 128 + (size_t)stages * kKStageBytes + (size_t)rb * kHeadDim * sizeof(float) +
+    return 128 + (size_t)kQTileBytes + (size_t)stages * kKVStageBytes +
            (size_t)(gathered_split_len > 0 ? gathered_split_len : 0) * sizeof(int);
 }
 
@@ -69,6 +75,7 @@ struct AttnParams {
     int64_t dr_sb, dr_si, dr_sh;
     // split geometry
     int nsplit, split_len, nrg, stages;
+    int prefetch;   // lengths / indices / K-V rows may be read before the preceding kernel finishes
     // outputs / scratch
     float* part_m;        // [B*Hkv*R*nsplit]
     float* part_l;        // [B*Hkv*R*nsplit]
@@ -116,13 +123,51 @@ struct CompactParams {
     unsigned* err;
 };
 
-// Launchers (return cudaGetLastError() of the launch).
-cudaError_t launch_attn_partial(const AttnParams& p, int mode, int rb, cudaStream_t s);
-cudaError_t launch_focal_combine(const FocalCombineParams& p, cudaStream_t s);
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
-cudaError_t launch_compact(const CompactParams& p, cudaStream_t s);
+// Launchers.  `pdl`: launch as a programmatic dependent of the preceding kernel on the stream.
+cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s);
+cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
+cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s);
+cudaError_t launch_compact(const CompactParams& p, bool pdl, cudaStream_t s);
 
-// Row-group width used for a given number of query rows per KV head.
-inline int rows_per_block(int R) { return R <= 1 ? 1 : (R <= 2 ? 2 : (R <= 4 ? 4 : 8)); }
+// Launch `kern` with optional programmatic stream serialization and a (1, cluster_y, 1) cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          unsigned cluster_y, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_y > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1;
+        attr[n].val.clusterDim.y = cluster_y;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+// Programmatic dependent launch: wait until the preceding kernel on the stream has finished and its
+// writes are visible (a no-op for a kernel launched without the attribute), and let the next kernel
+// start launching.  Every kernel here triggers only after its own wait, so when a kernel starts,
+// everything enqueued two or more launches before it has finished.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
+// Row-group width used for a given number of query rows per KV head (one 16-row MMA tile).
+inline int rows_per_block(int /*R*/) { return kRowsPerCta; }
 
 }  // namespace fx

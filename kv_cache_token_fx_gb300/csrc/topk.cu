@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
     __shared__ uint32_t swarp[33];
     __shared__ uint32_t s_digit, s_gt, s_thr, s_bad;
 
+    griddep_wait();   // the scores usually come from the kernel just before
+    griddep_launch();
     const int row = blockIdx.x;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t s)
+cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s)
 {
     if (p.n <= kSmemKeys) {
         const size_t smem = (size_t)p.n * sizeof(uint32_t);
@@ -241,11 +243,9 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s)
             if (e != cudaSuccess) return e;
             configured_device = dev;
         }
-        topk_kernel<true><<<p.rows, kTkThreads, smem, s>>>(p);
-    } else {
-        topk_kernel<false><<<p.rows, kTkThreads, 0, s>>>(p);
+        return launch_kernel(topk_kernel<true>, dim3(p.rows), dim3(kTkThreads), smem, s, pdl, 0u, p);
     }
-    return cudaGetLastError();
+    return launch_kernel(topk_kernel<false>, dim3(p.rows), dim3(kTkThreads), 0, s, pdl, 0u, p);
 }
 
 }  // namespace fx

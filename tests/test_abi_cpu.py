@@ -41,17 +41,19 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_argument_checks_without_gpu(lib):
     lib.fx_last_error.restype = ctypes.c_char_p
     lib.fx_abi_version.restype = ctypes.c_int
-    assert lib.fx_abi_version() == 1
+    assert lib.fx_abi_version() == 2
     lib.fx_topk_select.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                                   ctypes.c_void_p, ctypes.c_void_p]
-    assert lib.fx_topk_select(None, 1, 4, 2, None, None, None) == 1
+                                   ctypes.c_void_p, ctypes.c_uint, ctypes.c_void_p]
+    assert lib.fx_topk_select(None, 1, 4, 2, None, None, 0, None) == 1
     assert b"non-NULL" in lib.fx_last_error()
     fake = ctypes.c_void_p(256)
-    assert lib.fx_topk_select(fake, 1, 4, 5, None, fake, None) == 1       # k > n
+    assert lib.fx_topk_select(fake, 1, 4, 5, None, fake, 0, None) == 1       # k > n
     assert b"k (5) <= n (4)" in lib.fx_last_error()
+    assert lib.fx_topk_select(fake, 1, 4, 2, None, fake, 0x80, None) == 1    # unknown launch flag
+    assert b"unknown launch flags" in lib.fx_last_error()
     lib.fx_focal_attn_scores.restype = ctypes.c_int
     assert lib.fx_focal_attn_scores(None, None, 1, 1, -1, ctypes.c_float(1.0), 0, 0, None, None, None,
-                                    ctypes.c_size_t(0), None) == 1
+                                    ctypes.c_size_t(0), ctypes.c_uint(0), None) == 1
     lib.fx_sparse_workspace_bytes.restype = ctypes.c_size_t
     assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) > 0
     assert lib.fx_sparse_workspace_bytes(0, 8, 16, 205, 4096, 4864) == 0

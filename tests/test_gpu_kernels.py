@@ -317,3 +317,31 @@ def test_sparse_split_counts(fx, n_keys):
     ref = oracle.sparse_decode(k, v, length, q, None, 0)
     out = fx.fx_sparse_gqa_decode(dev(k), dev(v), dev(length), dev(q), None, 0)
     pu.assert_out_close(out, ref, float(v.float().abs().max()))
+
+
+def test_programmatic_dependent_launch_chain_is_identical(fx):
+    """The same focal -> top-k -> sparse -> sparse chain launched plainly and as programmatic dependent
+    launches (with and without early input reads) gives bit-identical results."""
+    B, Hkv, G, T, kk = 2, 2, 2, 900, 40
+    k, v = kv_case(B, Hkv, T, 101)
+    q1, q2, q3 = (rnd((B, Hkv * G, 1, D), 101, s) for s in (3, 4, 5))
+    length = torch.tensor([T, 777], dtype=torch.int32)
+    dk, dv, dl = dev(k), dev(v), dev(length)
+
+    def chain(flags_focal, flags_topk, flags_sp1, flags_sp2):
+        out0, sc = fx.fx_focal_attn_scores(dk, dv, dl, dev(q1), cand=(0, 700), flags=flags_focal)
+        idx = fx.fx_topk_select(sc, kk, flags=flags_topk)
+        o1 = fx.fx_sparse_gqa_decode(dk, dv, dl, dev(q2), idx, 700, flags=flags_sp1)
+        o2 = fx.fx_sparse_gqa_decode(dk, dv, dl, dev(q3), idx, 700, flags=flags_sp2)
+        torch.cuda.synchronize()
+        return [t.clone() for t in (out0, sc, idx, o1, o2)]
+
+    P, R = fx.FX_LAUNCH_PDL, fx.FX_LAUNCH_INPUTS_READY
+    plain = chain(0, 0, 0, 0)
+    for variant in ((P, P, P, P), (P | R, P, P, P | R)):
+        got = chain(*variant)
+        for a, b in zip(plain, got):
+            assert torch.equal(a, b)
+    assert fx.fx_device_errors() == 0
+    ref = oracle.sparse_decode(k, v, length, q3, plain[2].cpu(), 700)
+    pu.assert_out_close(plain[4], ref, float(v.float().abs().max()))
