@@ -1,6 +1,8 @@
 // Host side of libfx: argument checks, workspace planning, kernel launches and the device error word.
 // Every entry point is extern "C" and declared in include/fx.h.
 #include <math.h>
+
+#include <algorithm>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -92,10 +94,18 @@ Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_clust
     pl.nrg = cdiv(R, pl.rb);
     const int keys = max_keys > 0 ? max_keys : 1;
     const int per_split = pairs * pl.nrg;
-    // Small calls: as many splits as fill one wave of resident CTAs (every SM gets the same number of
-    // CTAs, so no SM carries extra work).  Large calls: at least four waves.
+    // Small calls: enough splits to give every SM work in one wave -- about one wave of resident CTAs
+    // for the focal call; for calls merged in a cluster, about 1.5 CTAs per SM, because larger clusters
+    // of large CTAs are harder to place (measured on the decode shapes: 4 splits of ~250 keys beat
+    // 6, 8 and 16).  Large calls: at least four waves.
     const int resident = kResidentPerSm * sm_count;
-    int ns = per_split >= resident ? cdiv(4 * resident, per_split) : resident / per_split;
+    int ns;
+    if (per_split >= resident)
+        ns = cdiv(4 * resident, per_split);
+    else if (merge_in_cluster)
+        ns = std::min(resident / per_split, cdiv(3 * sm_count / 2, per_split));
+    else
+        ns = resident / per_split;
     const int min_ns = gathered ? cdiv(keys, kMaxSplitTokens) : 1;
     if (ns < min_ns) ns = min_ns;
     if (ns > cdiv(keys, 16)) ns = cdiv(keys, 16);
