@@ -254,6 +254,28 @@ FX_API fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_
                                   float scale, float* out, void* ws, size_t ws_bytes, unsigned flags,
                                   void* stream);
 
+/* ------------------------------------------------------------------------------------------- */
+/* fx_focal_attn_scores_noalloc -- fx_focal_attn_scores for callers that cannot allocate device
+ * memory.  The pages have no counterpart for this call; it is a convenience of this library.
+ *
+ * Who needs it: code that runs while a CUDA graph is being captured (allocating there is refused or
+ * forces a device-wide synchronisation that breaks the capture), real-time loops that allow no
+ * allocator calls after start-up, and hosts that reach the GPU only through this C interface.
+ *
+ * Same arguments and results as fx_focal_attn_scores, without ws / ws_bytes: the scratch is one
+ * fixed device array inside the library, fx_noalloc_scratch_bytes() = 16 MiB, which every GPU that
+ * loads the library holds until the process exits.  A call whose fx_focal_workspace_bytes() exceeds
+ * that size returns FX_ERR_UNSUPPORTED and launches nothing.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture.  All calls on a device share the one array and leave their data in it; nothing in it has
+ * to start at zero.  Calls that can overlap on the GPU (for example on two streams) race on the
+ * array: the caller must order them.  The call allocates nothing.
+ */
+FX_API size_t fx_noalloc_scratch_bytes(void);
+FX_API fx_status fx_focal_attn_scores_noalloc(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq,
+                                              int q_pos0, float scale, int cand_lo, int cand_hi,
+                                              float* out, float* scores, unsigned flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -186,6 +186,8 @@ fx_status check_flags(unsigned flags)
 
 }  // namespace
 
+fx_status fx::set_error(fx_status st, const char* msg) { return fail(st, "%s", msg); }
+
 extern "C" {
 
 const char* fx_last_error(void) { return g_msg; }

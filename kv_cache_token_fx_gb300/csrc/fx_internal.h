@@ -123,6 +123,9 @@ struct CompactParams {
     unsigned* err;
 };
 
+// Sets the calling thread's error message (read back by fx_last_error) and returns `st`.
+fx_status set_error(fx_status st, const char* msg);
+
 // Launchers.  `pdl`: launch as a programmatic dependent of the preceding kernel on the stream.
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
