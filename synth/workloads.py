@@ -309,6 +309,28 @@ class HpdBranch:
         off[1:] = torch.cumsum(L, 0)
         return off.to(torch.int32)
 
+    def suffix_rows(self, layer, b, device="cpu"):
+        """Suffix K, V rows of branch b only: [Hkv, L_b, 128] each (same values as layer_inputs)."""
+        off = self.offsets()
+        o0, o1 = int(off[b]), int(off[b + 1])
+        smax = self.Br * self.max_suffix
+        ks, vs = [], []
+        for h in range(self.Hkv):
+            ks.append(normal_bf16(self.seed, stream_id(_SUFK, layer), (o1 - o0, D), device=device,
+                                  offset=(h * smax + o0) * D))
+            vs.append(normal_bf16(self.seed, stream_id(_SUFV, layer), (o1 - o0, D), device=device,
+                                  offset=(h * smax + o0) * D))
+        return torch.stack(ks), torch.stack(vs)
+
+    def small_inputs(self, layer, device="cpu"):
+        """Everything but the suffixes: prefix [Hkv, P, 128], draft [Br, Mq, Hkv, 128], q [Br, Hq, Mq, 128]."""
+        return dict(
+            pk=normal_bf16(self.seed, stream_id(_PREK, layer), (self.Hkv, self.P, D), device=device),
+            pv=normal_bf16(self.seed, stream_id(_PREV, layer), (self.Hkv, self.P, D), device=device),
+            dk=normal_bf16(self.seed, stream_id(_DRK, layer), (self.Br, self.Mq, self.Hkv, D), device=device),
+            dv=normal_bf16(self.seed, stream_id(_DRV, layer), (self.Br, self.Mq, self.Hkv, D), device=device),
+            q=normal_bf16(self.seed, stream_id(_Q, layer), (self.Br, self.Hq, self.Mq, D), device=device))
+
     def layer_inputs(self, layer, device="cpu", Br=None):
         """prefix K/V [Hkv, P, 128]; suffix K/V [Hkv, S, 128]; offsets [Br+1]; draft K/V [Br, Mq, Hkv, 128];
         q [Br, Hq, Mq, 128].  Br defaults to all 512 branches; a smaller Br takes the first branches."""

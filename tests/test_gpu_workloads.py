@@ -1,0 +1,214 @@
+"""Parity at the full workload sizes, on sampled rows.
+
+The device runs each workload end to end through the library at its full size; the fp64 oracle then
+recomputes sampled (sequence / branch, KV head) rows from host-regenerated inputs (the generator is
+bit-identical on both devices, checked first) and the two are compared:
+  outputs      max |gpu - oracle| <= 2e-3 * max|V|
+  importance   relative 1e-4
+  index sets   exact on rows whose oracle rank-k / rank-(k+1) gap is >= 1e-3; otherwise the
+               tie-tolerant check; outputs that depend on a set are compared where the two sets agree
+  compaction   bit-exact
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.workloads import D, HpdBranch, KvSelect, LongCtx, OcrDecode
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import kv_cache_token_fx_gb300 as fx
+    fx.load_library()
+
+
+def _as_kv(rows):
+    return rows.view(1, 1, *rows.shape).contiguous()
+
+
+def test_generator_is_bit_identical_across_devices():
+    s = synth.stream_id(3, 9)
+    a = synth.normal_bf16(7, s, (3, 1000), device="cuda", offset=123456789012).cpu()
+    b = synth.normal_bf16(7, s, (3, 1000), device="cpu", offset=123456789012)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    w = OcrDecode()
+    tab = w.fourier_table(5)
+    k, v = w.layer_kv(5, device="cuda", table=tab)
+    kr, vr = w.layer_kv_rows(5, 3, 6, table=tab)
+    assert torch.equal(k[3, 6].cpu().view(torch.int16), kr.view(torch.int16))
+    assert torch.equal(v[3, 6].cpu().view(torch.int16), vr.view(torch.int16))
+    assert torch.equal(w.query(9, 5, device="cuda", table=tab).cpu().view(torch.int16),
+                       w.query(9, 5, table=tab).view(torch.int16))
+    ks = KvSelect()
+    k15, _ = ks.layer_kv(ks.switch_layer, device="cuda")
+    r15, _ = ks.layer_kv_rows(ks.switch_layer, 2, 3)
+    assert torch.equal(k15[2, 3].cpu().view(torch.int16), r15.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------------------------
+def test_ocr_decode_full_run_sampled():
+    from tests.workload_runs import ocr_decode_run
+    w = OcrDecode()
+    keep = (0, 1, 2, 131, 255)
+    gpu = ocr_decode_run(w, set(keep))
+    G = w.Hq // w.Hkv
+    pairs = [(0, 0), (3, 5), (7, 7)]
+    layers_check = (0, 2, 3, 5, 14, 20, 27)
+    tables = {}
+    stats = dict(rows=0, gapped=0, exact=0, sparse_checked=0)
+    for t in keep:
+        L_t = w.length_at(t)
+        ln = torch.tensor([L_t], dtype=torch.int32)
+        for b, h in pairs:
+            # the oracle's own sets at this step (and layer 14's at the previous step)
+            own = {}
+            for (l, tt) in ((3, t), (14, t)) + (((14, t - 1),) if t > 0 else ()):
+                tab = tables.setdefault(l, w.fourier_table(l))
+                kr, vr = w.layer_kv_rows(l, b, h, table=tab)
+                q = w.query(tt, l, table=tab)[b:b + 1, h * G:(h + 1) * G].contiguous()
+                lnt = torch.tensor([w.length_at(tt)], dtype=torch.int32)
+                out, sc = oracle.focal(_as_kv(kr), _as_kv(vr), lnt, q, cand=(0, w.n_vis))
+                own[(l, tt)] = (oracle.topk(sc, w.k_keep)[0, 0], sc[0, 0], out)
+            for l in layers_check:
+                tab = tables.setdefault(l, w.fourier_table(l))
+                kr, vr = w.layer_kv_rows(l, b, h, table=tab)
+                q = w.query(t, l, table=tab)[b:b + 1, h * G:(h + 1) * G].contiguous()
+                vmax = float(vr.float().abs().max())
+                g_out = gpu[t]["out"][l, b, h * G:(h + 1) * G]
+                if l in w.focal_layers:
+                    ref_idx, ref_sc, ref_out = own[(l, t)]
+                    pu.assert_out_close(g_out, ref_out[0], vmax, f"t{t} l{l} focal out")
+                    pu.assert_scores_close(gpu[t]["scores"][l][b, h], ref_sc, f"t{t} l{l} scores")
+                    r, gp, ex = pu.check_index_sets(gpu[t]["sets"][l][b, h].view(1, -1), ref_idx.reshape(1, -1),
+                                                     ref_sc.reshape(1, -1), w.k_keep)
+                    stats["rows"] += r
+                    stats["gapped"] += gp
+                    stats["exact"] += ex
+                    continue
+                if l < 3:
+                    if t == 0:
+                        ref = oracle.sparse_decode(_as_kv(kr), _as_kv(vr), ln, q, None, 0)
+                        pu.assert_out_close(g_out, ref[0], vmax, f"t{t} l{l} dense")
+                        stats["sparse_checked"] += 1
+                        continue
+                    src_layer, src_t, gpu_set = 14, t - 1, gpu[t]["prev14"][b, h]
+                elif l < 14:
+                    src_layer, src_t, gpu_set = 3, t, gpu[t]["sets"][3][b, h]
+                else:
+                    src_layer, src_t, gpu_set = 14, t, gpu[t]["sets"][14][b, h]
+                ref_set = own[(src_layer, src_t)][0]
+                if not np.array_equal(gpu_set.numpy(), ref_set):
+                    continue      # a near-tie resolved the other way; the set itself was checked above
+                ref = oracle.sparse_decode(_as_kv(kr), _as_kv(vr), ln, q,
+                                           torch.from_numpy(ref_set).view(1, 1, -1), w.n_vis)
+                pu.assert_out_close(g_out, ref[0], vmax, f"t{t} l{l} sparse")
+                stats["sparse_checked"] += 1
+    assert stats["sparse_checked"] >= 0.6 * len(keep) * len(pairs) * 5
+    print("ocr_decode sampled:", stats)
+
+
+# ----------------------------------------------------------------------------------------------
+def test_kv_select_full_sampled():
+    from tests.workload_runs import kv_select_run
+    w = KvSelect()
+    sample_layers = (0, w.switch_layer, w.n_layers - 1)
+    steps = (0, 1, w.decode_steps - 1)
+    gpu = kv_select_run(w, steps, sample_layers)
+    T, G, ncand = w.T, w.Hq // w.Hkv, w.T - w.window
+    assert gpu["clen"].tolist() == [w.keep] * w.B
+    qw = w.window_queries("cpu")
+    appended = {l: w.appended_kv(l) for l in sample_layers}
+    for b, h in [(0, 0), (2, 5), (3, 7)]:
+        kr, vr = w.layer_kv_rows(w.switch_layer, b, h)
+        q = qw[b:b + 1, h * G:(h + 1) * G].contiguous()
+        _, sc = oracle.focal(_as_kv(kr), _as_kv(vr), torch.tensor([T], dtype=torch.int32), q, q_pos0=T - w.window,
+                             cand=(0, ncand), want_out=False)
+        pu.assert_scores_close(gpu["scores"][b, h], sc[0, 0], f"scores b{b} h{h}")
+        ref_idx = oracle.topk(sc[0, 0], w.k_select)
+        pu.check_index_sets(gpu["idx"][b, h].view(1, -1), ref_idx.reshape(1, -1), sc[0, 0].reshape(1, -1),
+                            w.k_select)
+        same = np.array_equal(gpu["idx"][b, h].numpy(), ref_idx)
+        for l in sample_layers:
+            krl, vrl = w.layer_kv_rows(l, b, h)
+            ck, cv, cl = oracle.kv_compact(_as_kv(krl), _as_kv(vrl), torch.tensor([T], dtype=torch.int32),
+                                           torch.from_numpy(ref_idx).view(1, 1, -1), ncand, w.compact_cap)
+            assert int(cl[0]) == w.keep
+            if same:
+                gk, gv = gpu["compact"][l]
+                assert torch.equal(gk[b, h, :w.keep].view(torch.int16), ck[0, 0, :w.keep].view(torch.int16))
+                assert torch.equal(gv[b, h, :w.keep].view(torch.int16), cv[0, 0, :w.keep].view(torch.int16))
+            ak, av = appended[l]
+            for t in steps:
+                full_k = torch.cat([ck[0, 0, :w.keep], ak[b, h, :t + 1]])
+                full_v = torch.cat([cv[0, 0, :w.keep], av[b, h, :t + 1]])
+                q = w.decode_query(t, l)[b:b + 1, h * G:(h + 1) * G].contiguous()
+                n = full_k.shape[0]
+                ref = oracle.sparse_decode(_as_kv(full_k), _as_kv(full_v), torch.tensor([n], dtype=torch.int32), q,
+                                           None, 0)
+                if same:
+                    pu.assert_out_close(gpu["decode"][(t, l)][b, h * G:(h + 1) * G], ref[0],
+                                        float(full_v.float().abs().max()), f"decode t{t} l{l} b{b} h{h}")
+
+
+# ----------------------------------------------------------------------------------------------
+def test_long_ctx_full_sampled():
+    from tests.workload_runs import long_ctx_run
+    w = LongCtx()
+    gpu = long_ctx_run(w)
+    G = w.Hq // w.Hkv
+    q0 = w.query(0, "cpu")
+    q1 = w.query(1, "cpu")
+    ln = torch.tensor([w.T], dtype=torch.int32)
+    gapped = 0
+    for b, h in [(0, 0), (31, 5), (63, 7)]:
+        kr, vr = w.layer_kv_rows(0, b, h)
+        vmax = float(vr.float().abs().max())
+        out, sc = oracle.focal(_as_kv(kr), _as_kv(vr), ln, q0[b:b + 1, h * G:(h + 1) * G].contiguous())
+        pu.assert_out_close(gpu["out"][b, h * G:(h + 1) * G], out[0], vmax, f"focal out b{b} h{h}")
+        pu.assert_scores_close(gpu["scores"][b, h].cpu(), sc[0, 0], f"scores b{b} h{h}")
+        ref_idx = oracle.topk(sc[0, 0], w.k)
+        _, gp, _ = pu.check_index_sets(gpu["idx"][b, h].view(1, -1), ref_idx.reshape(1, -1),
+                                       sc[0, 0].reshape(1, -1), w.k)
+        gapped += gp
+        if np.array_equal(gpu["idx"][b, h].numpy(), ref_idx):
+            ref = oracle.sparse_decode(_as_kv(kr), _as_kv(vr), ln, q1[b:b + 1, h * G:(h + 1) * G].contiguous(),
+                                       torch.from_numpy(ref_idx).view(1, 1, -1), w.T)
+            pu.assert_out_close(gpu["sparse"][b, h * G:(h + 1) * G], ref[0], vmax, f"sparse b{b} h{h}")
+    print("long_ctx gapped rows:", gapped, "of 3")
+
+
+# ----------------------------------------------------------------------------------------------
+def test_hpd_branch_full_sampled():
+    from tests.workload_runs import hpd_run
+    w = HpdBranch()
+    gpu = hpd_run(w)
+    d = w.small_inputs(0, device="cpu")
+    off = w.offsets().tolist()
+    G = w.Hq // w.Hkv
+    for b in (0, 100, 511):
+        sk, sv = w.suffix_rows(0, b)
+        vmax = max(float(t.float().abs().max()) for t in (d["pv"], sv, d["dv"]))
+        o1 = torch.tensor([0, off[b + 1] - off[b]], dtype=torch.int32)
+        dk, dv, q = d["dk"][b:b + 1], d["dv"][b:b + 1], d["q"][b:b + 1]
+        ref = oracle.shared_prefix(d["pk"], d["pv"], sk, sv, o1, dk, dv, q)
+        pu.assert_out_close(gpu["dense"][b], ref[0], vmax, f"dense branch {b}")
+        # sparse variant: the oracle's own prefix selection
+        _, psc = oracle.focal(d["pk"].unsqueeze(0), d["pv"].unsqueeze(0), torch.tensor([w.P], dtype=torch.int32), q,
+                              want_out=False)
+        pu.assert_scores_close(gpu["pscores"][b], psc[0], f"prefix scores branch {b}")
+        ref_idx = oracle.topk(psc[0], w.kp)
+        pu.check_index_sets(gpu["pidx"][b], ref_idx, psc[0], w.kp)
+        same = [np.array_equal(gpu["pidx"][b, h].numpy(), ref_idx[h]) for h in range(w.Hkv)]
+        ref_s = oracle.shared_prefix(d["pk"], d["pv"], sk, sv, o1, dk, dv, q,
+                                     torch.from_numpy(ref_idx).view(1, w.Hkv, w.kp))
+        for h in range(w.Hkv):
+            if same[h]:
+                pu.assert_out_close(gpu["sparse"][b, h * G:(h + 1) * G], ref_s[0, h * G:(h + 1) * G], vmax,
+                                    f"sparse branch {b} head {h}")
