@@ -153,6 +153,23 @@ def _cudart():
     return None
 
 
+def profiled_traffic_ratio():
+    """DRAM bytes per algorithmic byte of the dominant kernel from its committed ncu summary, or None
+    when that summary was taken on a different revision of the kernel source."""
+    import hashlib
+    import re
+    try:
+        prof = open(os.path.join(ROOT, "profiles", "sparse_gqa_decode_ocr_decode.md")).read()
+        src = os.path.join(ROOT, "kv_cache_token_fx_gb300", "csrc", "attn_splitkv.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    f = dict(re.findall(r"^\s+(\w+): (\S+)$", prof, flags=re.M))
+    if f.get("kernel_source_sha256") != sha:
+        return None
+    return float(f["profiled_launch_dram_bytes"]) / float(f["profiled_launch_algorithmic_bytes"])
+
+
 def measured_hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -336,8 +353,11 @@ def run_fx(args, rank, local, ws):
     roofline = None
     if n_launch:
         achieved = kern_bytes / (kern_ms / 1e3) / 1e9
+        ratio = profiled_traffic_ratio()
+        traffic = int(ratio * kern_bytes / n_launch) if ratio is not None else None
         roofline = {"kernel": "fx_sparse_gqa_decode", "bound": "hbm", "achieved": round(achieved, 1),
-                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "traffic_note": "ncu dram bytes of a captured last-step launch, scaled by algorithmic bytes",
                     "peak_source": peak_kind, "avg_launch_us": round(kern_ms * 1e3 / n_launch, 3),
                     "avg_bytes_per_launch": int(kern_bytes / n_launch), "launches_timed": n_launch,
                     "timing": "CUDA events around graphs of the 26 sparse launches per step"}
