@@ -47,8 +47,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one_pending() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_none_pending() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+// all of this thread's commit groups but the newest kWarpStages-1 have completed
+__device__ __forceinline__ void cp_async_wait_stages()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kWarpStages - 1) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all_groups() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
 {
@@ -125,7 +129,9 @@ struct KeySource {
     const uint16_t* kb;   // main cache / prefix base for this (b, h)
     const uint16_t* vb;
     int64_t st;
-    int kk;               // gathered positions (sparse idx / prefix idx)
+    const int32_t* irow;  // gathered positions of this (b, h) (sparse idx / prefix idx), or null
+    int kk;               // number of gathered positions
+    int lim_tok;          // exclusive bound of a gathered position (len for sparse, P for prefix)
     int tail_lo;          // sparse: first tail token
     int np, L;            // prefix: prefix rows, suffix rows
     const uint16_t* suf_k;
@@ -134,33 +140,24 @@ struct KeySource {
     const uint16_t* dr_k;
     const uint16_t* dr_v;
     int64_t dr_si;
-    bool gathered;        // prefix positions come from the index table
-    int s0;
+    unsigned* err;
 
-    __device__ __forceinline__ bool row(int pos, const int* s_tok, const uint16_t*& kp, const uint16_t*& vp) const
+    // Token row of sequence position pos; false when it must not be read (a rejected index, which
+    // is also reported in the device error word).
+    __device__ __forceinline__ bool row(int pos, const uint16_t*& kp, const uint16_t*& vp) const
     {
         if (MODE == kModeFocal) {
             kp = kb + (int64_t)pos * st;
             vp = vb + (int64_t)pos * st;
             return true;
         }
-        if (MODE == kModeSparse) {
-            int t;
-            if (pos < kk) {
-                t = s_tok[pos - s0];
-                if (t < 0) return false;
-            } else {
-                t = tail_lo + (pos - kk);
-            }
-            kp = kb + (int64_t)t * st;
-            vp = vb + (int64_t)t * st;
-            return true;
-        }
-        if (pos < np) {
+        if (MODE == kModeSparse || pos < np) {
             int t = pos;
-            if (gathered) {
-                t = s_tok[pos - s0];
-                if (t < 0) return false;
+            if (MODE == kModeSparse) t = pos < kk ? __ldg(irow + pos) : tail_lo + (pos - kk);
+            else if (irow != nullptr) t = __ldg(irow + pos);
+            if ((MODE == kModeSparse ? pos < kk : irow != nullptr) && (t < 0 || t >= lim_tok)) {
+                atomicOr(err, FX_DEVERR_INDEX);
+                return false;
             }
             kp = kb + (int64_t)t * st;
             vp = vb + (int64_t)t * st;
@@ -182,10 +179,9 @@ template <int MODE, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    const int nst = p.stages;
-    unsigned char* sQ = smem + 128;                                          // [16][kPitch] bf16
-    unsigned char* sKV = sQ + kQTileBytes;                                   // [nst][K tile, V tile]
-    int* s_tok = reinterpret_cast<int*>(sKV + (size_t)nst * kKVStageBytes);  // [split_len]
+    unsigned char* sQ = smem + 128;                                      // [16][kPitch] bf16
+    unsigned char* sKV = sQ + kQTileBytes;                               // [kWarps][kWarpStages][K, V]
+    __shared__ uint32_t s_vmask[kWarps][kWarpStages];   // valid-row bits of each staged sub-tile
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -213,10 +209,11 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     src.st = p.st;
     src.kk = p.kk;
     src.tail_lo = p.tail_lo;
-    src.gathered = p.idx != nullptr;
+    src.irow = p.idx != nullptr ? p.idx + (int64_t)bh * p.kk : nullptr;
+    src.err = p.err;
     src.np = 0;
     src.L = 0;
-    int lim_tok = p.P;    // exclusive bound of a gathered index
+    src.lim_tok = p.P;
     if (MODE == kModeFocal || MODE == kModeSparse) {
         int l = p.len[b];
         if (l < 0 || l > p.Tcap) {
@@ -224,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             l = l < 0 ? 0 : p.Tcap;
         }
         n_keys = (MODE == kModeFocal) ? l : p.kk + max(0, l - p.tail_lo);
-        lim_tok = l;
+        src.lim_tok = l;
     } else {
         src.np = p.idx ? p.kk : p.P;
         const int o0 = p.suf_off[b];
@@ -250,51 +247,53 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
     const int s0 = split * p.split_len;
     const int s1 = min(n_keys, s0 + p.split_len);
-    src.s0 = s0;
-    const int ntiles = s1 > s0 ? (s1 - s0 + kTile - 1) / kTile : 0;
+    // this warp's contiguous share of the split, in sub-tiles of kSub keys
+    const int wl = ((max(s1 - s0, 0) + kWarps * kSub - 1) / (kWarps * kSub)) * kSub;
+    const int ws = min(s1, s0 + warp * wl);
+    const int we = min(s1, ws + wl);
+    const int nsub = (we - ws + kSub - 1) / kSub;
 
-    // gathered token positions of this split, checked once
-    if (MODE != kModeFocal && p.idx != nullptr) {
-        const int32_t* irow = p.idx + (int64_t)bh * p.kk;
-        const int hi = min(s1, p.kk);
-        for (int pos = s0 + tid; pos < hi; pos += kThreads) {
-            int t = __ldg(irow + pos);
-            if (t < 0 || t >= lim_tok) {
-                flag(p.err, FX_DEVERR_INDEX);
-                t = -1;
-            }
-            s_tok[pos - s0] = t;
-        }
-    }
-    __syncthreads();
-
-    // a tile is copied with 16-byte cp.async operations, one commit group per tile; each warp
-    // instruction moves two whole rows (lanes 0-15 one row, lanes 16-31 the next), so the copies are
-    // fully coalesced.  Rows that must not be read are zero-filled instead.
-    auto issue = [&](int tile, int stage) {
-        const int c16 = lane & 15;
+    // Each warp stages its own sub-tiles (16 K rows + 16 V rows) with 16-byte cp.async operations --
+    // every warp instruction moves two whole rows -- into its private ring of kWarpStages buffers.  One
+    // commit group per sub-tile (empty past the end), so "all but kWarpStages-1 groups done" always
+    // means "the oldest sub-tile has landed".  No CTA-wide barrier is needed inside the loop.
+    unsigned char* wbuf = sKV + (size_t)warp * kWarpBytes;
+    auto issue = [&](int j) {
+        if (j < nsub) {
+            const int c16 = lane & 15;
+            unsigned char* stage = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
+            // lane l resolves the token row of key (l & 15) of the sub-tile (one index load per lane);
+            // the copies then take each row's address from the lane that resolved it
+            const int mypos = ws + j * kSub + (lane & 15);
+            const uint16_t* mk = src.kb;
+            const uint16_t* mv = src.vb;
+            const bool mok = mypos < we && src.row(mypos, mk, mv);
+            const uint32_t vmask = __ballot_sync(kFull, mok) & 0xffffu;
+            const int64_t mko = mk - src.kb;
+            const int64_t mvo = mv - src.vb;
 #pragma unroll
-        for (int u = 0; u < kTile / (2 * kWarps); ++u) {
-            const int r = 2 * (warp + kWarps * u) + (lane >> 4);
-            const int pos = s0 + tile * kTile + r;
-            const uint16_t* kp = src.kb;
-            const uint16_t* vp = src.vb;
-            const bool ok = pos < s1 && src.row(pos, s_tok, kp, vp);
-            unsigned char* dk = sKV + (size_t)stage * kKVStageBytes + (size_t)r * kPitch + 16 * c16;
-            unsigned char* dv = dk + kTile * kPitch;
-            if (ok) {
-                cp_async16(smem_addr(dk), kp + 8 * c16);
-                cp_async16(smem_addr(dv), vp + 8 * c16);
-            } else {
-                *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < kSub / 2; ++u) {
+                const int r = 2 * u + (lane >> 4);
+                const uint16_t* kp = src.kb + __shfl_sync(kFull, mko, r);
+                const uint16_t* vp = src.vb + (MODE == kModePrefix ? __shfl_sync(kFull, mvo, r)
+                                                                   : __shfl_sync(kFull, mko, r));
+                unsigned char* dk = stage + (size_t)r * kPitch + 16 * c16;
+                unsigned char* dv = dk + kSub * kPitch;
+                if ((vmask >> r) & 1u) {
+                    cp_async16(smem_addr(dk), kp + 8 * c16);
+                    cp_async16(smem_addr(dv), vp + 8 * c16);
+                } else {
+                    *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
+            if (lane == 0) s_vmask[warp][j % kWarpStages] = vmask;
         }
         cp_async_commit();
     };
 
-    if (ntiles > 0) issue(0, 0);
-    if (ntiles > 1 && nst > 1) issue(1, 1);
+#pragma unroll
+    for (int j = 0; j < kWarpStages; ++j) issue(j);
 
     // ---- stage B: after the preceding kernel -- the query rows, then everything that writes ------
     if (early) griddep_wait();
@@ -348,47 +347,42 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int stage = nst > 1 ? (tile & 1) : 0;
-        const int base = s0 + tile * kTile + warp * kKeysPerWarp;   // first key of this warp
-        if (nst > 1 && tile + 1 < ntiles)
-            cp_async_wait_one_pending();
-        else
-            cp_async_wait_none_pending();
-        __syncthreads();
-        const unsigned char* sk = sKV + (size_t)stage * kKVStageBytes + (size_t)(warp * kKeysPerWarp) * kPitch;
-        const unsigned char* sv = sk + kTile * kPitch;
+    for (int j = 0; j < nsub; ++j) {
+        const int base = ws + j * kSub;   // first key of this sub-tile
+        cp_async_wait_stages();
+        __syncwarp();
+        const unsigned char* sk = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
+        const unsigned char* sv = sk + kSub * kPitch;
+        const uint32_t vmask = s_vmask[warp][j % kWarpStages];
 
         // S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys)
         float s[2][4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) s[j][e] = 0.f;
-            const int krow = 8 * j + (lane & 7);
+            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+            const int krow = 8 * nt + (lane & 7);
             const int kcol = 8 * (lane >> 3);   // matrices: dims +0, +8, +16, +24 of a 32-dim slice
 #pragma unroll
             for (int kp = 0; kp < 4; ++kp) {     // pairs of k-steps
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4(smem_addr(sk + krow * kPitch + (32 * kp + kcol) * 2), b0, b1, b2, b3);
-                mma_bf16(s[j], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
-                mma_bf16(s[j], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+                mma_bf16(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
+                mma_bf16(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
             }
         }
 
         // scale to base 2, mask, store logits (focal), online softmax
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hr = e >> 1;
-                const int pos = base + 8 * j + 2 * t4 + (e & 1);
-                bool ok = pos < s1 && pos <= lim[hr];
-                if (MODE == kModeSparse && ok && pos < p.kk) ok = s_tok[pos - s0] >= 0;
-                if (MODE == kModePrefix && ok && src.gathered && pos < src.np) ok = s_tok[pos - s0] >= 0;
-                const float x = ok ? s[j][e] * p.qscale : -INFINITY;
-                s[j][e] = x;
+                const int pos = base + 8 * nt + 2 * t4 + (e & 1);
+                const bool ok = ((vmask >> (pos - base)) & 1u) && pos <= lim[hr];
+                const float x = ok ? s[nt][e] * p.qscale : -INFINITY;
+                s[nt][e] = x;
                 mx[hr] = fmaxf(mx[hr], x);
             }
         }
@@ -399,10 +393,10 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 if (row < p.R) {
                     float* lrow = p.logits + (int64_t)(bh * p.R + row) * p.Tcap;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int pos = base + 8 * j + 2 * t4;
-                        if (pos < s1) lrow[pos] = s[j][2 * hr];
-                        if (pos + 1 < s1) lrow[pos + 1] = s[j][2 * hr + 1];
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int pos = base + 8 * nt + 2 * t4;
+                        if (pos < we) lrow[pos] = s[nt][2 * hr];
+                        if (pos + 1 < we) lrow[pos + 1] = s[nt][2 * hr + 1];
                     }
                 }
             }
@@ -426,11 +420,11 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             o[n][3] *= alpha[1];
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float pe = fast_exp2(s[j][e] - ms[e >> 1]);
-                s[j][e] = pe;
+                const float pe = fast_exp2(s[nt][e] - ms[e >> 1]);
+                s[nt][e] = pe;
                 l_run[e >> 1] += pe;
             }
         }
@@ -455,9 +449,11 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             }
         }
 
-        __syncthreads();   // every warp is done with this stage
-        if (tile + nst < ntiles) issue(tile + nst, stage);
+        __syncwarp();      // every lane is done with this buffer before it is refilled
+        issue(j + kWarpStages);
     }
+    cp_async_wait_all_groups();
+    __syncthreads();       // all warps are done with their buffers (reused below)
 
     // row sums over the quad
 #pragma unroll
@@ -518,22 +514,30 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         for (int e = (int)me * kThreads + tid; e < nr * kHeadDim; e += (int)cs * kThreads) {
             const int r = e >> 7;
             const int c = e & (kHeadDim - 1);
-            float mq[kMaxClusterSplits];
-            float M = -INFINITY;
+            // one batch of independent remote loads, then the arithmetic
+            float mq[kMaxClusterSplits], lq[kMaxClusterSplits], oq[kMaxClusterSplits];
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplits; ++q) {
-                mq[q] = (unsigned)q < cs ? ld_cluster(cluster_map(&c_m[r], q)) : -INFINITY;
-                M = fmaxf(M, mq[q]);
+                if ((unsigned)q < cs) {
+                    mq[q] = ld_cluster(cluster_map(&c_m[r], q));
+                    lq[q] = ld_cluster(cluster_map(&c_l[r], q));
+                    oq[q] = ld_cluster(cluster_map(&c_o[r * kHeadDim + c], q));
+                } else {
+                    mq[q] = -INFINITY;
+                    lq[q] = 0.f;
+                    oq[q] = 0.f;
+                }
             }
+            float M = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < kMaxClusterSplits; ++q) M = fmaxf(M, mq[q]);
             const float Ms = (M == -INFINITY) ? 0.f : M;
             float Ls = 0.f, O = 0.f;
 #pragma unroll
             for (int q = 0; q < kMaxClusterSplits; ++q) {
-                if ((unsigned)q < cs) {
-                    const float w = fast_exp2(mq[q] - Ms);
-                    Ls = fmaf(ld_cluster(cluster_map(&c_l[r], q)), w, Ls);
-                    O = fmaf(ld_cluster(cluster_map(&c_o[r * kHeadDim + c], q)), w, O);
-                }
+                const float w = fast_exp2(mq[q] - Ms);
+                Ls = fmaf(lq[q], w, Ls);
+                O = fmaf(oq[q], w, O);
             }
             const int row = r0 + r;
             const int gi = row / p.Mq;
@@ -653,7 +657,7 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
     auto kern = attn_tile_kernel<MODE, CLUSTER>;
     if (configured != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_smem_bytes(2, kMaxSplitTokens));
+                                             (int)attn_smem_bytes());
         if (e != cudaSuccess) return e;
         if (CLUSTER) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -661,7 +665,7 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
         }
         configured = dev;
     }
-    const size_t smem = attn_smem_bytes(p.stages, (MODE != kModeFocal && p.idx != nullptr) ? p.split_len : 0);
+    const size_t smem = attn_smem_bytes();
     dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
     // with CLUSTER, every split of one (b, h, row group) is one CTA of a (1, nsplit, 1) cluster
     return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, CLUSTER ? (unsigned)p.nsplit : 0u, p);

@@ -15,30 +15,27 @@ constexpr int kMaxRows = 64;   // G * Mq limit per KV head
 constexpr int kWarps = 4;                               // warps per attention CTA
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row (256 bytes)
-constexpr int kTile = 64;                               // keys per staged tile
-constexpr int kKeysPerWarp = kTile / kWarps;            // 16: two n-tiles of the S = Q K^T MMA
+constexpr int kSub = 16;                                // keys per warp sub-tile (two n-tiles of S = Q K^T)
+constexpr int kWarpStages = 3;                          // sub-tiles in flight per warp
 constexpr int kRowsPerCta = 16;                         // query rows per CTA: one m16 MMA tile
 constexpr int kPitch = kRowBytes + 16;                  // staged row pitch: the 16-byte pad puts the 8
                                                         // rows of an ldmatrix on 8 distinct bank groups
 constexpr int kQTileBytes = kRowsPerCta * kPitch;       // bf16 query tile
-constexpr int kKVStageBytes = 2 * kTile * kPitch;       // K and V rows of one tile (34 KB)
+constexpr int kSubBytes = 2 * kSub * kPitch;            // K and V rows of one sub-tile (8.5 KB)
+constexpr int kWarpBytes = kWarpStages * kSubBytes;     // one warp's ring of sub-tile buffers
+constexpr int kTile = kWarps * kSub;                    // keys one CTA has in flight per pipeline step
 constexpr int kMaxSplitTokens = 4096;                   // longest gathered split (bounds the index table)
 constexpr unsigned kSpinLimit = 1u << 22;               // bounded mbarrier waits
 constexpr int kMaxClusterSplits = 16;                   // splits merged inside one thread-block cluster
-constexpr int kResidentPerSm = 3;                       // attention CTAs that fit one SM (shared memory)
+constexpr int kResidentPerSm = 2;                       // attention CTAs that fit one SM (shared memory)
 // Arrival counters of the last-CTA merge live in a fixed region at the start of every workspace
 // (one slot per (b, h, row group); grid.z <= 65535 and at most 4 row groups), so no other data of
 // any call ever overlaps them and they stay zero between calls.
 constexpr size_t kCounterSlots = 65536u * 4u;
 constexpr size_t kCounterBytes = kCounterSlots * sizeof(unsigned);
 
-// Dynamic shared memory of one attention CTA: mbarriers, the query tile, `stages` K+V tiles and the
-// gathered-index table of its split.
-inline size_t attn_smem_bytes(int stages, int gathered_split_len)
-{
-    return 128 + (size_t)kQTileBytes + (size_t)stages * kKVStageBytes +
-           (size_t)(gathered_split_len > 0 ? gathered_split_len : 0) * sizeof(int);
-}
+// Dynamic shared memory of one attention CTA: the query tile and each warp's ring of sub-tile buffers.
+inline size_t attn_smem_bytes() { return 128 + (size_t)kQTileBytes + (size_t)kWarps * kWarpBytes; }
 
 // Which key sequence an attention CTA walks.
 enum AttnMode : int {
