@@ -142,20 +142,27 @@ struct KeySource {
     int64_t dr_si;
     unsigned* err;
 
-    // Token row of sequence position pos; false when it must not be read (a rejected index, which
-    // is also reported in the device error word).
-    __device__ __forceinline__ bool row(int pos, const uint16_t*& kp, const uint16_t*& vp) const
+    // Token of sequence position pos: an index-row load for the gathered part (only for pos < kk, so
+    // always inside the row), the position itself otherwise.  Nothing is checked here.
+    __device__ __forceinline__ int token(int pos) const
+    {
+        if (MODE == kModeSparse) return pos < kk ? __ldg(irow + pos) : tail_lo + (pos - kk);
+        if (MODE == kModePrefix) return (irow != nullptr && pos < kk) ? __ldg(irow + pos) : pos;
+        return pos;
+    }
+
+    // K and V rows of position pos whose token is t; false when they must not be read (a rejected
+    // index, which is also reported in the device error word).
+    __device__ __forceinline__ bool row(int pos, int t, const uint16_t*& kp, const uint16_t*& vp) const
     {
         if (MODE == kModeFocal) {
-            kp = kb + (int64_t)pos * st;
-            vp = vb + (int64_t)pos * st;
+            kp = kb + (int64_t)t * st;
+            vp = vb + (int64_t)t * st;
             return true;
         }
         if (MODE == kModeSparse || pos < np) {
-            int t = pos;
-            if (MODE == kModeSparse) t = pos < kk ? __ldg(irow + pos) : tail_lo + (pos - kk);
-            else if (irow != nullptr) t = __ldg(irow + pos);
-            if ((MODE == kModeSparse ? pos < kk : irow != nullptr) && (t < 0 || t >= lim_tok)) {
+            const bool gathered = MODE == kModeSparse ? pos < kk : irow != nullptr;
+            if (gathered && (t < 0 || t >= lim_tok)) {
                 atomicOr(err, FX_DEVERR_INDEX);
                 return false;
             }
@@ -214,6 +221,15 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     src.np = 0;
     src.L = 0;
     src.lim_tok = p.P;
+    // this warp's contiguous share of the split (the host makes split_len a multiple of kWarps * kSub),
+    // and the index loads of its first sub-tiles, issued before the length is known
+    const int s0 = split * p.split_len;
+    const int wl = p.split_len / kWarps;
+    const int ws = s0 + warp * wl;
+    int tpre[kWarpStages];
+#pragma unroll
+    for (int j = 0; j < kWarpStages; ++j) tpre[j] = src.token(ws + j * kSub + (lane & 15));
+
     if (MODE == kModeFocal || MODE == kModeSparse) {
         int l = p.len[b];
         if (l < 0 || l > p.Tcap) {
@@ -245,20 +261,16 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         src.dr_si = p.dr_si;
         n_keys = src.np + L + p.Mq;
     }
-    const int s0 = split * p.split_len;
     const int s1 = min(n_keys, s0 + p.split_len);
-    // this warp's contiguous share of the split, in sub-tiles of kSub keys
-    const int wl = ((max(s1 - s0, 0) + kWarps * kSub - 1) / (kWarps * kSub)) * kSub;
-    const int ws = min(s1, s0 + warp * wl);
     const int we = min(s1, ws + wl);
-    const int nsub = (we - ws + kSub - 1) / kSub;
+    const int nsub = we > ws ? (we - ws + kSub - 1) / kSub : 0;
 
     // Each warp stages its own sub-tiles (16 K rows + 16 V rows) with 16-byte cp.async operations --
     // every warp instruction moves two whole rows -- into its private ring of kWarpStages buffers.  One
     // commit group per sub-tile (empty past the end), so "all but kWarpStages-1 groups done" always
     // means "the oldest sub-tile has landed".  No CTA-wide barrier is needed inside the loop.
     unsigned char* wbuf = sKV + (size_t)warp * kWarpBytes;
-    auto issue = [&](int j) {
+    auto issue = [&](int j, int mytok) {
         if (j < nsub) {
             const int c16 = lane & 15;
             unsigned char* stage = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             const int mypos = ws + j * kSub + (lane & 15);
             const uint16_t* mk = src.kb;
             const uint16_t* mv = src.vb;
-            const bool mok = mypos < we && src.row(mypos, mk, mv);
+            const bool mok = mypos < we && src.row(mypos, mytok, mk, mv);
             const uint32_t vmask = __ballot_sync(kFull, mok) & 0xffffu;
             const int64_t mko = mk - src.kb;
             const int64_t mvo = mv - src.vb;
@@ -293,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     };
 
 #pragma unroll
-    for (int j = 0; j < kWarpStages; ++j) issue(j);
+    for (int j = 0; j < kWarpStages; ++j) issue(j, tpre[j]);
 
     // ---- stage B: after the preceding kernel -- the query rows, then everything that writes ------
     if (early) griddep_wait();
@@ -349,6 +361,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     float l_run[2] = {0.f, 0.f};
     for (int j = 0; j < nsub; ++j) {
         const int base = ws + j * kSub;   // first key of this sub-tile
+        const int tnext = src.token(base + kWarpStages * kSub + (lane & 15));   // for the refill below
         cp_async_wait_stages();
         __syncwarp();
         const unsigned char* sk = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
@@ -450,7 +463,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         }
 
         __syncwarp();      // every lane is done with this buffer before it is refilled
-        issue(j + kWarpStages);
+        issue(j + kWarpStages, tnext);
     }
     cp_async_wait_all_groups();
     __syncthreads();       // all warps are done with their buffers (reused below)
@@ -463,14 +476,16 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
 
     // ---- combine the warps into this CTA's partial (the stage buffers are free now) -------------
+    const int nr = min(kRowsPerCta, p.R - r0);   // rows of this group that exist
     __shared__ float sm_m[kWarps][kRowsPerCta];
     __shared__ float sm_l[kWarps][kRowsPerCta];
     float* sm_o = reinterpret_cast<float*>(sKV);   // [kWarps][16][128]
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
+    for (int n = 0; n < 16; ++n) {   // only the rows that exist
         const int c = 8 * n + 2 * t4;
-        *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kHeadDim + c) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kHeadDim + c) = make_float2(o[n][2], o[n][3]);
+        if (g < nr) *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kHeadDim + c) = make_float2(o[n][0], o[n][1]);
+        if (g + 8 < nr)
+            *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kHeadDim + c) = make_float2(o[n][2], o[n][3]);
     }
     if (t4 == 0) {
         sm_m[warp][g] = m_run[0];
@@ -483,7 +498,6 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     __shared__ float c_m[kRowsPerCta];
     __shared__ float c_l[kRowsPerCta];
     float* c_o = sm_o;   // [16][128]: combined in place over warp 0's slice (each element by its own thread)
-    const int nr = min(kRowsPerCta, p.R - r0);   // rows of this group that exist
     for (int e = tid; e < nr * kHeadDim; e += kThreads) {
         const int r = e >> 7;
         const int c = e & (kHeadDim - 1);

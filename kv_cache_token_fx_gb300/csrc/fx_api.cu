@@ -111,7 +111,7 @@ Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_clust
     if (ns > cdiv(keys, 16)) ns = cdiv(keys, 16);
     if (merge_in_cluster && ns > kMaxClusterSplits && min_ns <= kMaxClusterSplits) ns = kMaxClusterSplits;
     if (ns < 1) ns = 1;
-    pl.split_len = cdiv(cdiv(keys, ns), 16) * 16;   // the last tile of a split may be partial
+    pl.split_len = cdiv(cdiv(keys, ns), kTile) * kTile;   // equal whole sub-tiles per warp; the last split may be short
     pl.nsplit = cdiv(keys, pl.split_len);
     pl.stages = pl.split_len > kTile ? 2 : 1;
     return pl;

@@ -23,8 +23,8 @@ constexpr int kPitch = kRowBytes + 16;                  // staged row pitch: the
 constexpr int kQTileBytes = kRowsPerCta * kPitch;       // bf16 query tile
 constexpr int kSubBytes = 2 * kSub * kPitch;            // K and V rows of one sub-tile (8.5 KB)
 constexpr int kWarpBytes = kWarpStages * kSubBytes;     // one warp's ring of sub-tile buffers
-constexpr int kTile = kWarps * kSub;                    // keys one CTA has in flight per pipeline step
-constexpr int kMaxSplitTokens = 4096;                   // longest gathered split (bounds the index table)
+constexpr int kTile = kWarps * kSub;                    // split lengths are multiples of this (whole sub-tiles per warp)
+constexpr int kMaxSplitTokens = 4096;                   // gathered rows longer than 16 such splits merge in the workspace
 constexpr unsigned kSpinLimit = 1u << 22;               // bounded mbarrier waits
 constexpr int kMaxClusterSplits = 16;                   // splits merged inside one thread-block cluster
 constexpr int kResidentPerSm = 2;                       // attention CTAs that fit one SM (shared memory)
