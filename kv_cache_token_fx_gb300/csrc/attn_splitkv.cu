@@ -122,6 +122,25 @@ __device__ __forceinline__ float ld_cluster(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // ---- key sequences --------------------------------------------------------------------------------
 // Where the rows of one (b, h) key sequence live: sequence position -> K row and V row.
 template <int MODE>
@@ -182,7 +201,14 @@ struct KeySource {
 };
 
 // ---- the kernel -----------------------------------------------------------------------------------
-template <int MODE, bool CLUSTER>
+// How the splits of one (b, h, row group) are merged.
+enum Merge {
+    kMergeWorkspace = 0,   // partials through the workspace; the last-arriving CTA merges
+    kMergePull = 1,        // one cluster; every CTA reads all partials from distributed shared memory
+    kMergePush = 2,        // one cluster; the others push their partials into CTA 0, which merges alone
+};
+
+template <int MODE, int MERGE>
 __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -519,7 +545,53 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         }
     }
 
-    if (CLUSTER) {
+    if constexpr (MERGE == kMergePush) {
+        // CTAs 1 .. cs-1 store their partial into CTA 0's receive area and arrive on the cluster barrier,
+        // then exit (the barrier's wait only counts threads that have not exited); CTA 0 arrives, waits
+        // -- after which every partial is visible -- and merges alone.  One barrier phase in all.
+        __shared__ __align__(16) float s_recv[kRecvFloats];   // [cs-1][nr][128] O, [cs-1][nr] m, [cs-1][nr] l
+        const unsigned cs = cluster_size();
+        const unsigned me = cluster_rank();
+        const int npeer = (int)cs - 1;
+        float* recv_m = s_recv + npeer * nr * kHeadDim;
+        float* recv_l = recv_m + npeer * nr;
+        if (me != 0) {
+            __syncthreads();   // the combined partial (written by all threads) is complete
+            const uint32_t dst = cluster_map(s_recv + (me - 1) * nr * kHeadDim, 0);
+            for (int e = tid; e < nr * (kHeadDim / 4); e += kThreads)
+                st_cluster_v4(dst + 16 * e, *reinterpret_cast<const float4*>(c_o + 4 * e));
+            if (tid < nr) {
+                st_cluster_f32(cluster_map(recv_m + (me - 1) * nr + tid, 0), c_m[tid]);
+                st_cluster_f32(cluster_map(recv_l + (me - 1) * nr + tid, 0), c_l[tid]);
+            }
+            cluster_arrive_release();
+            return;
+        }
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        for (int e = tid; e < nr * kHeadDim; e += kThreads) {
+            const int r = e >> 7;
+            const int c = e & (kHeadDim - 1);
+            float M = c_m[r];
+            for (int q = 0; q < npeer; ++q) M = fmaxf(M, recv_m[q * nr + r]);
+            const float Ms = (M == -INFINITY) ? 0.f : M;
+            float w = fast_exp2(c_m[r] - Ms);
+            float Ls = c_l[r] * w;
+            float O = c_o[r * kHeadDim + c] * w;
+            for (int q = 0; q < npeer; ++q) {
+                w = fast_exp2(recv_m[q * nr + r] - Ms);
+                Ls = fmaf(recv_l[q * nr + r], w, Ls);
+                O = fmaf(s_recv[(q * nr + r) * kHeadDim + c], w, O);
+            }
+            const int row = r0 + r;
+            const int gi = row / p.Mq;
+            const int i = row - gi * p.Mq;
+            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = Ls > 0.f ? O / Ls : 0.f;
+        }
+        return;
+    }
+
+    if constexpr (MERGE == kMergePull) {
         // every split of this (b, h, row group) is one CTA of the cluster: merge through distributed
         // shared memory, each CTA producing a slice of the output rows
         cluster_sync();
@@ -662,18 +734,19 @@ __global__ void __launch_bounds__(256) focal_combine_kernel(const FocalCombinePa
     }
 }
 
-template <int MODE, bool CLUSTER>
+template <int MODE, int MERGE>
 cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
 {
     static int configured = -1;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = attn_tile_kernel<MODE, CLUSTER>;
+    auto kern = attn_tile_kernel<MODE, MERGE>;
+    const bool cluster = MERGE != kMergeWorkspace;
     if (configured != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)attn_smem_bytes());
         if (e != cudaSuccess) return e;
-        if (CLUSTER) {
+        if (cluster) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
         }
@@ -681,19 +754,25 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
     }
     const size_t smem = attn_smem_bytes();
     dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
-    // with CLUSTER, every split of one (b, h, row group) is one CTA of a (1, nsplit, 1) cluster
-    return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, CLUSTER ? (unsigned)p.nsplit : 0u, p);
+    // merged in a cluster: every split of one (b, h, row group) is one CTA of a (1, nsplit, 1) cluster
+    return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, cluster ? (unsigned)p.nsplit : 0u, p);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s)
 {
-    if (mode == kModeFocal) return launch_one<kModeFocal, false>(p, pdl, s);
+    if (mode == kModeFocal) return launch_one<kModeFocal, kMergeWorkspace>(p, pdl, s);
     const bool cl = p.nsplit <= kMaxClusterSplits;
-    if (mode == kModeSparse)
-        return cl ? launch_one<kModeSparse, true>(p, pdl, s) : launch_one<kModeSparse, false>(p, pdl, s);
-    return cl ? launch_one<kModePrefix, true>(p, pdl, s) : launch_one<kModePrefix, false>(p, pdl, s);
+    // pushed partials of the other CTAs must fit CTA 0's receive area
+    const int rows = p.R < kRowsPerCta ? p.R : kRowsPerCta;
+    const bool push = cl && (p.nsplit - 1) * rows * (kHeadDim + 2) <= kRecvFloats;
+    if (mode == kModeSparse) {
+        if (push) return launch_one<kModeSparse, kMergePush>(p, pdl, s);
+        return cl ? launch_one<kModeSparse, kMergePull>(p, pdl, s) : launch_one<kModeSparse, kMergeWorkspace>(p, pdl, s);
+    }
+    if (push) return launch_one<kModePrefix, kMergePush>(p, pdl, s);
+    return cl ? launch_one<kModePrefix, kMergePull>(p, pdl, s) : launch_one<kModePrefix, kMergeWorkspace>(p, pdl, s);
 }
 
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s)

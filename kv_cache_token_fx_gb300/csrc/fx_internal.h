@@ -27,6 +27,7 @@ constexpr int kTile = kWarps * kSub;                    // split lengths are mul
 constexpr int kMaxSplitTokens = 4096;                   // gathered rows longer than 16 such splits merge in the workspace
 constexpr unsigned kSpinLimit = 1u << 22;               // bounded mbarrier waits
 constexpr int kMaxClusterSplits = 16;                   // splits merged inside one thread-block cluster
+constexpr int kRecvFloats = 1024;                       // CTA 0's receive area for pushed partials (4 KB)
 constexpr int kResidentPerSm = 2;                       // attention CTAs that fit one SM (shared memory)
 // Arrival counters of the last-CTA merge live in a fixed region at the start of every workspace
 // (one slot per (b, h, row group); grid.z <= 65535 and at most 4 row groups), so no other data of
