@@ -77,6 +77,14 @@ __device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// transpose of an 8x8 b16 matrix held one 32-bit pair per lane (row lane/4, columns 2*(lane%4) + 0, 1)
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -208,7 +216,7 @@ enum Merge {
     kMergePush = 2,        // one cluster; the others push their partials into CTA 0, which merges alone
 };
 
-template <int MODE, int MERGE>
+template <int MODE, int MERGE, int NR>
 __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     const int bh = blockIdx.z;
     const int b = bh / p.Hkv;
     const int h = bh - b * p.Hkv;
-    const int r0 = rg * kRowsPerCta;
+    const int r0 = rg * NR;
 
     // ---- stage A: what depends only on the caller's lengths, indices and K/V rows.  With
     // FX_LAUNCH_INPUTS_READY it runs before the preceding kernel on the stream has finished, so the
@@ -337,8 +345,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     if (early) griddep_wait();
     griddep_launch();
 
-    // the query rows of this group as one bf16 16-row tile (rows past R are zero)
-    for (int e = tid; e < kRowsPerCta * (kHeadDim / 8); e += kThreads) {
+    // the query rows of this group as one bf16 NR-row tile (rows past R are zero)
+    for (int e = tid; e < NR * (kHeadDim / 8); e += kThreads) {
         const int rr = e >> 4;
         const int c8 = e & 15;
         const int row = r0 + rr;
@@ -352,38 +360,54 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
     __syncthreads();
 
-    // causal / draft limits of the two accumulator rows this thread holds (g and g + 8)
-    int lim[2];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int row = r0 + g + 8 * hr;
+    // Visibility limit of one query row: the last key position it may see.
+    auto row_limit = [&](int row) {
         const int i = row - (row / p.Mq) * p.Mq;
-        if (row >= p.R)
-            lim[hr] = -1;   // padding row: sees nothing
-        else if (MODE == kModeFocal)
-            lim[hr] = p.q_pos0 >= 0 ? p.q_pos0 + i : 0x7fffffff;
-        else if (MODE == kModePrefix)
-            lim[hr] = src.np + src.L + i;   // draft row j is visible iff j <= i
-        else
-            lim[hr] = 0x7fffffff;
-    }
+        if (row >= p.R) return -1;   // padding row: sees nothing
+        if (MODE == kModeFocal) return p.q_pos0 >= 0 ? p.q_pos0 + i : 0x7fffffff;
+        if (MODE == kModePrefix) return src.np + src.L + i;   // draft row j is visible iff j <= i
+        return 0x7fffffff;
+    };
 
-    // Q fragments for the 8 k-steps of the 128-wide head
-    uint32_t qa[8][4];
-    {
+    // Two layouts of the per-warp math (both mma.sync m16n8k16, bf16 in, fp32 accumulate):
+    //   NR == 16 (wide): the query rows are the M side.  S = Q K^T is a 16-row x 16-key tile (2 n-tiles),
+    //     O = P V accumulates 16 rows x 128 dims.  48 MMAs per 16 keys.
+    //   NR == 8 (narrow, at most 8 query rows): the keys are the M side.  S^T = K Q^T is 16 keys x 8 rows
+    //     (one tile per k-step), O^T = V^T P^T accumulates 128 dims x 8 rows; P^T reaches the B operand
+    //     through movmatrix.trans.  24 MMAs per 16 keys -- half the tensor work when few rows exist.
+    constexpr int kOT = NR == 8 ? 8 : 16;   // accumulator tiles of O (wide) / O^T (narrow)
+    constexpr int kQF = NR == 8 ? 2 : 4;    // registers of one k-step's Q fragment
+    int lim[2];
+    uint32_t qf[8][kQF];
+    if constexpr (NR == 8) {
+        // this thread's accumulator columns are query rows 2*t4 and 2*t4 + 1
+        lim[0] = row_limit(r0 + 2 * t4);
+        lim[1] = row_limit(r0 + 2 * t4 + 1);
+        // B fragments of Q^T: matrices (rows 0-7, dims 32kp + 0/8/16/24 .. +7)
+        const int qrow = lane & 7;
+        const int qcol = 8 * (lane >> 3);
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp)
+            ldsm_x4(smem_addr(sQ + qrow * kPitch + (32 * kp + qcol) * 2), qf[2 * kp][0], qf[2 * kp][1],
+                    qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+    } else {
+        // this thread's accumulator rows are g and g + 8
+        lim[0] = row_limit(r0 + g);
+        lim[1] = row_limit(r0 + g + 8);
+        // A fragments of Q for the 8 k-steps of the 128-wide head
         const int qrow = (lane & 7) + 8 * ((lane >> 3) & 1);
         const int qcol = 8 * (lane >> 4);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            ldsm_x4(smem_addr(sQ + qrow * kPitch + (16 * ks + qcol) * 2), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+            ldsm_x4(smem_addr(sQ + qrow * kPitch + (16 * ks + qcol) * 2), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
     }
 
-    float o[16][4];
+    float o[kOT][4];
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
+    for (int n = 0; n < kOT; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};
+    float m_run[2] = {-INFINITY, -INFINITY};   // per accumulator row (wide) / query column (narrow)
     float l_run[2] = {0.f, 0.f};
     for (int j = 0; j < nsub; ++j) {
         const int base = ws + j * kSub;   // first key of this sub-tile
@@ -394,97 +418,174 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         const unsigned char* sv = sk + kSub * kPitch;
         const uint32_t vmask = s_vmask[warp][j % kWarpStages];
 
-        // S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys)
-        float s[2][4];
+        if constexpr (NR == 8) {
+            // S^T = K Q^T: 16 keys x 8 rows; two accumulators (even / odd k-steps) for independent chains
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int kcol = 8 * (lane >> 4);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
-            const int krow = 8 * nt + (lane & 7);
-            const int kcol = 8 * (lane >> 3);   // matrices: dims +0, +8, +16, +24 of a 32-dim slice
-#pragma unroll
-            for (int kp = 0; kp < 4; ++kp) {     // pairs of k-steps
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(smem_addr(sk + krow * kPitch + (32 * kp + kcol) * 2), b0, b1, b2, b3);
-                mma_bf16(s[nt], qa[2 * kp][0], qa[2 * kp][1], qa[2 * kp][2], qa[2 * kp][3], b0, b1);
-                mma_bf16(s[nt], qa[2 * kp + 1][0], qa[2 * kp + 1][1], qa[2 * kp + 1][2], qa[2 * kp + 1][3], b2, b3);
+                for (int ks = 0; ks < 8; ks += 2) {
+                    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+                    ldsm_x4(smem_addr(sk + krow * kPitch + (16 * ks + kcol) * 2), a0, a1, a2, a3);
+                    ldsm_x4(smem_addr(sk + krow * kPitch + (16 * ks + 16 + kcol) * 2), c0, c1, c2, c3);
+                    mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                    mma_bf16(sb, c0, c1, c2, c3, qf[ks + 1][0], qf[ks + 1][1]);
+                }
             }
-        }
-
-        // scale to base 2, mask, store logits (focal), online softmax
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+            // element e: key g + 8*(e >> 1) of the sub-tile, query column 2*t4 + (e & 1)
+            float x[4];
+            float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int hr = e >> 1;
-                const int pos = base + 8 * nt + 2 * t4 + (e & 1);
-                const bool ok = ((vmask >> (pos - base)) & 1u) && pos <= lim[hr];
-                const float x = ok ? s[nt][e] * p.qscale : -INFINITY;
-                s[nt][e] = x;
-                mx[hr] = fmaxf(mx[hr], x);
+                const int kr = g + 8 * (e >> 1);
+                const int qc = e & 1;
+                const bool ok = ((vmask >> kr) & 1u) && base + kr <= lim[qc];
+                x[e] = ok ? (sa[e] + sb[e]) * p.qscale : -INFINITY;
+                mx[qc] = fmaxf(mx[qc], x[e]);
             }
-        }
-        if (MODE == kModeFocal && p.logits != nullptr) {
+            if (MODE == kModeFocal && p.logits != nullptr) {
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = r0 + g + 8 * hr;
-                if (row < p.R) {
-                    float* lrow = p.logits + (int64_t)(bh * p.R + row) * p.Tcap;
+                for (int e = 0; e < 4; ++e) {
+                    const int row = r0 + 2 * t4 + (e & 1);
+                    const int pos = base + g + 8 * (e >> 1);
+                    if (row < p.R && pos < we) p.logits[(int64_t)(bh * p.R + row) * p.Tcap + pos] = x[e];
+                }
+            }
+            float alpha[2], ms[2];
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int pos = base + 8 * nt + 2 * t4;
-                        if (pos < we) lrow[pos] = s[nt][2 * hr];
-                        if (pos + 1 < we) lrow[pos + 1] = s[nt][2 * hr + 1];
+            for (int qc = 0; qc < 2; ++qc) {   // max over the 16 keys: the 8 lanes of this t4
+                mx[qc] = fmaxf(mx[qc], __shfl_xor_sync(kFull, mx[qc], 4));
+                mx[qc] = fmaxf(mx[qc], __shfl_xor_sync(kFull, mx[qc], 8));
+                mx[qc] = fmaxf(mx[qc], __shfl_xor_sync(kFull, mx[qc], 16));
+                const float mn = fmaxf(m_run[qc], mx[qc]);
+                ms[qc] = (mn == -INFINITY) ? 0.f : mn;
+                alpha[qc] = fast_exp2(m_run[qc] - ms[qc]);
+                m_run[qc] = mn;
+                l_run[qc] *= alpha[qc];
+            }
+#pragma unroll
+            for (int n = 0; n < kOT; ++n) {
+                o[n][0] *= alpha[0];
+                o[n][1] *= alpha[1];
+                o[n][2] *= alpha[0];
+                o[n][3] *= alpha[1];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[e] = fast_exp2(x[e] - ms[e & 1]);
+                l_run[e & 1] += x[e];
+            }
+            // P^T as B fragments: (keys 2t4.., row g) = the transpose of the (key g, rows 2t4..) layout;
+            // P = hi + lo in bf16
+            uint32_t h01, l01, h23, l23;
+            split_bf16(x[0], x[1], h01, l01);
+            split_bf16(x[2], x[3], h23, l23);
+            const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
+            const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
+            // O^T += V^T P^T: A fragments of V^T straight from the row-major V tile with ldmatrix.trans
+            const int vrow = (lane & 7) + 8 * (lane >> 4);
+            const int vcol = 8 * ((lane >> 3) & 1);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * mt + vcol) * 2), a0, a1, a2, a3);
+                mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+                mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            }
+        } else {
+            // S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys)
+            float s[2][4];
+    #pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+                const int krow = 8 * nt + (lane & 7);
+                const int kcol = 8 * (lane >> 3);   // matrices: dims +0, +8, +16, +24 of a 32-dim slice
+    #pragma unroll
+                for (int kp = 0; kp < 4; ++kp) {     // pairs of k-steps
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(smem_addr(sk + krow * kPitch + (32 * kp + kcol) * 2), b0, b1, b2, b3);
+                    mma_bf16(s[nt], qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
+                    mma_bf16(s[nt], qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
+                }
+            }
+
+            // scale to base 2, mask, store logits (focal), online softmax
+            float mx[2] = {-INFINITY, -INFINITY};
+    #pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int hr = e >> 1;
+                    const int pos = base + 8 * nt + 2 * t4 + (e & 1);
+                    const bool ok = ((vmask >> (pos - base)) & 1u) && pos <= lim[hr];
+                    const float x = ok ? s[nt][e] * p.qscale : -INFINITY;
+                    s[nt][e] = x;
+                    mx[hr] = fmaxf(mx[hr], x);
+                }
+            }
+            if (MODE == kModeFocal && p.logits != nullptr) {
+    #pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int row = r0 + g + 8 * hr;
+                    if (row < p.R) {
+                        float* lrow = p.logits + (int64_t)(bh * p.R + row) * p.Tcap;
+    #pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int pos = base + 8 * nt + 2 * t4;
+                            if (pos < we) lrow[pos] = s[nt][2 * hr];
+                            if (pos + 1 < we) lrow[pos + 1] = s[nt][2 * hr + 1];
+                        }
                     }
                 }
             }
-        }
-        float alpha[2], ms[2];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 1));
-            mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 2));
-            const float mn = fmaxf(m_run[hr], mx[hr]);
-            ms[hr] = (mn == -INFINITY) ? 0.f : mn;
-            alpha[hr] = fast_exp2(m_run[hr] - ms[hr]);
-            m_run[hr] = mn;
-            l_run[hr] *= alpha[hr];
-        }
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            o[n][0] *= alpha[0];
-            o[n][1] *= alpha[0];
-            o[n][2] *= alpha[1];
-            o[n][3] *= alpha[1];
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float pe = fast_exp2(s[nt][e] - ms[e >> 1]);
-                s[nt][e] = pe;
-                l_run[e >> 1] += pe;
+            float alpha[2], ms[2];
+    #pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 1));
+                mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 2));
+                const float mn = fmaxf(m_run[hr], mx[hr]);
+                ms[hr] = (mn == -INFINITY) ? 0.f : mn;
+                alpha[hr] = fast_exp2(m_run[hr] - ms[hr]);
+                m_run[hr] = mn;
+                l_run[hr] *= alpha[hr];
             }
-        }
+    #pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                o[n][0] *= alpha[0];
+                o[n][1] *= alpha[0];
+                o[n][2] *= alpha[1];
+                o[n][3] *= alpha[1];
+            }
+    #pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float pe = fast_exp2(s[nt][e] - ms[e >> 1]);
+                    s[nt][e] = pe;
+                    l_run[e >> 1] += pe;
+                }
+            }
 
-        // O += P V over this warp's 16 keys (one k-step); P = hi + lo in bf16
-        {
-            uint32_t ph[4], pl[4];
-            split_bf16(s[0][0], s[0][1], ph[0], pl[0]);
-            split_bf16(s[0][2], s[0][3], ph[1], pl[1]);
-            split_bf16(s[1][0], s[1][1], ph[2], pl[2]);
-            split_bf16(s[1][2], s[1][3], ph[3], pl[3]);
-            const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
-            const int vcol = 8 * (lane >> 4);
-#pragma unroll
-            for (int np2 = 0; np2 < 8; ++np2) {   // pairs of 8-dim n-tiles
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * np2 + vcol) * 2), b0, b1, b2, b3);
-                mma_bf16(o[2 * np2], ph[0], ph[1], ph[2], ph[3], b0, b1);
-                mma_bf16(o[2 * np2], pl[0], pl[1], pl[2], pl[3], b0, b1);
-                mma_bf16(o[2 * np2 + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-                mma_bf16(o[2 * np2 + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+            // O += P V over this warp's 16 keys (one k-step); P = hi + lo in bf16
+            {
+                uint32_t ph[4], pl[4];
+                split_bf16(s[0][0], s[0][1], ph[0], pl[0]);
+                split_bf16(s[0][2], s[0][3], ph[1], pl[1]);
+                split_bf16(s[1][0], s[1][1], ph[2], pl[2]);
+                split_bf16(s[1][2], s[1][3], ph[3], pl[3]);
+                const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int vcol = 8 * (lane >> 4);
+    #pragma unroll
+                for (int np2 = 0; np2 < 8; ++np2) {   // pairs of 8-dim n-tiles
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * np2 + vcol) * 2), b0, b1, b2, b3);
+                    mma_bf16(o[2 * np2], ph[0], ph[1], ph[2], ph[3], b0, b1);
+                    mma_bf16(o[2 * np2], pl[0], pl[1], pl[2], pl[3], b0, b1);
+                    mma_bf16(o[2 * np2 + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+                    mma_bf16(o[2 * np2 + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+                }
             }
         }
 
@@ -494,30 +595,54 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     cp_async_wait_all_groups();
     __syncthreads();       // all warps are done with their buffers (reused below)
 
-    // row sums over the quad
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        l_run[hr] += __shfl_xor_sync(kFull, l_run[hr], 1);
-        l_run[hr] += __shfl_xor_sync(kFull, l_run[hr], 2);
-    }
-
     // ---- combine the warps into this CTA's partial (the stage buffers are free now) -------------
-    const int nr = min(kRowsPerCta, p.R - r0);   // rows of this group that exist
+    const int nr = min(NR, p.R - r0);   // rows of this group that exist
     __shared__ float sm_m[kWarps][kRowsPerCta];
     __shared__ float sm_l[kWarps][kRowsPerCta];
     float* sm_o = reinterpret_cast<float*>(sKV);   // [kWarps][16][128]
+    if constexpr (NR == 8) {
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {   // only the rows that exist
-        const int c = 8 * n + 2 * t4;
-        if (g < nr) *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kHeadDim + c) = make_float2(o[n][0], o[n][1]);
-        if (g + 8 < nr)
-            *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kHeadDim + c) = make_float2(o[n][2], o[n][3]);
-    }
-    if (t4 == 0) {
-        sm_m[warp][g] = m_run[0];
-        sm_m[warp][g + 8] = m_run[1];
-        sm_l[warp][g] = l_run[0];
-        sm_l[warp][g + 8] = l_run[1];
+        for (int qc = 0; qc < 2; ++qc) {   // sums over the 16 keys: the 8 lanes of this t4
+            l_run[qc] += __shfl_xor_sync(kFull, l_run[qc], 4);
+            l_run[qc] += __shfl_xor_sync(kFull, l_run[qc], 8);
+            l_run[qc] += __shfl_xor_sync(kFull, l_run[qc], 16);
+        }
+#pragma unroll
+        for (int qc = 0; qc < 2; ++qc) {
+            const int r = 2 * t4 + qc;
+            if (r < nr) {
+                float* dst = sm_o + (warp * kRowsPerCta + r) * kHeadDim + g;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    dst[16 * mt] = o[mt][qc];
+                    dst[16 * mt + 8] = o[mt][2 + qc];
+                }
+                if (g == 0) {
+                    sm_m[warp][r] = m_run[qc];
+                    sm_l[warp][r] = l_run[qc];
+                }
+            }
+        }
+    } else {
+        // row sums over the quad
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            l_run[hr] += __shfl_xor_sync(kFull, l_run[hr], 1);
+            l_run[hr] += __shfl_xor_sync(kFull, l_run[hr], 2);
+        }
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {   // only the rows that exist
+            const int c = 8 * n + 2 * t4;
+            if (g < nr) *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kHeadDim + c) = make_float2(o[n][0], o[n][1]);
+            if (g + 8 < nr)
+                *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kHeadDim + c) = make_float2(o[n][2], o[n][3]);
+        }
+        if (t4 == 0) {
+            sm_m[warp][g] = m_run[0];
+            sm_m[warp][g + 8] = m_run[1];
+            sm_l[warp][g] = l_run[0];
+            sm_l[warp][g + 8] = l_run[1];
+        }
     }
     __syncthreads();
 
@@ -734,13 +859,13 @@ __global__ void __launch_bounds__(256) focal_combine_kernel(const FocalCombinePa
     }
 }
 
-template <int MODE, int MERGE>
+template <int MODE, int MERGE, int NR>
 cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
 {
     static int configured = -1;
     int dev = 0;
     cudaGetDevice(&dev);
-    auto kern = attn_tile_kernel<MODE, MERGE>;
+    auto kern = attn_tile_kernel<MODE, MERGE, NR>;
     const bool cluster = MERGE != kMergeWorkspace;
     if (configured != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -758,21 +883,35 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
     return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, cluster ? (unsigned)p.nsplit : 0u, p);
 }
 
+template <int MODE, int NR>
+cudaError_t launch_rows(const AttnParams& p, bool pdl, cudaStream_t s)
+{
+    if constexpr (MODE == kModeFocal) {
+        return launch_one<MODE, kMergeWorkspace, NR>(p, pdl, s);
+    } else {
+        const bool cl = p.nsplit <= kMaxClusterSplits;
+        // pushed partials of the other CTAs must fit CTA 0's receive area
+        const int rows = p.R < NR ? p.R : NR;
+        const bool push = cl && (p.nsplit - 1) * rows * (kHeadDim + 2) <= kRecvFloats;
+        if (push) return launch_one<MODE, kMergePush, NR>(p, pdl, s);
+        return cl ? launch_one<MODE, kMergePull, NR>(p, pdl, s) : launch_one<MODE, kMergeWorkspace, NR>(p, pdl, s);
+    }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const AttnParams& p, bool pdl, cudaStream_t s)
+{
+    return p.rb == 8 ? launch_rows<MODE, 8>(p, pdl, s) : launch_rows<MODE, 16>(p, pdl, s);
+}
+
 }  // namespace
 
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s)
 {
-    if (mode == kModeFocal) return launch_one<kModeFocal, kMergeWorkspace>(p, pdl, s);
-    const bool cl = p.nsplit <= kMaxClusterSplits;
-    // pushed partials of the other CTAs must fit CTA 0's receive area
-    const int rows = p.R < kRowsPerCta ? p.R : kRowsPerCta;
-    const bool push = cl && (p.nsplit - 1) * rows * (kHeadDim + 2) <= kRecvFloats;
-    if (mode == kModeSparse) {
-        if (push) return launch_one<kModeSparse, kMergePush>(p, pdl, s);
-        return cl ? launch_one<kModeSparse, kMergePull>(p, pdl, s) : launch_one<kModeSparse, kMergeWorkspace>(p, pdl, s);
-    }
-    if (push) return launch_one<kModePrefix, kMergePush>(p, pdl, s);
-    return cl ? launch_one<kModePrefix, kMergePull>(p, pdl, s) : launch_one<kModePrefix, kMergeWorkspace>(p, pdl, s);
+    if (p.rb != 8 && p.rb != 16) return cudaErrorInvalidValue;
+    if (mode == kModeFocal) return launch_mode<kModeFocal>(p, pdl, s);
+    if (mode == kModeSparse) return launch_mode<kModeSparse>(p, pdl, s);
+    return launch_mode<kModePrefix>(p, pdl, s);
 }
 
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s)

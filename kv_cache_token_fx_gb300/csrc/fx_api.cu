@@ -277,6 +277,7 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     p.nsplit = pl.nsplit;
     p.split_len = pl.split_len;
     p.nrg = pl.nrg;
+    p.rb = pl.rb;
     p.stages = pl.stages;
     p.part_m = reinterpret_cast<float*>(w + L.part_m);
     p.part_l = reinterpret_cast<float*>(w + L.part_l);
@@ -397,6 +398,7 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     p.nsplit = pl.nsplit;
     p.split_len = pl.split_len;
     p.nrg = pl.nrg;
+    p.rb = pl.rb;
     p.stages = pl.stages;
     p.part_m = reinterpret_cast<float*>(w + L.part_m);
     p.part_l = reinterpret_cast<float*>(w + L.part_l);
@@ -554,6 +556,7 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     p.nsplit = pl.nsplit;
     p.split_len = pl.split_len;
     p.nrg = pl.nrg;
+    p.rb = pl.rb;
     p.stages = pl.stages;
     p.part_m = reinterpret_cast<float*>(w + L.part_m);
     p.part_l = reinterpret_cast<float*>(w + L.part_l);

@@ -73,6 +73,7 @@ struct AttnParams {
     int64_t dr_sb, dr_si, dr_sh;
     // split geometry
     int nsplit, split_len, nrg, stages;
+    int rb;         // query rows per CTA (8 or 16)
     int prefetch;   // lengths / indices / K-V rows may be read before the preceding kernel finishes
     // outputs / scratch
     float* part_m;        // [B*Hkv*R*nsplit]
@@ -169,6 +170,7 @@ __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.
 #endif
 
 // Row-group width used for a given number of query rows per KV head (one 16-row MMA tile).
-inline int rows_per_block(int /*R*/) { return kRowsPerCta; }
+// Query rows per attention CTA: 8 (keys on the MMA's M side) when at most 8 rows exist, else 16.
+inline int rows_per_block(int R) { return R <= 8 ? 8 : kRowsPerCta; }
 
 }  // namespace fx
