@@ -138,6 +138,44 @@ __device__ __forceinline__ void cluster_wait_acquire()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+// asynchronous stores into another CTA's shared memory that complete bytes on that CTA's mbarrier
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+                 "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init_for_cluster(uint64_t* bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, unsigned parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v)
 {
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
@@ -240,6 +278,13 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     // FX_LAUNCH_INPUTS_READY it runs before the preceding kernel on the stream has finished, so the
     // first tiles are already in flight when that kernel ends.
     const bool early = p.prefetch != 0;
+    // kMergePush: CTA 0's barrier for the pushed partials, initialised before anything else; the cluster
+    // barrier phase opened here (closed before the first push) makes the initialisation visible.
+    __shared__ __align__(8) uint64_t s_merge_bar;
+    if constexpr (MERGE == kMergePush) {
+        if (tid == 0 && cluster_rank() == 0) mbar_init_for_cluster(&s_merge_bar, 1);
+        cluster_arrive_relaxed();
+    }
     if (!early) griddep_wait();
 
     // key sequence of this (b, h)
@@ -671,29 +716,38 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
 
     if constexpr (MERGE == kMergePush) {
-        // CTAs 1 .. cs-1 store their partial into CTA 0's receive area and arrive on the cluster barrier,
-        // then exit (the barrier's wait only counts threads that have not exited); CTA 0 arrives, waits
-        // -- after which every partial is visible -- and merges alone.  One barrier phase in all.
+        // CTAs 1 .. cs-1 send their partial into CTA 0's receive area with asynchronous remote stores
+        // that count their bytes on CTA 0's barrier, and exit at once; CTA 0 announces the bytes it
+        // expects, waits for them and merges alone.
         __shared__ __align__(16) float s_recv[kRecvFloats];   // [cs-1][nr][128] O, [cs-1][nr] m, [cs-1][nr] l
         const unsigned cs = cluster_size();
         const unsigned me = cluster_rank();
         const int npeer = (int)cs - 1;
         float* recv_m = s_recv + npeer * nr * kHeadDim;
         float* recv_l = recv_m + npeer * nr;
+        __syncthreads();          // the combined partial (written by all threads) is complete
+        cluster_wait_acquire();   // CTA 0's barrier is initialised
         if (me != 0) {
-            __syncthreads();   // the combined partial (written by all threads) is complete
+            const uint32_t rbar = cluster_map(&s_merge_bar, 0);
             const uint32_t dst = cluster_map(s_recv + (me - 1) * nr * kHeadDim, 0);
             for (int e = tid; e < nr * (kHeadDim / 4); e += kThreads)
-                st_cluster_v4(dst + 16 * e, *reinterpret_cast<const float4*>(c_o + 4 * e));
+                st_async_v4(dst + 16 * e, *reinterpret_cast<const float4*>(c_o + 4 * e), rbar);
             if (tid < nr) {
-                st_cluster_f32(cluster_map(recv_m + (me - 1) * nr + tid, 0), c_m[tid]);
-                st_cluster_f32(cluster_map(recv_l + (me - 1) * nr + tid, 0), c_l[tid]);
+                st_async_f32(cluster_map(recv_m + (me - 1) * nr + tid, 0), c_m[tid], rbar);
+                st_async_f32(cluster_map(recv_l + (me - 1) * nr + tid, 0), c_l[tid], rbar);
             }
-            cluster_arrive_release();
             return;
         }
-        cluster_arrive_release();
-        cluster_wait_acquire();
+        if (npeer > 0) {
+            if (tid == 0) mbar_arrive_expect_tx(&s_merge_bar, (unsigned)(npeer * nr * (kHeadDim + 2) * 4));
+            unsigned spins = 0;
+            while (!mbar_try_wait_cluster(&s_merge_bar, 0)) {
+                if (++spins == kSpinLimit) {
+                    if (tid == 0) flag(p.err, FX_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+        }
         for (int e = tid; e < nr * kHeadDim; e += kThreads) {
             const int r = e >> 7;
             const int c = e & (kHeadDim - 1);
