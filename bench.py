@@ -217,6 +217,8 @@ class OcrDecodeRun:
         self.rt = _cudart()
         self.graphs, self.graphs_e2e, self.graphs_sparse, self.sparse_bytes = {}, {}, {}, {}
         self.launches_per_step = 0
+        self.launches_estimate = 0
+        self.launches_source = None
 
     # one decode step; `only_sparse` replays just the sparse-decode launches of the step (used to time
     # the dominant kernel on its own); `nbytes_out` collects the algorithmic bytes of each sparse launch.
@@ -238,7 +240,7 @@ class OcrDecodeRun:
                                         scores=self.scores, ws=self.ws, flags=pdl | ready)
                 prev = self.sets[l][1 - p] if t > 0 else None
                 fx.fx_topk_select(self.scores, w.k_keep, prev=prev, out=self.sets[l][p], flags=pdl)
-                launches += 3
+                launches += 2   # attention + top-k (a separate combine kernel, if any, is not counted here)
                 after_topk = True
                 continue
             if l < w.focal_layers[0]:
@@ -259,7 +261,7 @@ class OcrDecodeRun:
                 nbytes_out.append(nbytes)
             launches += 1
         if not only_sparse:
-            self.launches_per_step = launches
+            self.launches_estimate = launches
 
     def e2e_inputs(self, t: int):
         """Copy step t's inputs from pinned host memory (queries, new K/V row) into device memory."""
@@ -277,7 +279,36 @@ class OcrDecodeRun:
             if err != 0:
                 raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
 
+    def count_kernel_nodes(self, t: int):
+        """Kernel launches of one step, counted as the kernel nodes of a captured graph of it (None when
+        this PyTorch cannot hand out the raw graph)."""
+        try:
+            g = torch.cuda.CUDAGraph(keep_graph=True)
+        except TypeError:
+            return None
+        s = torch.cuda.Stream(self.dev)
+        with torch.cuda.graph(g, stream=s):
+            self.step(t)
+        rt = self.rt
+        graph = ctypes.c_void_p(int(g.raw_cuda_graph()))
+        n = ctypes.c_size_t(0)
+        if rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
+            return None
+        nodes = (ctypes.c_void_p * n.value)()
+        if rt.cudaGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
+            return None
+        kernels = 0
+        for i in range(n.value):
+            ty = ctypes.c_int(-1)
+            if rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(ty)) != 0:
+                return None
+            kernels += int(ty.value == 0)   # cudaGraphNodeTypeKernel
+        del g
+        return kernels
+
     def capture(self):
+        counted = self.count_kernel_nodes(self.w.steps - 1)
+        self.launches_source = "kernel nodes of a captured step graph" if counted is not None else "host count"
         s = torch.cuda.Stream(self.dev)
         for t in range(self.w.steps):
             g = torch.cuda.CUDAGraph()
@@ -289,6 +320,7 @@ class OcrDecodeRun:
             with torch.cuda.graph(gs, stream=s):
                 self.step(t, only_sparse=True, nbytes_out=nb)
             self.graphs_sparse[t] = gs
+            self.launches_per_step = counted if counted is not None else self.launches_estimate
             self.sparse_bytes[t] = nb
             if self.with_e2e:
                 g2 = torch.cuda.CUDAGraph()
@@ -413,6 +445,7 @@ def run_fx(args, rank, local, ws):
         "kv_gbs": round(kv_gbs, 1), "kv_frac_of_hbm": round(kv_gbs / ws / peak, 4),
         "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
         "gpu_launches": run.launches_per_step * len(steps),
+        "gpu_launches_source": run.launches_source,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -130,10 +130,6 @@ __device__ __forceinline__ float ld_cluster(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_wait_acquire()
 {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -176,15 +172,10 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, unsigned pa
         : "memory");
     return done != 0;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v)
+
+__device__ __forceinline__ void prefetch_l2(const void* p)
 {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
-{
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // ---- key sequences --------------------------------------------------------------------------------
@@ -385,6 +376,16 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 
 #pragma unroll
     for (int j = 0; j < kWarpStages; ++j) issue(j, tpre[j]);
+
+    // The query rows may be written by the preceding kernel, so they are read only after the wait
+    // below; a prefetch into L2 is only a hint (L2 stays coherent with later writes) and shortens that
+    // read when the rows were not in L2 yet.  Two 128-byte lines per row.
+    if (tid < 2 * NR && r0 + (tid >> 1) < p.R) {
+        const int row = r0 + (tid >> 1);
+        const int gi = row / p.Mq;
+        const int i = row - gi * p.Mq;
+        prefetch_l2(p.q + ((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + 64 * (tid & 1));
+    }
 
     // ---- stage B: after the preceding kernel -- the query rows, then everything that writes ------
     if (early) griddep_wait();
