@@ -1,22 +1,27 @@
 // Split-KV decode / verify attention for sm_103a.
 //
-// One CTA (4 warps) = (group of up to 16 query rows of one KV head, one split of that head's key
-// sequence, one (b, KV head)).  The split is walked in tiles of 64 keys:
-//   * Data movement: the K and V rows of a tile (256 bytes each; contiguous rows for the focal mode,
-//     gathered rows for the sparse/prefix modes) are copied into shared memory with 16-byte cp.async
-//     operations, each warp instruction moving two whole rows, one commit group per tile.  Rows are padded to 272 bytes so
-//     that the 8-row ldmatrix reads below hit 8 different bank groups.  Two stages: tile i+1 is in
-//     flight while tile i is used.  Rows that must not be read (past the split, rejected index) are
-//     zero-filled instead.  (Per-row cp.async.bulk TMA copies were measured slower here: 256-byte
-//     requests keep the TMA engine, not HBM, busy.)
-//   * Math: each warp takes 16 keys of the tile.  S = Q K^T with mma.sync m16n8k16 (bf16 in, fp32
-//     accumulate; the query rows sit in one 16-row A tile, rows past R are zero), then an online
-//     softmax on the accumulator fragments in base-2 units, then O += P V with the same MMA, where P
-//     is split into bf16 hi + lo parts (two MMAs) so that the probabilities keep ~16 bits.
-// Partial (max, sum, unnormalised output) triples per split are merged either inside a thread-block
-// cluster -- all splits of one (b, h, row group) form one cluster and read each other's partials
-// from distributed shared memory -- or, for the focal call and for very long rows, through the
-// workspace (the focal call's combine kernel also forms the per-token importance from the logits
+// One CTA (4 warps) = (group of NR = 8 or 16 query rows of one KV head, one split of that head's key
+// sequence, one (b, KV head)).  Each warp owns a fixed, contiguous range of whole 16-key sub-tiles of
+// the split and walks it on its own:
+//   * Data movement: the warp stages its sub-tiles (16 K rows + 16 V rows of 256 bytes; contiguous
+//     rows for the focal mode, gathered rows for the sparse/prefix modes) into a private ring of
+//     kWarpStages buffers with 16-byte cp.async, each warp instruction moving two whole rows, one
+//     commit group per sub-tile, so no CTA-wide barrier is needed in the loop.  Lane l resolves the
+//     token of row l & 15 (one index load per lane); the copies take the row addresses by warp
+//     shuffle and a ballot records which rows are valid.  Rows are padded to 272 bytes so that the
+//     8-row ldmatrix reads hit 8 different bank groups; invalid rows are zero-filled.  (Per-row
+//     cp.async.bulk TMA copies were measured slower here: 256-byte requests keep the TMA engine, not
+//     HBM, busy.)
+//   * Math: mma.sync m16n8k16 (bf16 in, fp32 accumulate), online softmax on the accumulator
+//     fragments in base-2 units, P split into bf16 hi + lo parts (two MMAs) so that the
+//     probabilities keep ~16 bits.  With NR = 8 the keys are the M side (S^T = K Q^T, O^T = V^T P^T,
+//     P^T moved into the B operand with movmatrix.trans): half the MMAs of the NR = 16 layout, where
+//     the query rows are the M side (S = Q K^T, O = P V).
+// Partial (max, sum, unnormalised output) triples per split are merged inside a thread-block cluster
+// -- all splits of one (b, h, row group) form one cluster; either the others push their partials
+// into CTA 0 with st.async (completing on CTA 0's mbarrier) and exit, or every CTA reads all
+// partials from distributed shared memory -- or, for the focal call and for very long rows, through
+// the workspace (the focal call's combine kernel also forms the per-token importance from the logits
 // this kernel stores).
 //
 // Attention and importance follow FastOCR (Methodology: Focal-Guided Pruning): focal layers attend
