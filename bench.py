@@ -208,11 +208,16 @@ class OcrDecodeRun:
         self.with_e2e = with_e2e
         self.pdl = pdl
         if with_e2e:
-            # the per-step inputs as a host would hold them: queries of all layers and the new K/V row
-            self.Q_host = self.Q.cpu().pin_memory()
+            # the per-step inputs as a host would hold them, one pinned block per step:
+            # [queries of all layers | new K rows | new V rows]
+            self.nq = self.Q[0].numel()
             pos = [w.n_vis + w.n_text + t for t in range(w.steps)]
-            self.Knew_host = torch.stack([self.K[:, :, :, p] for p in pos]).cpu().pin_memory()
-            self.Vnew_host = torch.stack([self.V[:, :, :, p] for p in pos]).cpu().pin_memory()
+            knew = torch.stack([self.K[:, :, :, p] for p in pos])
+            vnew = torch.stack([self.V[:, :, :, p] for p in pos])
+            self.nkv = knew[0].numel()
+            self.In_host = torch.cat([self.Q.reshape(w.steps, -1), knew.reshape(w.steps, -1),
+                                      vnew.reshape(w.steps, -1)], dim=1).cpu().pin_memory()
+            del knew, vnew
             self.O_host = torch.empty(self.O.shape, dtype=torch.float32).pin_memory()
         self.rt = _cudart()
         self.graphs, self.graphs_e2e, self.graphs_sparse, self.sparse_bytes = {}, {}, {}, {}
@@ -264,18 +269,20 @@ class OcrDecodeRun:
             self.launches_estimate = launches
 
     def e2e_inputs(self, t: int):
-        """Copy step t's inputs from pinned host memory (queries, new K/V row) into device memory."""
+        """Copy step t's inputs from pinned host memory into device memory: the queries of all layers in
+        one copy, and the new K and V rows in one strided 2-D copy each (28*8*8 rows of 256 bytes; the
+        device pitch is one (layer, b, h) cache)."""
         w = self.w
-        self.Q[t].copy_(self.Q_host[t], non_blocking=True)
+        nq, nkv = self.nq, self.nkv
+        self.Q[t].copy_(self.In_host[t, :nq].view(self.Q[t].shape), non_blocking=True)
         pos = w.n_vis + w.n_text + t
-        # one strided 2-D copy per tensor: 28*8*8 rows of 256 bytes, device pitch = one (l, b, h) cache
-        for dst, src in ((self.K, self.Knew_host), (self.V, self.Vnew_host)):
-            rows = w.n_layers * w.B * w.Hkv
-            dptr = dst.data_ptr() + pos * D * 2
-            err = self.rt.cudaMemcpy2DAsync(ctypes.c_void_p(dptr), ctypes.c_size_t(w.tcap * D * 2),
-                                            ctypes.c_void_p(src[t].data_ptr()), ctypes.c_size_t(D * 2),
-                                            ctypes.c_size_t(D * 2), ctypes.c_size_t(rows), ctypes.c_int(1),
-                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        rows = w.n_layers * w.B * w.Hkv
+        for dst, off in ((self.K, nq), (self.V, nq + nkv)):
+            err = self.rt.cudaMemcpy2DAsync(ctypes.c_void_p(dst.data_ptr() + pos * D * 2),
+                                            ctypes.c_size_t(w.tcap * D * 2),
+                                            ctypes.c_void_p(self.In_host[t].data_ptr() + off * 2),
+                                            ctypes.c_size_t(D * 2), ctypes.c_size_t(D * 2), ctypes.c_size_t(rows),
+                                            ctypes.c_int(1), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
             if err != 0:
                 raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
 
@@ -346,6 +353,13 @@ def run_fx(args, rank, local, ws):
         raise RuntimeError("device error flag set during warm-up")
 
     steps = [(args.warmup + i) % w.steps for i in range(args.steps)]
+    # every graph is launched once before any timing: its first launch also uploads it to the device
+    for t in range(w.steps):
+        run.graphs[t].replay()
+        run.graphs_sparse[t].replay()
+        if run.with_e2e:
+            run.graphs_e2e[t].replay()
+    torch.cuda.synchronize()
     for i in range(args.warmup):
         run.graphs[i % w.steps].replay()
     torch.cuda.synchronize()
@@ -418,7 +432,7 @@ def run_fx(args, rank, local, ws):
         torch.cuda.synchronize()
         barrier(ws)
         ems = max_over_ranks(a.elapsed_time(b), ws)
-        h2d = run.Q_host[0].numel() * 2 + run.Knew_host[0].numel() * 2 * 2
+        h2d = run.In_host[0].numel() * 2
         d2h = run.O_host.numel() * 4
         e2e = {"value": round(tokens / (ems / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ems / len(steps), 4)}
