@@ -3,10 +3,9 @@
 // Order: score descending, index ascending (FastOCR, Focal-Guided Pruning: the top-attended tokens;
 // ties go to the lower index).  Each fp32 score maps to a uint32 key that orders like the float.
 // Four 8-bit radix passes find K*, the k-th largest key, and how many keys equal to K* must be taken
-// (need_eq).  A final ordered pass -- tiles of 1024 scores, one per thread, with a block-wide
-// exclusive scan of (greater, equal) counts -- writes every index with key > K* and the first need_eq
-// indices with key == K*, in ascending index order.  No atomics decide the output, so the result is
-// bit-reproducible.
+// (need_eq).  A final ordered pass -- a block-wide exclusive scan of (greater, equal) counts --
+// writes every index with key > K* and the first need_eq indices with key == K*, in ascending index
+// order.  No atomics decide the output, so the result is bit-reproducible.
 //
 // Warm start (FastOCR, Cross-Step Fixation Reuse): with the previous set S_prev, the threshold
 // T = min over S_prev of the current scores is exceeded-or-met by at least k entries, so the top-k
@@ -69,61 +68,95 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
     return res;
 }
 
-template <bool SMEM>
-__global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
+// Warp 0 (all 32 lanes): the radix digit that holds the krem-th largest counted key, from the 256-bin
+// histogram, and the number of counted keys in higher bins; digit = 0xffffffff when fewer than krem
+// keys were counted.
+__device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t krem, uint32_t* digit, uint32_t* gt_out)
 {
-    extern __shared__ uint32_t skeys[];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t swarp[33];
-    __shared__ uint32_t s_digit, s_gt, s_thr, s_bad;
+    const int lane = threadIdx.x & 31;
+    uint32_t loc[8];
+    uint32_t tot = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        loc[e] = hist[8 * lane + e];
+        tot += loc[e];
+    }
+    uint32_t inc = tot;   // inclusive suffix sum over lanes >= lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xffffffffu, inc, o);
+        if (lane + o < 32) inc += t;
+    }
+    const uint32_t all = __shfl_sync(0xffffffffu, inc, 0);
+    uint32_t run = inc - tot;   // count of digits above this lane's bins
+    int found = -1;
+    uint32_t gt = 0u;
+#pragma unroll
+    for (int e = 7; e >= 0; --e) {
+        const uint32_t before = run;
+        run += loc[e];
+        if (found < 0 && run >= krem && before < krem) {
+            found = 8 * lane + e;
+            gt = before;
+        }
+    }
+    if (found >= 0) {
+        *digit = (uint32_t)found;
+        *gt_out = gt;
+    }
+    if (lane == 0 && all < krem) *digit = 0xffffffffu;   // fewer candidates than needed
+}
 
-    griddep_wait();   // the scores usually come from the kernel just before
-    griddep_launch();
-    const int row = blockIdx.x;
+struct SelectShared {
+    uint32_t hist[256];
+    uint32_t swarp[33];
+    uint32_t digit, gt, thr, bad;
+};
+
+// The top-k of one row of n keys (in skeys when SMEM, else read from src), written to orow in
+// ascending index order.  prow: the previous set of this row (warm start) or nullptr.  All threads of
+// the CTA call it; it begins and ends with a barrier.
+template <bool SMEM>
+__device__ void select_row(SelectShared& sh, const uint32_t* skeys, const float* src, int n, int k,
+                           const int32_t* prow, int32_t* orow, unsigned* err)
+{
     const int tid = threadIdx.x;
     const int lane = tid & 31;
-    const int n = p.n;
-    const float* src = p.scores + (int64_t)row * n;
-
-    if (SMEM) {
-        for (int j = tid; j < n; j += kTkThreads) skeys[j] = order_key(src[j]);
-    }
     if (tid == 0) {
-        s_thr = p.prev != nullptr ? 0xffffffffu : 0u;
-        s_bad = 0u;
+        sh.thr = prow != nullptr ? 0xffffffffu : 0u;
+        sh.bad = 0u;
     }
     __syncthreads();
 
     // ---- warm-start threshold ----------------------------------------------------------------
     uint32_t thr = 0u;
-    if (p.prev != nullptr) {
+    if (prow != nullptr) {
         uint32_t kmin = 0xffffffffu;
-        const int32_t* prow = p.prev + (int64_t)row * p.k;
-        for (int i = tid; i < p.k; i += kTkThreads) {
+        for (int i = tid; i < k; i += kTkThreads) {
             const int t = prow[i];
             if (t < 0 || t >= n)
-                s_bad = 1u;
+                sh.bad = 1u;
             else
                 kmin = min(kmin, get_key<SMEM>(skeys, src, t));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-        if (lane == 0) atomicMin(&s_thr, kmin);
+        if (lane == 0) atomicMin(&sh.thr, kmin);
         __syncthreads();
-        if (s_bad) {
-            if (tid == 0) atomicOr(p.err, FX_DEVERR_INDEX);
+        if (sh.bad) {
+            if (tid == 0) atomicOr(err, FX_DEVERR_INDEX);
         } else {
-            thr = s_thr;
+            thr = sh.thr;
         }
     }
 
     // ---- radix select: K* and the number of equal keys to take --------------------------------
     uint32_t prefix = 0u, pmask = 0u;
-    uint32_t krem = (uint32_t)p.k;
+    uint32_t krem = (uint32_t)k;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         for (int attempt = 0; attempt < 2; ++attempt) {
-            for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
+            for (int i = tid; i < 256; i += kTkThreads) sh.hist[i] = 0u;
             __syncthreads();
             for (int j0 = 0; j0 < n; j0 += kTkThreads) {
                 const int j = j0 + tid;   // whole warps iterate together (ballot/match below)
@@ -133,45 +166,13 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
                 if (take) {
                     const uint32_t digit = (key >> shift) & 255u;
                     const unsigned peers = __match_any_sync(active, digit);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+                    if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
                 }
             }
             __syncthreads();
-            if (tid < 32) {
-                uint32_t loc[8];
-                uint32_t tot = 0u;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    loc[e] = hist[8 * tid + e];
-                    tot += loc[e];
-                }
-                uint32_t inc = tot;   // inclusive suffix sum over lanes >= tid
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t t = __shfl_down_sync(0xffffffffu, inc, o);
-                    if (tid + o < 32) inc += t;
-                }
-                const uint32_t all = __shfl_sync(0xffffffffu, inc, 0);
-                uint32_t run = inc - tot;   // count of digits above this lane's bins
-                int found = -1;
-                uint32_t gt = 0u;
-#pragma unroll
-                for (int e = 7; e >= 0; --e) {
-                    const uint32_t before = run;
-                    run += loc[e];
-                    if (found < 0 && run >= krem && before < krem) {
-                        found = 8 * tid + e;
-                        gt = before;
-                    }
-                }
-                if (found >= 0) {
-                    s_digit = (uint32_t)found;
-                    s_gt = gt;
-                }
-                if (tid == 0 && all < krem) s_digit = 0xffffffffu;  // fewer candidates than needed
-            }
+            if (tid < 32) find_digit(sh.hist, krem, &sh.digit, &sh.gt);
             __syncthreads();
-            if (s_digit == 0xffffffffu && thr != 0u) {
+            if (sh.digit == 0xffffffffu && thr != 0u) {
                 // only possible in pass 0 with a warm-start threshold built from repeated indices:
                 // drop the threshold and count again
                 thr = 0u;
@@ -180,52 +181,112 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
             }
             break;
         }
-        const bool missing = (s_digit == 0xffffffffu);
+        const bool missing = (sh.digit == 0xffffffffu);
         __syncthreads();
         if (missing) {
             // unreachable for 1 <= k <= n (checked on the host); keep the kernel finite anyway
             if (tid == 0) {
-                atomicOr(p.err, FX_DEVERR_INDEX);
-                s_digit = 0u;
-                s_gt = 0u;
+                atomicOr(err, FX_DEVERR_INDEX);
+                sh.digit = 0u;
+                sh.gt = 0u;
             }
             __syncthreads();
         }
-        prefix |= s_digit << shift;
+        prefix |= sh.digit << shift;
         pmask |= 255u << shift;
-        krem -= s_gt;
+        krem -= sh.gt;
         __syncthreads();
     }
     const uint32_t kstar = prefix;
     const uint32_t need_eq = krem;
 
     // ---- ordered output -------------------------------------------------------------------------
-    int32_t* orow = p.out + (int64_t)row * p.k;
-    uint32_t base_g = 0u, base_e = 0u;
-    for (int t0 = 0; t0 < n; t0 += kTkThreads) {
-        const int j = t0 + tid;
-        uint32_t key = 0u;
+    // position of an index j = (# greater before j) + min(# equal before j, need_eq); an equal key is
+    // taken while (# equal before j) < need_eq.  Positions are < k by construction; the bound checks
+    // keep a logic slip from writing past the row.
+    if (SMEM) {
+        // each thread owns a contiguous chunk of the row: one scan for the whole row
+        const int per = (n + kTkThreads - 1) / kTkThreads;
+        const int j0 = tid * per;
+        const int j1 = min(n, j0 + per);
         uint32_t g = 0u, e = 0u;
-        if (j < n) {
-            key = get_key<SMEM>(skeys, src, j);
-            g = key > kstar ? 1u : 0u;
-            e = key == kstar ? 1u : 0u;
+        for (int j = j0; j < j1; ++j) {
+            const uint32_t key = skeys[j];
+            g += key > kstar ? 1u : 0u;
+            e += key == kstar ? 1u : 0u;
         }
         uint32_t total;
-        const uint32_t ex = block_exclusive_scan(g | (e << 16), swarp, &total);
-        const uint32_t gc = base_g + (ex & 0xffffu);
-        const uint32_t ec = base_e + (ex >> 16);
-        // positions are < k by construction; the bound check keeps a logic slip from writing past the row
-        if (g) {
-            const uint32_t pos = gc + min(ec, need_eq);
-            if (pos < (uint32_t)p.k) orow[pos] = j;
-        } else if (e && ec < need_eq) {
-            const uint32_t pos = gc + ec;
-            if (pos < (uint32_t)p.k) orow[pos] = j;
+        const uint32_t ex = block_exclusive_scan(g | (e << 16), sh.swarp, &total);
+        uint32_t gc = ex & 0xffffu;
+        uint32_t ec = ex >> 16;
+        for (int j = j0; j < j1; ++j) {
+            const uint32_t key = skeys[j];
+            if (key > kstar) {
+                const uint32_t pos = gc + min(ec, need_eq);
+                if (pos < (uint32_t)k) orow[pos] = j;
+                ++gc;
+            } else if (key == kstar) {
+                if (ec < need_eq && gc + ec < (uint32_t)k) orow[gc + ec] = j;
+                ++ec;
+            }
         }
-        base_g += total & 0xffffu;
-        base_e += total >> 16;
+    } else {
+        // tiles of one key per thread (coalesced global reads), one scan per tile
+        uint32_t base_g = 0u, base_e = 0u;
+        for (int t0 = 0; t0 < n; t0 += kTkThreads) {
+            const int j = t0 + tid;
+            uint32_t g = 0u, e = 0u;
+            if (j < n) {
+                const uint32_t key = get_key<SMEM>(skeys, src, j);
+                g = key > kstar ? 1u : 0u;
+                e = key == kstar ? 1u : 0u;
+            }
+            uint32_t total;
+            const uint32_t ex = block_exclusive_scan(g | (e << 16), sh.swarp, &total);
+            const uint32_t gc = base_g + (ex & 0xffffu);
+            const uint32_t ec = base_e + (ex >> 16);
+            if (g) {
+                const uint32_t pos = gc + min(ec, need_eq);
+                if (pos < (uint32_t)k) orow[pos] = j;
+            } else if (e && ec < need_eq) {
+                const uint32_t pos = gc + ec;
+                if (pos < (uint32_t)k) orow[pos] = j;
+            }
+            base_g += total & 0xffffu;
+            base_e += total >> 16;
+        }
     }
+    __syncthreads();
+}
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
+{
+    extern __shared__ uint32_t skeys[];
+    __shared__ SelectShared sh;
+
+    griddep_wait();   // the scores usually come from the kernel just before
+    griddep_launch();
+    const int row = blockIdx.x;
+    const float* src = p.scores + (int64_t)row * p.n;
+    if (SMEM) {
+        for (int j = threadIdx.x; j < p.n; j += kTkThreads) skeys[j] = order_key(src[j]);
+    }
+    select_row<SMEM>(sh, skeys, src, p.n, p.k, p.prev != nullptr ? p.prev + (int64_t)row * p.k : nullptr,
+                     p.out + (int64_t)row * p.k, p.err);
+}
+
+template <typename K>
+cudaError_t allow_smem_keys(K kern)
+{
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device == dev) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemKeys * (int)sizeof(uint32_t));
+    if (e == cudaSuccess) configured_device = dev;
+    return e;
 }
 
 }  // namespace
@@ -234,15 +295,8 @@ cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s)
 {
     if (p.n <= kSmemKeys) {
         const size_t smem = (size_t)p.n * sizeof(uint32_t);
-        static int configured_device = -1;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (configured_device != dev) {
-            cudaError_t e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmemKeys * (int)sizeof(uint32_t));
-            if (e != cudaSuccess) return e;
-            configured_device = dev;
-        }
+        cudaError_t e = allow_smem_keys(topk_kernel<true>);
+        if (e != cudaSuccess) return e;
         return launch_kernel(topk_kernel<true>, dim3(p.rows), dim3(kTkThreads), smem, s, pdl, 0u, p);
     }
     return launch_kernel(topk_kernel<false>, dim3(p.rows), dim3(kTkThreads), 0, s, pdl, 0u, p);
