@@ -598,6 +598,215 @@ def run_kernel_case(args):
         raise SystemExit(1)
 
 
+def run_kv_select(args):
+    """The FastKV-shaped workload (4 sequences of 32768 tokens, 32 layers, 32 q / 8 kv heads): per-layer
+    KV retention once (window scores of every layer, its top 2040 + the 8 window tokens, compaction of
+    every layer with its own set), then decode steps over the compacted caches (one token per sequence
+    per step, 32 dense decode calls over 2048 + t rows).  One JSON line; not the headline workload."""
+    import kv_cache_token_fx_gb300 as fx
+    from synth.workloads import KvSelect
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = KvSelect()
+    L, B, Hkv, Hq, T, win = w.n_layers, w.B, w.Hkv, w.Hq, w.T, w.window
+    K = torch.empty((L, B, Hkv, T, D), dtype=torch.bfloat16, device=dev)
+    V = torch.empty_like(K)
+    QW = torch.empty((L, B, Hq, win, D), dtype=torch.bfloat16, device=dev)
+    for l in range(L):
+        k, v = w.layer_kv_salient(l, device=dev)
+        K[l].copy_(k)
+        V[l].copy_(v)
+        QW[l].copy_(w.window_queries_at(l, device=dev))
+        del k, v
+    ln = torch.full((B,), T, dtype=torch.int32, device=dev)
+    cap, ncand = w.compact_cap, T - win
+    CK = torch.zeros((L, B, Hkv, cap, D), dtype=torch.bfloat16, device=dev)
+    CV = torch.zeros_like(CK)
+    clen = torch.zeros(B, dtype=torch.int32, device=dev)
+    ws = fx.Workspace(dev, fx.load_library().fx_retain_workspace_bytes(B, Hkv, Hq, win, T, ncand))
+    pdl = 0 if args.no_pdl else fx.FX_LAUNCH_PDL
+    retain = lambda: fx.fx_kv_retain_per_layer(K, V, ln, QW, w.k_select, ncand, ncand, CK, CV, clen,
+                                               q_pos0=ncand, ws=ws, flags=pdl)
+    retain()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    a.record()
+    for _ in range(reps):
+        retain()
+    b.record()
+    torch.cuda.synchronize()
+    retain_ms = a.elapsed_time(b) / reps
+    # algorithmic bytes: K rows of every layer for the scores (V is not read), the compaction's reads
+    # and writes of the kept rows
+    retain_bytes = L * B * Hkv * (T * 256 + w.keep * 512 * 2)
+    del K, V
+    # decode: step t appends its K/V row at position keep + t of every layer, then attends densely
+    for l in range(L):
+        ak, av = w.appended_kv(l, dev)
+        CK[l, :, :, w.keep:w.keep + w.decode_steps] = ak
+        CV[l, :, :, w.keep:w.keep + w.decode_steps] = av
+    n_steps = min(args.steps, w.decode_steps)
+    Qd = torch.stack([torch.stack([w.decode_query(t, l, dev) for l in range(L)]) for t in range(n_steps)])
+    lens = torch.tensor([[w.keep + t + 1] * B for t in range(n_steps)], dtype=torch.int32, device=dev)
+    O = torch.empty((L, B, Hq, 1, D), dtype=torch.float32, device=dev)
+    dws = fx.Workspace(dev, fx.fx_sparse_workspace_bytes(B, Hkv, Hq, 0, 0, cap))
+    fl = pdl | (0 if args.no_pdl else fx.FX_LAUNCH_INPUTS_READY)
+
+    def step(t):
+        for l in range(L):
+            fx.fx_sparse_gqa_decode(CK[l], CV[l], lens[t], Qd[t, l], None, 0, out=O[l], ws=dws, flags=fl)
+    step(0)
+    torch.cuda.synchronize()
+    graphs = []
+    s = torch.cuda.Stream(dev)
+    for t in range(n_steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step(t)
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    for t in range(max(args.warmup, 3)):
+        graphs[t % n_steps].replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        a.record()
+        for g in graphs:
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    bits = fx.fx_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits}")
+    # per decode call: K+V rows of (keep + t + 1) positions, q, out
+    dec_bytes = sum(L * (B * Hkv * (w.keep + t + 1) * ROW_BYTES + B * Hq * D * 6) for t in range(n_steps))
+    n_calls = L * n_steps
+    achieved = dec_bytes / (ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    line = {
+        "metric": "kv_select decode tokens/s (FastKV per-layer retention, then dense decode over the kept rows)",
+        "value": round(B * n_steps / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": n_steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms / n_steps, 4), "higher_is_better": True,
+        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": "kv_select: 4 sequences x 32768 tokens, 32 layers, 32 q / 8 kv heads, d 128; every "
+                               "layer keeps its own top 2040 by the last 8 positions' attention + the 8 window "
+                               "tokens; decode over 2048 + t kept rows",
+                   "timing": "per-step CUDA graphs of 32 decode calls, CUDA events"},
+        "roofline": {"kernel": "fx_sparse_gqa_decode (dense over the compacted cache)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "peak_source": peak_kind,
+                     "avg_launch_us": round(ms * 1e3 / n_calls, 3), "avg_bytes_per_launch": int(dec_bytes / n_calls)},
+        "retention": {"ms": round(retain_ms, 3), "algorithmic_bytes": int(retain_bytes),
+                      "gbs": round(retain_bytes / (retain_ms / 1e3) / 1e9, 1),
+                      "frac": round(retain_bytes / (retain_ms / 1e3) / 1e9 / peak, 4),
+                      "launches": L * 3 + 1, "kept_rows": int(clen[0])},
+        "clocks": sampler.summary(), "gpu_launches": n_calls,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_hpd_branch(args):
+    """The HPD-Parsing-shaped draft verification (512 branches sharing a 2304-token prefix, private
+    suffixes of U[0, 1024] tokens, 7 draft positions, 16 q / 8 kv heads, 28 layers): a step verifies
+    every branch's 7 draft tokens at every layer.  Dense: attention over the whole prefix; sparse: over
+    the 256 prefix tokens per (branch, KV head) chosen at the first layer by the branch's draft queries
+    (prefix scoring + top-k), then every layer.  Layer inputs (1.14 GB each) are cycled over 4 buffers.
+    One JSON line; not the headline workload."""
+    import kv_cache_token_fx_gb300 as fx
+    from synth.workloads import HpdBranch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = HpdBranch()
+    Br, Hkv, Hq, Mq, P, L = w.Br, w.Hkv, w.Hq, w.Mq, w.P, w.n_layers
+    NB = 4
+    bufs = [w.layer_inputs(l, device=dev) for l in range(NB)]
+    S = int(bufs[0]["off"][-1])
+    out = torch.empty((Br, Hq, Mq, D), dtype=torch.float32, device=dev)
+    ws = fx.Workspace(dev, max(fx.fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, P, w.max_suffix),
+                               fx.fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, w.kp, w.max_suffix),
+                               fx.fx_focal_workspace_bytes(Br, Hkv, Hq, Mq, P)))
+    plen = torch.full((Br,), P, dtype=torch.int32, device=dev)
+    pscores = torch.empty((Br, Hkv, P), dtype=torch.float32, device=dev)
+    pidx = torch.empty((Br, Hkv, w.kp), dtype=torch.int32, device=dev)
+    pdl = 0 if args.no_pdl else fx.FX_LAUNCH_PDL
+    ready = 0 if args.no_pdl else fx.FX_LAUNCH_INPUTS_READY
+
+    def dense_step():
+        for l in range(L):
+            d = bufs[l % NB]
+            fx.fx_shared_prefix_decode(d["pk"], d["pv"], d["sk"], d["sv"], d["off"], d["dk"], d["dv"], d["q"],
+                                       max_suffix=w.max_suffix, out=out, ws=ws, flags=pdl | ready)
+
+    def sparse_step():
+        d = bufs[0]
+        # every branch sees the same prefix rows (batch stride 0)
+        pk4 = d["pk"].unsqueeze(0).expand(Br, Hkv, P, D)
+        pv4 = d["pv"].unsqueeze(0).expand(Br, Hkv, P, D)
+        fx.fx_focal_attn_scores(pk4, pv4, plen, d["q"], want_out=False, scores=pscores, ws=ws, flags=pdl | ready)
+        fx.fx_topk_select(pscores, w.kp, out=pidx, flags=pdl)
+        for l in range(L):
+            d = bufs[l % NB]
+            fx.fx_shared_prefix_decode(d["pk"], d["pv"], d["sk"], d["sv"], d["off"], d["dk"], d["dv"], d["q"],
+                                       max_suffix=w.max_suffix, prefix_idx=pidx, out=out, ws=ws,
+                                       flags=pdl | (ready if l > 0 else 0))
+
+    res = {}
+    for name, fn in (("dense", dense_step), ("sparse", sparse_step)):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        for _ in range(max(args.warmup, 3)):
+            g.replay()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 16))
+        sampler = ClockSampler(0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with sampler:
+            a.record()
+            for _ in range(n):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+        res[name] = (a.elapsed_time(b) / n, n, sampler.summary())
+    bits = fx.fx_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits}")
+    # algorithmic bytes per dense layer call: prefix K/V once, every branch's suffix and draft rows, q, out
+    row = 2 * D * 2
+    dense_bytes = Hkv * P * row + Hkv * S * row + Br * Mq * Hkv * row + Br * Hq * Mq * D * (2 + 4)
+    sparse_bytes = Hkv * P * row + Hkv * S * row + Br * Mq * Hkv * row + Br * Hq * Mq * D * (2 + 4)
+    peak, peak_kind = measured_hbm_peak()
+    ms_d, n_d, clk = res["dense"]
+    ms_s, n_s, _ = res["sparse"]
+    tokens = Br * Mq
+    line = {
+        "metric": "hpd_branch verified draft tokens/s (shared-prefix draft verification, dense prefix)",
+        "value": round(tokens / (ms_d / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": n_d,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_d, 4), "higher_is_better": True,
+        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": "hpd_branch: 512 branches, shared prefix 2048 + 256 tokens, suffix U[0,1024] tokens, "
+                               "7 draft positions, 16 q / 8 kv heads, d 128, 28 layers (inputs cycled over 4 buffers)",
+                   "suffix_rows": S, "timing": "one CUDA graph per step, CUDA events"},
+        "roofline": {"kernel": "fx_shared_prefix_decode (dense prefix)", "bound": "hbm",
+                     "achieved": round(dense_bytes * L / (ms_d / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dense_bytes * L / (ms_d / 1e3) / 1e9 / peak, 4), "traffic": None,
+                     "peak_source": peak_kind, "avg_launch_us": round(ms_d * 1e3 / L, 3),
+                     "avg_bytes_per_launch": int(dense_bytes)},
+        "sparse": {"value": round(tokens / (ms_s / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms_s, 4),
+                   "note": "prefix scoring + top-256 at the first layer, then 28 sparse-prefix layers",
+                   "layer_bytes": int(sparse_bytes)},
+        "clocks": clk, "gpu_launches": L * n_d,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,9 +821,18 @@ def main():
                     help="run a small fixed case of one kernel (for profiler captures) instead of the bench")
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--workload", choices=["ocr_decode", "kv_select", "hpd_branch"], default="ocr_decode",
+                    help="ocr_decode: the headline workload; kv_select: FastKV per-layer retention + decode; "
+                         "hpd_branch: shared-prefix draft verification")
     args = ap.parse_args()
     if args.kernel_case:
         run_kernel_case(args)
+        return
+    if args.workload == "kv_select" and args.impl == "fx":
+        run_kv_select(args)
+        return
+    if args.workload == "hpd_branch" and args.impl == "fx":
+        run_hpd_branch(args)
         return
     if args.warmup < 3 and args.impl == "fx":
         args.warmup = 3

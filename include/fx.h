@@ -194,7 +194,7 @@ FX_API fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, in
  * contiguous cache, once, after prefill.  [FastKV] 2.B.
  *
  * For every layer l < n_layers, b and h, destination row r of
- *   S = idx[b, h, 0..k) followed by tail_lo .. len[b]-1
+ *   S = idx_l[b, h, 0..k) followed by tail_lo .. len[b]-1,   idx_l = idx + l*idx_stride_layer
  * receives source row S[r] (K and V, bit-exact copies), so the kept rows stay in the order given
  * (ascending when idx is ascending and below tail_lo).  dst->len[b] = k + max(0, len[b] - tail_lo).
  * Layer l of the source starts at element offset l*src_stride_layer from src->k / src->v, layer l of
@@ -202,12 +202,39 @@ FX_API fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, in
  * not touched.  An idx entry outside [0, len[b]) sets FX_DEVERR_INDEX and its row is not written; a
  * new length above dst->Tcap sets FX_DEVERR_CAPACITY and only dst->Tcap rows are written (dst->len
  * is then clamped to dst->Tcap).
- *   idx [B, Hkv, k] int32 (NULL when k == 0).  src and dst must agree on B, Hkv and d.
+ *   idx [B, Hkv, k] int32 per layer (NULL when k == 0); idx_stride_layer (elements) = 0: one set
+ *   for every layer (a selection made at one layer), B*Hkv*k for a [n_layers, B, Hkv, k] array of
+ *   per-layer sets (FastKV's per-layer KV retention).  src and dst must agree on B, Hkv and d.
  * No workspace.
  */
-FX_API fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx, int k,
-                        int tail_lo, const fx_kv_out_desc* dst, int64_t dst_stride_layer,
-                        int n_layers, unsigned flags, void* stream);
+FX_API fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx,
+                        int64_t idx_stride_layer, int k, int tail_lo, const fx_kv_out_desc* dst,
+                        int64_t dst_stride_layer, int n_layers, unsigned flags, void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* fx_kv_retain_per_layer -- FastKV decoupled KV retention with its own selection at every layer.
+ * [FastKV] 2.A (saliency: attention of a window of recent queries to all context tokens) and 2.B
+ * (KV retention rate: how many entries each layer keeps for decoding).
+ *
+ * For every layer l < n_layers (layer l of the cache at element offset l*src_stride_layer from
+ * kv->k / kv->v; all layers share kv->len):
+ *   scores_l = fx_focal_attn_scores(layer l, window queries q_l, q_pos0, scale, candidates [0, cand_hi))
+ *              (scores only: no output rows, V is not read)
+ *   idx_l    = fx_topk_select(scores_l, keep_k)  -> idx_out + l*B*Hkv*keep_k
+ * then fx_kv_compact of all n_layers layers with the per-layer sets idx_l followed by the tail
+ * [tail_lo, len[b]) (the window), into dst (layer l at l*dst_stride_layer; dst->len = new lengths).
+ *   q        [n_layers, B, Hq, Mq, 128] bf16 (contiguous): layer l's window queries
+ *   idx_out  [n_layers, B, Hkv, keep_k] int32, written (ascending per row)
+ *   1 <= keep_k <= cand_hi <= Tcap.  Results equal those of the individual calls.
+ * Workspace: fx_retain_workspace_bytes(B, Hkv, Hq, Mq, Tcap, cand_hi) bytes (one layer's focal
+ * scratch and scores, reused layer after layer).
+ */
+FX_API size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi);
+FX_API fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer, int n_layers,
+                                 const fx_bf16* q, int Hq, int Mq, int q_pos0, float scale, int cand_hi,
+                                 int keep_k, int tail_lo, int32_t* idx_out, const fx_kv_out_desc* dst,
+                                 int64_t dst_stride_layer, void* ws, size_t ws_bytes, unsigned flags,
+                                 void* stream);
 
 /* ------------------------------------------------------------------------------------------- */
 /* fx_shared_prefix_decode -- parallel draft verification over a shared prefix.  [HPD] parts 2

@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "FxError", "load_library", "library_path", "Workspace", "fx_focal_attn_scores", "fx_topk_select",
-    "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode", "fx_device_errors",
+    "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode", "fx_device_errors",
     "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
     "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
     "FX_LAUNCH_PDL", "FX_LAUNCH_INPUTS_READY",
@@ -94,14 +94,19 @@ def load_library():
         lib.fx_sparse_workspace_bytes.restype = c_size
         lib.fx_sparse_gqa_decode.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_vp, c_int, c_int, c_float,
                                              c_vp, c_vp, c_size, c_uint, c_vp]
-        lib.fx_kv_compact.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_vp, c_int, c_int, ctypes.POINTER(KVOutDesc),
-                                      c_i64, c_int, c_uint, c_vp]
+        lib.fx_kv_compact.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_vp, c_i64, c_int, c_int,
+                                      ctypes.POINTER(KVOutDesc), c_i64, c_int, c_uint, c_vp]
+        lib.fx_retain_workspace_bytes.argtypes = [c_int] * 6
+        lib.fx_retain_workspace_bytes.restype = c_size
+        lib.fx_kv_retain_per_layer.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_int, c_vp, c_int, c_int, c_int,
+                                               c_float, c_int, c_int, c_int, c_vp, ctypes.POINTER(KVOutDesc), c_i64,
+                                               c_vp, c_size, ctypes.c_uint, c_vp]
         lib.fx_shared_prefix_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_shared_prefix_workspace_bytes.restype = c_size
         lib.fx_shared_prefix_decode.argtypes = [ctypes.POINTER(PrefixDesc), ctypes.POINTER(BranchDesc), c_vp, c_int,
                                                 c_vp, c_int, c_float, c_vp, c_vp, c_size, c_uint, c_vp]
         for name in ("fx_device_errors", "fx_workspace_init", "fx_focal_attn_scores", "fx_topk_select",
-                     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_shared_prefix_decode"):
+                     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode"):
             getattr(lib, name).restype = c_int
         _lib = lib
         return lib
@@ -266,7 +271,9 @@ def fx_sparse_gqa_decode(k, v, length, q, idx, tail_lo: int, *, scale=None, out=
 
 
 def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, stream=None, flags: int = 0):
-    """Compact the retained rows of one layer ([B, Hkv, T, 128]) or of L layers ([L, B, Hkv, T, 128])."""
+    """Compact the retained rows of one layer ([B, Hkv, T, 128]) or of L layers ([L, B, Hkv, T, 128]).
+
+    idx: [B, Hkv, k] (one set for every layer) or, for L layers, [L, B, Hkv, k] (a set per layer)."""
     lib = load_library()
     if k.dim() == 5:
         n_layers = k.shape[0]
@@ -281,16 +288,55 @@ def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, str
         n_layers, s_layer, d_layer = 1, 0, 0
         src = _kv_desc(k, v, length)
         dst = _kv_desc(dst_k, dst_v, dst_len)
-    kk = 0
+    kk, i_layer = 0, 0
     if idx is not None:
         _need_cuda(idx, "idx", torch.int32)
         if not idx.is_contiguous():
-            raise FxError(FX_ERR_INVALID_ARG, "idx must be contiguous [B, Hkv, k]")
+            raise FxError(FX_ERR_INVALID_ARG, "idx must be contiguous [B, Hkv, k] or [L, B, Hkv, k]")
         kk = idx.shape[-1]
+        if idx.dim() == 4:
+            if k.dim() != 5 or idx.shape[0] != n_layers:
+                raise FxError(FX_ERR_INVALID_ARG, "a per-layer idx [L, B, Hkv, k] needs L-layer caches")
+            i_layer = idx.stride(0)
     dst_out = KVOutDesc(*[getattr(dst, f) for f, _ in KVDesc._fields_])
-    _check(lib.fx_kv_compact(ctypes.byref(src), s_layer, _ptr(idx) if kk else None, kk, int(tail_lo),
+    _check(lib.fx_kv_compact(ctypes.byref(src), s_layer, _ptr(idx) if kk else None, i_layer, kk, int(tail_lo),
                              ctypes.byref(dst_out), d_layer, n_layers, int(flags), _stream(stream)))
     return dst_k, dst_v, dst_len
+
+
+def fx_kv_retain_per_layer(k, v, length, q, keep_k: int, cand_hi: int, tail_lo: int, dst_k, dst_v, dst_len, *,
+                           q_pos0: int = -1, scale=None, idx_out=None, ws=None, stream=None, flags: int = 0):
+    """FastKV retention with a selection per layer: window scores of every layer, its top keep_k, and
+    the compaction of every layer with its own set plus the tail [tail_lo, len).
+
+    k, v [L, B, Hkv, T, 128]; q [L, B, Hq, Mq, 128] (each layer's window queries); dst_k, dst_v
+    [L, B, Hkv, cap, 128]; dst_len int32 [B].  Returns idx [L, B, Hkv, keep_k] (ascending rows)."""
+    lib = load_library()
+    if k.dim() != 5 or dst_k.dim() != 5 or q.dim() != 5 or not (k.shape[0] == dst_k.shape[0] == q.shape[0]):
+        raise FxError(FX_ERR_INVALID_ARG, "k, v, dst and q need a leading layer dimension of the same size")
+    L, B, Hkv, T, d = k.shape
+    _need_cuda(q, "q", torch.bfloat16)
+    if not q.is_contiguous():
+        raise FxError(FX_ERR_INVALID_ARG, "q must be a contiguous [L, B, Hq, Mq, 128] tensor")
+    s_layer, d_layer = k.stride(0), dst_k.stride(0)
+    if v.stride(0) != s_layer or dst_v.stride(0) != d_layer:
+        raise FxError(FX_ERR_INVALID_ARG, "k/v layer strides must match")
+    src = _kv_desc(k[0], v[0], length)
+    dst = _kv_desc(dst_k[0], dst_v[0], dst_len)
+    dst_out = KVOutDesc(*[getattr(dst, f) for f, _ in KVDesc._fields_])
+    _, _, Hq, Mq, _ = q.shape
+    if idx_out is None:
+        idx_out = torch.empty((L, B, Hkv, int(keep_k)), dtype=torch.int32, device=k.device)
+    _need_cuda(idx_out, "idx_out", torch.int32)
+    if idx_out.numel() != L * B * Hkv * int(keep_k) or not idx_out.is_contiguous():
+        raise FxError(FX_ERR_INVALID_ARG, "idx_out must be a contiguous [L, B, Hkv, keep_k] int32 tensor")
+    nbytes = lib.fx_retain_workspace_bytes(B, Hkv, Hq, Mq, T, int(cand_hi))
+    buf = _workspace(ws, nbytes, k.device, stream)
+    sc = _default_scale(d) if scale is None else float(scale)
+    _check(lib.fx_kv_retain_per_layer(ctypes.byref(src), s_layer, L, _ptr(q), Hq, Mq, int(q_pos0), sc, int(cand_hi),
+                                      int(keep_k), int(tail_lo), _ptr(idx_out), ctypes.byref(dst_out), d_layer,
+                                      _ptr(buf), buf.numel(), int(flags), _stream(stream)))
+    return idx_out
 
 
 def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, prefix_idx=None, scale=None,

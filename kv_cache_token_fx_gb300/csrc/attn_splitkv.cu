@@ -345,6 +345,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     // commit group per sub-tile (empty past the end), so "all but kWarpStages-1 groups done" always
     // means "the oldest sub-tile has landed".  No CTA-wide barrier is needed inside the loop.
     unsigned char* wbuf = sKV + (size_t)warp * kWarpBytes;
+    // a focal call that only scores (no output rows) needs no V rows and no P V products
+    const bool need_v = !(MODE == kModeFocal && p.no_v);
     auto issue = [&](int j, int mytok) {
         if (j < nsub) {
             const int c16 = lane & 15;
@@ -368,10 +370,10 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 unsigned char* dv = dk + kSub * kPitch;
                 if ((vmask >> r) & 1u) {
                     cp_async16(smem_addr(dk), kp + 8 * c16);
-                    cp_async16(smem_addr(dv), vp + 8 * c16);
+                    if (need_v) cp_async16(smem_addr(dv), vp + 8 * c16);
                 } else {
                     *reinterpret_cast<uint4*>(dk) = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
+                    if (need_v) *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             if (lane == 0) s_vmask[warp][j % kWarpStages] = vmask;
@@ -529,31 +531,33 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             }
             // P^T as B fragments: (keys 2t4.., row g) = the transpose of the (key g, rows 2t4..) layout;
             // P = hi + lo in bf16
-            uint32_t h01, l01, h23, l23;
-            split_bf16(x[0], x[1], h01, l01);
-            split_bf16(x[2], x[3], h23, l23);
-            const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
-            const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
-            // O^T += V^T P^T: A fragments of V^T straight from the row-major V tile with ldmatrix.trans
-            const int vrow = (lane & 7) + 8 * (lane >> 4);
-            const int vcol = 8 * ((lane >> 3) & 1);
+            if (need_v) {
+                uint32_t h01, l01, h23, l23;
+                split_bf16(x[0], x[1], h01, l01);
+                split_bf16(x[2], x[3], h23, l23);
+                const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
+                const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
+                // O^T += V^T P^T: A fragments of V^T straight from the row-major V tile with ldmatrix.trans
+                const int vrow = (lane & 7) + 8 * (lane >> 4);
+                const int vcol = 8 * ((lane >> 3) & 1);
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * mt + vcol) * 2), a0, a1, a2, a3);
-                mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-                mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+                for (int mt = 0; mt < 8; ++mt) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * mt + vcol) * 2), a0, a1, a2, a3);
+                    mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+                    mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+                }
             }
         } else {
             // S = Q K^T for this warp's 16 keys (2 n-tiles of 8 keys)
             float s[2][4];
-    #pragma unroll
+#pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
                 const int krow = 8 * nt + (lane & 7);
                 const int kcol = 8 * (lane >> 3);   // matrices: dims +0, +8, +16, +24 of a 32-dim slice
-    #pragma unroll
+#pragma unroll
                 for (int kp = 0; kp < 4; ++kp) {     // pairs of k-steps
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(smem_addr(sk + krow * kPitch + (32 * kp + kcol) * 2), b0, b1, b2, b3);
@@ -564,9 +568,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 
             // scale to base 2, mask, store logits (focal), online softmax
             float mx[2] = {-INFINITY, -INFINITY};
-    #pragma unroll
+#pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int hr = e >> 1;
                     const int pos = base + 8 * nt + 2 * t4 + (e & 1);
@@ -577,12 +581,12 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 }
             }
             if (MODE == kModeFocal && p.logits != nullptr) {
-    #pragma unroll
+#pragma unroll
                 for (int hr = 0; hr < 2; ++hr) {
                     const int row = r0 + g + 8 * hr;
                     if (row < p.R) {
                         float* lrow = p.logits + (int64_t)(bh * p.R + row) * p.Tcap;
-    #pragma unroll
+#pragma unroll
                         for (int nt = 0; nt < 2; ++nt) {
                             const int pos = base + 8 * nt + 2 * t4;
                             if (pos < we) lrow[pos] = s[nt][2 * hr];
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 }
             }
             float alpha[2], ms[2];
-    #pragma unroll
+#pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 1));
                 mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 2));
@@ -602,16 +606,16 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 m_run[hr] = mn;
                 l_run[hr] *= alpha[hr];
             }
-    #pragma unroll
+#pragma unroll
             for (int n = 0; n < 16; ++n) {
                 o[n][0] *= alpha[0];
                 o[n][1] *= alpha[0];
                 o[n][2] *= alpha[1];
                 o[n][3] *= alpha[1];
             }
-    #pragma unroll
+#pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float pe = fast_exp2(s[nt][e] - ms[e >> 1]);
                     s[nt][e] = pe;
@@ -620,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             }
 
             // O += P V over this warp's 16 keys (one k-step); P = hi + lo in bf16
-            {
+            if (need_v) {
                 uint32_t ph[4], pl[4];
                 split_bf16(s[0][0], s[0][1], ph[0], pl[0]);
                 split_bf16(s[0][2], s[0][3], ph[1], pl[1]);
@@ -628,7 +632,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 split_bf16(s[1][2], s[1][3], ph[3], pl[3]);
                 const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
                 const int vcol = 8 * (lane >> 4);
-    #pragma unroll
+#pragma unroll
                 for (int np2 = 0; np2 < 8; ++np2) {   // pairs of 8-dim n-tiles
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * np2 + vcol) * 2), b0, b1, b2, b3);

@@ -1,5 +1,6 @@
 // One-shot KV compaction for sm_103a (FastKV, 2.B Decoupled KV Retention): destination row r of
-// (layer, b, h) receives source row idx[b, h, r] for r < k, then the tail rows tail_lo .. len-1.
+// (layer, b, h) receives source row idx_layer[b, h, r] for r < k (one set shared by all layers, or one
+// per layer), then the tail rows tail_lo .. len-1.
 //
 // Pure data movement: 16 threads move one 256-byte row of K and one of V with 16-byte vector loads
 // and stores; each thread handles kRowsPerThread rows so several loads are in flight before the
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams
     const uint16_t* sv = p.sv + layer * p.s_layer + b * p.sb + h * p.sh;
     uint16_t* dk = p.dk + layer * p.d_layer + b * p.db + h * p.dh;
     uint16_t* dv = p.dv + layer * p.d_layer + b * p.db + h * p.dh;
-    const int32_t* irow = p.idx ? p.idx + ((int64_t)b * p.Hkv + h) * p.kk : nullptr;
+    const int32_t* irow = p.idx ? p.idx + layer * p.idx_layer + ((int64_t)b * p.Hkv + h) * p.kk : nullptr;
 
     const int rbase = blockIdx.x * (kRowsPerIter * kRowsPerThread);
     uint4 kv[kRowsPerThread], vv[kRowsPerThread];

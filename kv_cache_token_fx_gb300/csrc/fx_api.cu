@@ -13,7 +13,7 @@ using namespace fx;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;
 
@@ -283,6 +283,7 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     p.part_l = reinterpret_cast<float*>(w + L.part_l);
     p.part_o = reinterpret_cast<float*>(w + L.part_o);
     p.logits = scores ? reinterpret_cast<float*>(w + L.logits) : nullptr;
+    p.no_v = out == nullptr ? 1 : 0;
     p.err = ds->err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
@@ -414,9 +415,9 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
 }
 
 // ---------------------------------------------------------------------------------------------
-fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx, int k,
-                        int tail_lo, const fx_kv_out_desc* dst, int64_t dst_stride_layer,
-                        int n_layers, unsigned flags, void* stream)
+fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const int32_t* idx,
+                        int64_t idx_stride_layer, int k, int tail_lo, const fx_kv_out_desc* dst,
+                        int64_t dst_stride_layer, int n_layers, unsigned flags, void* stream)
 {
     fx_status st = check_kv(src, "src");
     if (st != FX_OK) return st;
@@ -430,6 +431,7 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
     if (n_layers < 1) return fail(FX_ERR_INVALID_ARG, "n_layers must be >= 1");
     if (k < 0 || (k > 0 && !idx)) return fail(FX_ERR_INVALID_ARG, "need k >= 0 and idx when k > 0");
     if (tail_lo < 0) return fail(FX_ERR_INVALID_ARG, "tail_lo must be >= 0");
+    if (idx_stride_layer < 0) return fail(FX_ERR_INVALID_ARG, "idx_stride_layer must be >= 0");
     if (!row_stride_ok(src_stride_layer) || !row_stride_ok(dst_stride_layer))
         return fail(FX_ERR_INVALID_ARG, "layer strides must be non-negative multiples of 8 elements");
     if ((int64_t)src->B * n_layers > 65535 || src->Hkv > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
@@ -448,6 +450,7 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
     p.Hkv = src->Hkv;
     p.Tcap = src->Tcap;
     p.idx = k > 0 ? idx : nullptr;
+    p.idx_layer = idx_stride_layer;
     p.kk = k;
     p.tail_lo = tail_lo;
     p.dk = dst->k;
@@ -465,6 +468,52 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
     cudaError_t e = launch_compact(p, (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "compaction launch");
     return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi)
+{
+    const size_t f = fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap);
+    if (f == 0 || cand_hi < 1) return 0;
+    return round_up(f) + round_up((size_t)B * Hkv * cand_hi * sizeof(float));
+}
+
+fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer, int n_layers, const fx_bf16* q,
+                                 int Hq, int Mq, int q_pos0, float scale, int cand_hi, int keep_k, int tail_lo,
+                                 int32_t* idx_out, const fx_kv_out_desc* dst, int64_t dst_stride_layer, void* ws,
+                                 size_t ws_bytes, unsigned flags, void* stream)
+{
+    fx_status st = check_kv(kv, "kv");
+    if (st != FX_OK) return st;
+    if ((st = check_flags(flags)) != FX_OK) return st;
+    if (n_layers < 1) return fail(FX_ERR_INVALID_ARG, "n_layers must be >= 1");
+    if (!q || !idx_out) return fail(FX_ERR_INVALID_ARG, "q and idx_out must be non-NULL");
+    if (cand_hi < 1 || cand_hi > kv->Tcap) return fail(FX_ERR_INVALID_ARG, "need 1 <= cand_hi <= Tcap");
+    if (keep_k < 1 || keep_k > cand_hi) return fail(FX_ERR_INVALID_ARG, "need 1 <= keep_k <= cand_hi");
+    if (!row_stride_ok(src_stride_layer)) return fail(FX_ERR_INVALID_ARG, "src_stride_layer must be a multiple of 8");
+    const size_t need = fx_retain_workspace_bytes(kv->B, kv->Hkv, Hq, Mq, kv->Tcap, cand_hi);
+    if (need == 0) return fail(FX_ERR_INVALID_ARG, "bad shape");
+    if ((st = check_ws(ws, ws_bytes, need)) != FX_OK) return st;
+    const size_t fbytes = round_up(fx_focal_workspace_bytes(kv->B, kv->Hkv, Hq, Mq, kv->Tcap));
+    float* scores = reinterpret_cast<float*>(static_cast<char*>(ws) + fbytes);
+    const int rows = kv->B * kv->Hkv;
+    const size_t q_layer = (size_t)kv->B * Hq * Mq * kHeadDim;
+    // Every call after the first runs as a programmatic dependent launch when the caller asked for
+    // one; the later focal calls read K and lengths that were written before the first call.
+    const unsigned pdl = flags & FX_LAUNCH_PDL;
+    for (int l = 0; l < n_layers; ++l) {
+        fx_kv_desc kl = *kv;
+        kl.k = kv->k + (int64_t)l * src_stride_layer;
+        kl.v = kv->v + (int64_t)l * src_stride_layer;
+        const unsigned ff = l == 0 ? flags : (pdl ? (FX_LAUNCH_PDL | FX_LAUNCH_INPUTS_READY) : 0u);
+        st = fx_focal_attn_scores(&kl, q + (size_t)l * q_layer, Hq, Mq, q_pos0, scale, 0, cand_hi, nullptr, scores, ws,
+                                  fbytes, ff, stream);
+        if (st != FX_OK) return st;
+        st = fx_topk_select(scores, rows, cand_hi, keep_k, nullptr, idx_out + (size_t)l * rows * keep_k, pdl, stream);
+        if (st != FX_OK) return st;
+    }
+    return fx_kv_compact(kv, src_stride_layer, idx_out, (int64_t)rows * keep_k, keep_k, tail_lo, dst,
+                         dst_stride_layer, n_layers, pdl, stream);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -75,6 +75,7 @@ struct AttnParams {
     int nsplit, split_len, nrg, stages;
     int rb;         // query rows per CTA (8 or 16)
     int prefetch;   // lengths / indices / K-V rows may be read before the preceding kernel finishes
+    int no_v;       // focal: scores only (no output rows), so V is neither read nor multiplied
     // outputs / scratch
     float* part_m;        // [B*Hkv*R*nsplit]
     float* part_l;        // [B*Hkv*R*nsplit]
@@ -113,6 +114,7 @@ struct CompactParams {
     int64_t sb, sh, st, s_layer;
     int B, Hkv, Tcap;
     const int32_t* idx;
+    int64_t idx_layer;   // element offset between the index sets of consecutive layers (0: shared)
     int kk, tail_lo;
     uint16_t* dk;
     uint16_t* dv;

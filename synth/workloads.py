@@ -184,6 +184,38 @@ class KvSelect:
     def planted_positions(self, b, h):
         return distinct_positions(self.seed, stream_id(_POS, b, h), self.T - self.window, self.n_planted)
 
+    # Per-layer retention (each layer selects its own tokens): every layer gets its own window queries
+    # and its own planted high-affinity tokens; at the switch layer both equal the ones above.
+    def window_queries_at(self, layer, device="cpu"):
+        """q of the last `window` prompt positions at `layer`: [B, Hq, window, 128]."""
+        return normal_bf16(self.seed, stream_id(_Q, layer, 999999), (self.B, self.Hq, self.window, D), device=device)
+
+    def planted_positions_at(self, layer, b, h):
+        if layer == self.switch_layer:
+            return self.planted_positions(b, h)
+        return distinct_positions(self.seed, stream_id(_POS, b, h, layer), self.T - self.window, self.n_planted)
+
+    def layer_kv_salient(self, layer, device="cpu"):
+        """Layer `layer` with its own planted tokens (equals layer_kv at the switch layer)."""
+        shape = (self.B, self.Hkv, self.T, D)
+        k = normal_bf16(self.seed, stream_id(_K, layer), shape, device=device)
+        v = normal_bf16(self.seed, stream_id(_V, layer), shape, device=device)
+        aff = self._affinity(self.window_queries_at(layer, device))
+        for b in range(self.B):
+            for h in range(self.Hkv):
+                pos = self.planted_positions_at(layer, b, h).to(device)
+                k[b, h, pos] = _add_f32(k[b, h, pos], aff[b, h][None])
+        return k, v
+
+    def layer_kv_salient_rows(self, layer, b, h):
+        shape = (self.B, self.Hkv, self.T, D)
+        k = _rows_of(self.seed, stream_id(_K, layer), shape, b, h, "cpu").clone()
+        v = _rows_of(self.seed, stream_id(_V, layer), shape, b, h, "cpu")
+        aff = self._affinity(self.window_queries_at(layer, "cpu"))
+        pos = self.planted_positions_at(layer, b, h)
+        k[pos] = _add_f32(k[pos], aff[b, h][None])
+        return k, v
+
     def _affinity(self, qw):
         """fp32 [B, Hkv, 128]: alpha * (sum of the group's window query rows, added in a fixed order)."""
         G = self.Hq // self.Hkv

@@ -41,7 +41,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_argument_checks_without_gpu(lib):
     lib.fx_last_error.restype = ctypes.c_char_p
     lib.fx_abi_version.restype = ctypes.c_int
-    assert lib.fx_abi_version() == 2
+    assert lib.fx_abi_version() == 3
     lib.fx_topk_select.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_uint, ctypes.c_void_p]
     assert lib.fx_topk_select(None, 1, 4, 2, None, None, 0, None) == 1
@@ -54,6 +54,21 @@ def test_host_argument_checks_without_gpu(lib):
     lib.fx_focal_attn_scores.restype = ctypes.c_int
     assert lib.fx_focal_attn_scores(None, None, 1, 1, -1, ctypes.c_float(1.0), 0, 0, None, None, None,
                                     ctypes.c_size_t(0), ctypes.c_uint(0), None) == 1
+    # per-layer retention: argument checks before any device work
+    from kv_cache_token_fx_gb300 import KVDesc, KVOutDesc
+    kv = KVDesc(256, 512, 768, 2 * 600 * 128, 600 * 128, 128, 2, 2, 600, 128)
+    dst = KVOutDesc(1024, 1280, 1536, 2 * 64 * 128, 64 * 128, 128, 2, 2, 64, 128)
+    lib.fx_kv_retain_per_layer.restype = ctypes.c_int
+    lib.fx_retain_workspace_bytes.restype = ctypes.c_size_t
+    retain = lambda n_layers, cand_hi, keep: lib.fx_kv_retain_per_layer(
+        ctypes.byref(kv), ctypes.c_int64(2 * 2 * 600 * 128), n_layers, ctypes.c_void_p(256), 4, 4, 596,
+        ctypes.c_float(1.0), cand_hi, keep, 596, ctypes.c_void_p(256), ctypes.byref(dst), ctypes.c_int64(0), None,
+        ctypes.c_size_t(0), ctypes.c_uint(0), None)
+    assert retain(0, 596, 37) == 1 and b"n_layers" in lib.fx_last_error()
+    assert retain(3, 601, 37) == 1 and b"cand_hi" in lib.fx_last_error()
+    assert retain(3, 596, 597) == 1 and b"keep_k" in lib.fx_last_error()
+    assert retain(3, 596, 37) == 3    # no workspace
+    assert lib.fx_retain_workspace_bytes(2, 2, 4, 4, 600, 596) > 2 * 2 * 596 * 4
     lib.fx_sparse_workspace_bytes.restype = ctypes.c_size_t
     assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) > 0
     assert lib.fx_sparse_workspace_bytes(0, 8, 16, 205, 4096, 4864) == 0

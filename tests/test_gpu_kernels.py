@@ -256,6 +256,61 @@ def test_compaction_is_bit_exact(fx, n_layers, kk, tail_lo):
             assert torch.all(dk[l, b, :, n:].float() == 7.0)   # rows past the new length untouched
 
 
+def test_compaction_with_per_layer_sets(fx):
+    """A [L, B, Hkv, k] index array gives every layer its own set."""
+    n_layers, B, Hkv, kk, tail_lo = 3, 2, 2, 25, 300
+    T = tail_lo + 40
+    ks = torch.stack([rnd((B, Hkv, T, D), 150 + l, 1) for l in range(n_layers)])
+    vs = torch.stack([rnd((B, Hkv, T, D), 150 + l, 2) for l in range(n_layers)])
+    length = torch.tensor([T, tail_lo + 7], dtype=torch.int32)
+    idx = torch.stack([_sorted_subsets(B, Hkv, tail_lo, kk, 20 + l) for l in range(n_layers)])
+    cap = kk + 64
+    dk = torch.zeros((n_layers, B, Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
+    dv = torch.zeros_like(dk)
+    dl = torch.zeros(B, dtype=torch.int32, device="cuda")
+    fx.fx_kv_compact(dev(ks), dev(vs), dev(length), dev(idx), tail_lo, dk, dv, dl)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    for l in range(n_layers):
+        rk, rv, rl = oracle.kv_compact(ks[l], vs[l], length, idx[l], tail_lo, cap)
+        assert torch.equal(dl.cpu(), rl)
+        for b in range(B):
+            n = int(rl[b])
+            assert torch.equal(dk[l, b, :, :n].cpu().view(torch.int16), rk[b, :, :n].view(torch.int16))
+            assert torch.equal(dv[l, b, :, :n].cpu().view(torch.int16), rv[b, :, :n].view(torch.int16))
+
+
+def test_per_layer_retention_matches_oracle(fx):
+    """fx_kv_retain_per_layer: each layer's window scores (causal window of the last Mq positions),
+    its own top-k, and the compaction of every layer with its own set plus the window tail."""
+    n_layers, B, Hkv, G, Mq, T, keep = 3, 2, 2, 2, 4, 600, 37
+    cand = T - Mq
+    ks = torch.stack([rnd((B, Hkv, T, D), 160 + l, 1) for l in range(n_layers)])
+    vs = torch.stack([rnd((B, Hkv, T, D), 160 + l, 2) for l in range(n_layers)])
+    qs = torch.stack([rnd((B, Hkv * G, Mq, D), 160 + l, 3) for l in range(n_layers)])
+    length = torch.tensor([T, 500], dtype=torch.int32)
+    cap = keep + Mq + 8
+    dk = torch.zeros((n_layers, B, Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
+    dv = torch.zeros_like(dk)
+    dl = torch.zeros(B, dtype=torch.int32, device="cuda")
+    idx = fx.fx_kv_retain_per_layer(dev(ks), dev(vs), dev(length), dev(qs), keep, cand, cand, dk, dv, dl,
+                                    q_pos0=cand)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert tuple(idx.shape) == (n_layers, B, Hkv, keep)
+    for l in range(n_layers):
+        _, sc = oracle.focal(ks[l], vs[l], length, qs[l], q_pos0=cand, cand=(0, cand), want_out=False)
+        ref_idx = oracle.topk(sc, keep)
+        pu.check_index_sets(idx[l], ref_idx, sc, keep)
+        # the compaction, checked on the sets the GPU chose
+        rk, rv, rl = oracle.kv_compact(ks[l], vs[l], length, idx[l].cpu(), cand, cap)
+        assert torch.equal(dl.cpu(), rl)
+        for b in range(B):
+            n = int(rl[b])
+            assert torch.equal(dk[l, b, :, :n].cpu().view(torch.int16), rk[b, :, :n].view(torch.int16))
+            assert torch.equal(dv[l, b, :, :n].cpu().view(torch.int16), rv[b, :, :n].view(torch.int16))
+
+
 def test_compaction_capacity_is_flagged(fx):
     B, Hkv, T = 1, 1, 50
     k, v = kv_case(B, Hkv, T, 60)
