@@ -244,7 +244,9 @@ class OcrDecodeRun:
                 fx.fx_focal_attn_scores(self.K[l], self.V[l], ln, self.Q[t, l], cand=(0, w.n_vis), out=self.O[l],
                                         scores=self.scores, ws=self.ws, flags=pdl | ready)
                 prev = self.sets[l][1 - p] if t > 0 else None
-                fx.fx_topk_select(self.scores, w.k_keep, prev=prev, out=self.sets[l][p], flags=pdl)
+                # the previous set was written a whole step earlier: it may be read before the scores
+                fx.fx_topk_select(self.scores, w.k_keep, prev=prev, out=self.sets[l][p],
+                                  flags=pdl | (ready if prev is not None else 0))
                 launches += 2   # attention + top-k (a separate combine kernel, if any, is not counted here)
                 after_topk = True
                 continue

@@ -162,7 +162,8 @@ FX_API fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, in
  * prev_idx (NULL or [rows, k] distinct indices in [0, n)) is the previous step's set: it only speeds
  * the search up (every score at least the smallest score over prev_idx is a candidate) and never
  * changes the result.  An index of prev_idx outside [0, n) sets FX_DEVERR_INDEX and that row runs
- * without the warm start.
+ * without the warm start.  Under FX_LAUNCH_INPUTS_READY, prev_idx is the index list read before the
+ * preceding kernel finishes; the scores are always read after it.
  * 1 <= k <= n.  No workspace.
  */
 FX_API fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int32_t* prev_idx,

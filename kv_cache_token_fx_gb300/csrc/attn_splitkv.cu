@@ -45,7 +45,6 @@ __device__ __forceinline__ float fast_exp2(float x)   // hardware 2^x (relative 
     return y;
 }
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
 {
@@ -105,40 +104,6 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
 
 __device__ __forceinline__ void flag(unsigned* err, unsigned bit) { atomicOr(err, bit); }
 
-// Thread-block-cluster helpers: rank, barrier, and loads from another CTA's shared memory.
-__device__ __forceinline__ unsigned cluster_rank()
-{
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ unsigned cluster_size()
-{
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_map(const void* p, unsigned rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float ld_cluster(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive_relaxed()
 {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");

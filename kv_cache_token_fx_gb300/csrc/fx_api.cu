@@ -332,6 +332,7 @@ fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int3
     p.n = n;
     p.k = k;
     p.prev = prev_idx;
+    p.prev_early = (prev_idx && (flags & FX_LAUNCH_PDL) && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
     p.out = idx_out;
     p.err = ds->err;
     cudaError_t e = launch_topk(p, (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));

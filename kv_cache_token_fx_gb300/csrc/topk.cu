@@ -23,6 +23,8 @@ namespace {
 constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kSmemKeys = 48 * 1024;   // 192 KB of keys
+constexpr int kClusterMinKeys = 16384;  // rows at least this long may be split over a cluster
+constexpr int kClusterMaxCtasPerSm = 152;   // (times 2) cluster CTAs allowed in one launch
 
 __device__ __forceinline__ uint32_t order_key(float f)
 {
@@ -116,9 +118,11 @@ struct SelectShared {
 // The top-k of one row of n keys (in skeys when SMEM, else read from src), written to orow in
 // ascending index order.  prow: the previous set of this row (warm start) or nullptr.  All threads of
 // the CTA call it; it begins and ends with a barrier.
+constexpr int kNoPre = -2147483647 - 1;   // "prev index of this thread not loaded in advance"
+
 template <bool SMEM>
 __device__ void select_row(SelectShared& sh, const uint32_t* skeys, const float* src, int n, int k,
-                           const int32_t* prow, int32_t* orow, unsigned* err)
+                           const int32_t* prow, int32_t* orow, unsigned* err, int pre = kNoPre)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -133,7 +137,7 @@ __device__ void select_row(SelectShared& sh, const uint32_t* skeys, const float*
     if (prow != nullptr) {
         uint32_t kmin = 0xffffffffu;
         for (int i = tid; i < k; i += kTkThreads) {
-            const int t = prow[i];
+            const int t = (i == tid && pre != kNoPre) ? pre : prow[i];
             if (t < 0 || t >= n)
                 sh.bad = 1u;
             else
@@ -265,25 +269,188 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
     extern __shared__ uint32_t skeys[];
     __shared__ SelectShared sh;
 
+    const int row = blockIdx.x;
+    // this thread's entry of the previous set, read before the wait when the caller allows it
+    int pre = kNoPre;
+    if (p.prev_early && p.prev != nullptr && threadIdx.x < p.k) pre = p.prev[(int64_t)row * p.k + threadIdx.x];
     griddep_wait();   // the scores usually come from the kernel just before
     griddep_launch();
-    const int row = blockIdx.x;
     const float* src = p.scores + (int64_t)row * p.n;
     if (SMEM) {
         for (int j = threadIdx.x; j < p.n; j += kTkThreads) skeys[j] = order_key(src[j]);
     }
     select_row<SMEM>(sh, skeys, src, p.n, p.k, p.prev != nullptr ? p.prev + (int64_t)row * p.k : nullptr,
-                     p.out + (int64_t)row * p.k, p.err);
+                     p.out + (int64_t)row * p.k, p.err, pre);
 }
 
-template <typename K>
-cudaError_t allow_smem_keys(K kern)
+// Few long rows: one cluster of kTkCluster CTAs per row.  CTA r of the cluster holds the contiguous
+// chunk r of the row in shared memory; each radix pass counts the chunks in parallel, CTA 0 adds the
+// histograms through distributed shared memory and decides the digit, which every CTA then reads
+// back.  The ordered output offsets each chunk by the (greater, equal) counts of the chunks before
+// it.  Same selection, bit for bit, as select_row.
+constexpr int kTkCluster = 8;
+
+__global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkParams p)
+{
+    extern __shared__ uint32_t skeys[];   // this CTA's chunk
+    __shared__ SelectShared sh;
+    __shared__ uint32_t s_tot[256];       // CTA 0: the row's histogram
+    __shared__ uint32_t s_cnt[2];         // (greater, equal) keys of this chunk
+    __shared__ uint32_t s_base[2];
+    const int row = blockIdx.y / kTkCluster;
+    const unsigned me = cluster_rank();
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int n = p.n;
+    const int k = p.k;
+    const int chunk = (n + kTkCluster - 1) / kTkCluster;
+    const int c0 = min(n, (int)me * chunk);
+    const int cn = min(n, c0 + chunk) - c0;
+    const int32_t* prow = p.prev != nullptr ? p.prev + (int64_t)row * k : nullptr;
+    int pre = kNoPre;
+    if (p.prev_early && prow != nullptr && tid < k) pre = prow[tid];
+    griddep_wait();   // the scores usually come from the kernel just before
+    griddep_launch();
+    const float* src = p.scores + (int64_t)row * n;
+    for (int j = tid; j < cn; j += kTkThreads) skeys[j] = order_key(src[c0 + j]);
+    if (tid == 0) {
+        sh.thr = prow != nullptr ? 0xffffffffu : 0u;
+        sh.bad = 0u;
+    }
+    __syncthreads();
+
+    // warm-start threshold, the same in every CTA (scores read from global memory)
+    uint32_t thr = 0u;
+    if (prow != nullptr) {
+        uint32_t kmin = 0xffffffffu;
+        for (int i = tid; i < k; i += kTkThreads) {
+            const int t = (i == tid && pre != kNoPre) ? pre : prow[i];
+            if (t < 0 || t >= n)
+                sh.bad = 1u;
+            else
+                kmin = min(kmin, order_key(__ldg(src + t)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        if (lane == 0) atomicMin(&sh.thr, kmin);
+        __syncthreads();
+        if (sh.bad) {
+            if (tid == 0 && me == 0) atomicOr(p.err, FX_DEVERR_INDEX);
+        } else {
+            thr = sh.thr;
+        }
+    }
+
+    uint32_t prefix = 0u, pmask = 0u;
+    uint32_t krem = (uint32_t)k;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        uint32_t digit = 0u, gt = 0u;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            for (int i = tid; i < 256; i += kTkThreads) sh.hist[i] = 0u;
+            __syncthreads();
+            for (int j0 = 0; j0 < cn; j0 += kTkThreads) {
+                const int j = j0 + tid;   // whole warps iterate together (ballot/match below)
+                const uint32_t key = j < cn ? skeys[j] : 0u;
+                const bool take = j < cn && key >= thr && (key & pmask) == prefix;
+                const unsigned active = __ballot_sync(0xffffffffu, take);
+                if (take) {
+                    const uint32_t d = (key >> shift) & 255u;
+                    const unsigned peers = __match_any_sync(active, d);
+                    if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+                }
+            }
+            cluster_sync();   // every chunk's histogram is complete
+            if (me == 0) {
+                for (int i = tid; i < 256; i += kTkThreads) {
+                    uint32_t t = 0u;
+                    for (int q = 0; q < kTkCluster; ++q) t += ld_cluster_u32(cluster_map(&sh.hist[i], q));
+                    s_tot[i] = t;
+                }
+                __syncthreads();
+                if (tid < 32) find_digit(s_tot, krem, &sh.digit, &sh.gt);
+            }
+            cluster_sync();   // CTA 0 has decided; every histogram has been read
+            if (tid == 0) {
+                s_base[0] = ld_cluster_u32(cluster_map(&sh.digit, 0));
+                s_base[1] = ld_cluster_u32(cluster_map(&sh.gt, 0));
+            }
+            __syncthreads();
+            digit = s_base[0];
+            gt = s_base[1];
+            __syncthreads();
+            if (digit == 0xffffffffu && thr != 0u) {
+                thr = 0u;   // warm-start threshold from repeated indices: count again without it
+                continue;
+            }
+            break;
+        }
+        if (digit == 0xffffffffu) {
+            // unreachable for 1 <= k <= n (checked on the host); keep the kernel finite anyway
+            if (tid == 0 && me == 0) atomicOr(p.err, FX_DEVERR_INDEX);
+            digit = 0u;
+            gt = 0u;
+        }
+        prefix |= digit << shift;
+        pmask |= 255u << shift;
+        krem -= gt;
+    }
+    const uint32_t kstar = prefix;
+    const uint32_t need_eq = krem;
+
+    // ordered output: counts of this chunk, then the offsets of the chunks before it
+    const int per = (cn + kTkThreads - 1) / kTkThreads;
+    const int j0 = tid * per;
+    const int j1 = min(cn, j0 + per);
+    uint32_t g = 0u, e = 0u;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t key = skeys[j];
+        g += key > kstar ? 1u : 0u;
+        e += key == kstar ? 1u : 0u;
+    }
+    uint32_t total;
+    const uint32_t ex = block_exclusive_scan(g | (e << 16), sh.swarp, &total);
+    if (tid == 0) {
+        s_cnt[0] = total & 0xffffu;
+        s_cnt[1] = total >> 16;
+    }
+    cluster_sync();   // every chunk's counts are visible
+    if (tid == 0) {
+        uint32_t bg = 0u, be = 0u;
+        for (unsigned q = 0; q < me; ++q) {
+            bg += ld_cluster_u32(cluster_map(&s_cnt[0], q));
+            be += ld_cluster_u32(cluster_map(&s_cnt[1], q));
+        }
+        s_base[0] = bg;
+        s_base[1] = be;
+    }
+    __syncthreads();
+    uint32_t gc = s_base[0] + (ex & 0xffffu);
+    uint32_t ec = s_base[1] + (ex >> 16);
+    int32_t* orow = p.out + (int64_t)row * k;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t key = skeys[j];
+        if (key > kstar) {
+            const uint32_t pos = gc + min(ec, need_eq);
+            if (pos < (uint32_t)k) orow[pos] = c0 + j;
+            ++gc;
+        } else if (key == kstar) {
+            if (ec < need_eq && gc + ec < (uint32_t)k) orow[gc + ec] = c0 + j;
+            ++ec;
+        }
+    }
+    cluster_sync();   // keep every CTA's shared memory alive until all remote reads are done
+}
+
+// Raise the kernel's dynamic shared memory limit to the largest key array (once per kernel and device).
+template <auto KERN>
+cudaError_t allow_smem_keys()
 {
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device == dev) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemKeys * (int)sizeof(uint32_t));
     if (e == cudaSuccess) configured_device = dev;
     return e;
@@ -293,9 +460,17 @@ cudaError_t allow_smem_keys(K kern)
 
 cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s)
 {
+    // few long rows: a cluster of CTAs per row (about two CTAs per SM at most)
+    if (p.n >= kClusterMinKeys && p.n <= kTkCluster * kSmemKeys && p.rows * kTkCluster <= 2 * kClusterMaxCtasPerSm) {
+        const int chunk = (p.n + kTkCluster - 1) / kTkCluster;
+        cudaError_t e = allow_smem_keys<topk_cluster_kernel>();
+        if (e != cudaSuccess) return e;
+        return launch_kernel(topk_cluster_kernel, dim3(1, p.rows * kTkCluster), dim3(kTkThreads),
+                             (size_t)chunk * sizeof(uint32_t), s, pdl, (unsigned)kTkCluster, p);
+    }
     if (p.n <= kSmemKeys) {
         const size_t smem = (size_t)p.n * sizeof(uint32_t);
-        cudaError_t e = allow_smem_keys(topk_kernel<true>);
+        cudaError_t e = allow_smem_keys<topk_kernel<true>>();
         if (e != cudaSuccess) return e;
         return launch_kernel(topk_kernel<true>, dim3(p.rows), dim3(kTkThreads), smem, s, pdl, 0u, p);
     }

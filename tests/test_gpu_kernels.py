@@ -118,6 +118,9 @@ def test_topk_warm_start_is_exact(fx, n, k):
     ref = oracle.topk(s.numpy(), k)
     got = fx.fx_topk_select(dev(s), k, prev=dev(prev))
     assert np.array_equal(got.cpu().numpy(), ref)
+    # the previous set read before the dependency wait (programmatic dependent launch, inputs ready)
+    got_early = fx.fx_topk_select(dev(s), k, prev=dev(prev), flags=fx.FX_LAUNCH_PDL | fx.FX_LAUNCH_INPUTS_READY)
+    assert np.array_equal(got_early.cpu().numpy(), ref)
     # a previous set that is the exact answer, and one with repeated entries, change nothing
     got2 = fx.fx_topk_select(dev(s), k, prev=dev(torch.from_numpy(ref)))
     assert np.array_equal(got2.cpu().numpy(), ref)
