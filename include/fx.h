@@ -170,6 +170,25 @@ FX_API fx_status fx_topk_select(const float* scores, int rows, int n, int k, con
                          int32_t* idx_out, unsigned flags, void* stream);
 
 /* ------------------------------------------------------------------------------------------- */
+/* Focal-layer selection by warm-up profiling.  [FastOCR] Focal-Guided Pruning, Focal Layer Selection
+ * (during w warm-up steps, profile each layer's image-attention ratio; the C layers with the highest
+ * ratio become the focal layers).
+ *
+ * fx_focal_mass: for each row r (one (b, KV head)) of scores [rows, n] from fx_focal_attn_scores with
+ * the image tokens as candidates,
+ *   mass[r] = (accumulate ? mass[r] : 0) + (sum_j scores[r, j]) / R
+ * which is the mean share of attention the group's R query rows put on the image tokens (a value in
+ * [0, 1]).  A layer's image-attention ratio is the mean of mass over its rows and the warm-up steps.
+ *   scores [rows, n] fp32; mass [rows] fp32 (read when accumulate != 0, then written).  No workspace.
+ *
+ * fx_choose_focal_layers (host only, no GPU): the C layers with the largest ratio[l] (ties go to the
+ * lower layer), written to layers_out[0..C) in ascending order.  1 <= C <= n_layers.
+ */
+FX_API fx_status fx_focal_mass(const float* scores, int rows, int n, int R, int accumulate, float* mass,
+                        unsigned flags, void* stream);
+FX_API fx_status fx_choose_focal_layers(const float* ratio, int n_layers, int C, int32_t* layers_out);
+
+/* ------------------------------------------------------------------------------------------- */
 /* fx_sparse_gqa_decode -- a non-focal layer: decode attention over the selected tokens only.
  * [FastOCR] Focal-Guided Pruning (non-focal layers attend only to the pruned set; the full cache
  * stays intact); [FastKV] 2.B (decoding over the retained entries).

@@ -19,6 +19,7 @@ from . import build as _build
 
 __all__ = [
     "FxError", "load_library", "library_path", "Workspace", "fx_focal_attn_scores", "fx_topk_select",
+    "fx_focal_mass", "fx_choose_focal_layers",
     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode", "fx_device_errors",
     "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
     "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
@@ -90,6 +91,9 @@ def load_library():
         lib.fx_focal_attn_scores.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_int, c_int, c_float, c_int,
                                              c_int, c_vp, c_vp, c_vp, c_size, c_uint, c_vp]
         lib.fx_topk_select.argtypes = [c_vp, c_int, c_int, c_int, c_vp, c_vp, c_uint, c_vp]
+        lib.fx_focal_mass.argtypes = [c_vp, c_int, c_int, c_int, c_int, c_vp, c_uint, c_vp]
+        lib.fx_choose_focal_layers.argtypes = [ctypes.POINTER(ctypes.c_float), c_int, c_int,
+                                               ctypes.POINTER(ctypes.c_int32)]
         lib.fx_sparse_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_sparse_workspace_bytes.restype = c_size
         lib.fx_sparse_gqa_decode.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_vp, c_int, c_int, c_float,
@@ -106,6 +110,7 @@ def load_library():
         lib.fx_shared_prefix_decode.argtypes = [ctypes.POINTER(PrefixDesc), ctypes.POINTER(BranchDesc), c_vp, c_int,
                                                 c_vp, c_int, c_float, c_vp, c_vp, c_size, c_uint, c_vp]
         for name in ("fx_device_errors", "fx_workspace_init", "fx_focal_attn_scores", "fx_topk_select",
+                     "fx_focal_mass", "fx_choose_focal_layers",
                      "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode"):
             getattr(lib, name).restype = c_int
         _lib = lib
@@ -224,6 +229,36 @@ def fx_focal_attn_scores(k, v, length, q, *, q_pos0: int = -1, scale=None, cand=
     _check(lib.fx_focal_attn_scores(ctypes.byref(desc), _ptr(q), Hq, Mq, int(q_pos0), sc, int(lo), int(hi),
                                     _ptr(out), _ptr(scores), _ptr(buf), buf.numel(), int(flags), _stream(stream)))
     return out, scores
+
+
+def fx_focal_mass(scores, R: int, *, mass=None, accumulate=False, stream=None, flags: int = 0):
+    """Image-attention share per row: mass[r] (+)= sum_j scores[r, j] / R.  scores [..., n] fp32
+    (contiguous, from fx_focal_attn_scores over the image tokens); returns mass [...] fp32."""
+    lib = load_library()
+    _need_cuda(scores, "scores", torch.float32)
+    if not scores.is_contiguous():
+        raise FxError(FX_ERR_INVALID_ARG, "scores must be contiguous")
+    n = scores.shape[-1]
+    rows = scores.numel() // n if n else 0
+    if mass is None:
+        if accumulate:
+            raise FxError(FX_ERR_INVALID_ARG, "accumulate needs a mass tensor")
+        mass = torch.empty(scores.shape[:-1], dtype=torch.float32, device=scores.device)
+    _need_cuda(mass, "mass", torch.float32)
+    if mass.numel() != rows or not mass.is_contiguous():
+        raise FxError(FX_ERR_INVALID_ARG, "mass must be a contiguous tensor of one value per row")
+    _check(lib.fx_focal_mass(_ptr(scores), rows, n, int(R), int(bool(accumulate)), _ptr(mass), int(flags),
+                             _stream(stream)))
+    return mass
+
+
+def fx_choose_focal_layers(ratio, C: int):
+    """The C layers with the largest image-attention ratio (ties: the lower layer), ascending."""
+    lib = load_library()
+    r = (ctypes.c_float * len(ratio))(*[float(x) for x in ratio])
+    out = (ctypes.c_int32 * int(C))()
+    _check(lib.fx_choose_focal_layers(r, len(ratio), int(C), out))
+    return [int(x) for x in out]
 
 
 def fx_topk_select(scores, k: int, *, prev=None, out=None, stream=None, flags: int = 0):

@@ -3,6 +3,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <vector>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -337,6 +338,37 @@ fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int3
     p.err = ds->err;
     cudaError_t e = launch_topk(p, (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+    return FX_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+fx_status fx_focal_mass(const float* scores, int rows, int n, int R, int accumulate, float* mass, unsigned flags,
+                        void* stream)
+{
+    if (!scores || !mass) return fail(FX_ERR_INVALID_ARG, "scores and mass must be non-NULL");
+    if (rows < 1 || n < 1 || R < 1) return fail(FX_ERR_INVALID_ARG, "need rows, n, R >= 1");
+    fx_status st = check_flags(flags);
+    if (st != FX_OK) return st;
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
+    cudaError_t e = launch_focal_mass(scores, rows, n, 1.0f / (float)R, accumulate ? 1 : 0, mass,
+                                      (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "focal mass launch");
+    return FX_OK;
+}
+
+fx_status fx_choose_focal_layers(const float* ratio, int n_layers, int C, int32_t* layers_out)
+{
+    if (!ratio || !layers_out) return fail(FX_ERR_INVALID_ARG, "ratio and layers_out must be non-NULL");
+    if (n_layers < 1 || C < 1 || C > n_layers) return fail(FX_ERR_INVALID_ARG, "need 1 <= C <= n_layers");
+    for (int l = 0; l < n_layers; ++l)
+        if (!isfinite(ratio[l])) return fail(FX_ERR_INVALID_ARG, "ratio[%d] is not finite", l);
+    // the C largest ratios (ties: the lower layer), reported in ascending layer order
+    std::vector<int> order(n_layers);
+    for (int l = 0; l < n_layers; ++l) order[l] = l;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return ratio[a] > ratio[b]; });
+    std::sort(order.begin(), order.begin() + C);
+    for (int i = 0; i < C; ++i) layers_out[i] = order[i];
     return FX_OK;
 }
 

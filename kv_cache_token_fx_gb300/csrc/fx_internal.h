@@ -132,6 +132,8 @@ fx_status set_error(fx_status st, const char* msg);
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s);
+cudaError_t launch_focal_mass(const float* scores, int rows, int n, float inv_r, int accumulate, float* mass,
+                              bool pdl, cudaStream_t s);
 cudaError_t launch_compact(const CompactParams& p, bool pdl, cudaStream_t s);
 
 // Launch `kern` with optional programmatic stream serialization and a (1, cluster_y, 1) cluster.

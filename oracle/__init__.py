@@ -145,6 +145,23 @@ def focal(k, v, length, q, *, scale=None, q_pos0: int = -1, cand=None, want_out=
     return out, sc
 
 
+def focal_mass(scores, R: int) -> np.ndarray:
+    """FastOCR, Focal-Guided Pruning (Focal Layer Selection): the share of attention the R query rows of
+    one (b, KV head) group put on the image tokens.  scores [..., n] are the group's softmax rows summed
+    over R (focal() with the image tokens as candidates), so the share is their sum over the tokens
+    divided by R.  Returns float64 [...]."""
+    s = np.asarray(scores, dtype=np.float64)
+    return s.sum(axis=-1) / float(R)
+
+
+def choose_focal_layers(ratio, C: int) -> list:
+    """FastOCR, Focal-Guided Pruning: the C layers with the highest image-attention ratio (ties go to
+    the lower layer index), listed in ascending layer order."""
+    r = [float(x) for x in ratio]
+    order = sorted(range(len(r)), key=lambda l: (-r[l], l))
+    return sorted(order[:C])
+
+
 def topk(scores, k: int, *, lib=None) -> np.ndarray:
     """scores [..., n] (any float type, compared in double) -> int32 [..., k]: the k best by
     (score descending, index ascending), written in ascending index order."""

@@ -5,6 +5,7 @@ import os
 import re
 import shutil
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -69,6 +70,17 @@ def test_host_argument_checks_without_gpu(lib):
     assert retain(3, 596, 597) == 1 and b"keep_k" in lib.fx_last_error()
     assert retain(3, 596, 37) == 3    # no workspace
     assert lib.fx_retain_workspace_bytes(2, 2, 4, 4, 600, 596) > 2 * 2 * 596 * 4
+    # the focal-layer choice is host code: it runs here, and agrees with the oracle's rule
+    import oracle
+    lib.fx_choose_focal_layers.restype = ctypes.c_int
+    g = np.random.default_rng(4)
+    for n in (1, 3, 7, 28):
+        ratio = g.integers(0, 4, size=n).astype(np.float32) / 4
+        for C in range(1, n + 1, max(1, n // 5)):
+            out = (ctypes.c_int32 * C)()
+            assert lib.fx_choose_focal_layers((ctypes.c_float * n)(*ratio), n, C, out) == 0
+            assert list(out) == oracle.choose_focal_layers(ratio.tolist(), C)
+    assert lib.fx_choose_focal_layers((ctypes.c_float * 2)(0.1, 0.2), 2, 3, (ctypes.c_int32 * 3)()) == 1
     lib.fx_sparse_workspace_bytes.restype = ctypes.c_size_t
     assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) > 0
     assert lib.fx_sparse_workspace_bytes(0, 8, 16, 205, 4096, 4864) == 0

@@ -314,6 +314,41 @@ def test_per_layer_retention_matches_oracle(fx):
             assert torch.equal(dv[l, b, :, :n].cpu().view(torch.int16), rv[b, :, :n].view(torch.int16))
 
 
+def test_focal_layer_profiling_matches_oracle(fx):
+    """Warm-up profiling of the image-attention ratio per layer (fx_focal_mass over each layer's image
+    scores, accumulated over the warm-up steps) and the choice of the C focal layers."""
+    n_layers, B, Hkv, G, T, n_img, steps, C = 4, 2, 2, 2, 300, 200, 2, 2
+    boost = (0.0, 0.5, 0.15, 0.9)   # how strongly each layer's image keys align with the queries
+    length = torch.tensor([T, 260], dtype=torch.int32)
+    qs = [[rnd((B, Hkv * G, 1, D), 170 + t, 10 + l) for l in range(n_layers)] for t in range(steps)]
+    ks, vs = [], []
+    for l in range(n_layers):
+        k = rnd((B, Hkv, T, D), 180 + l, 1).float()
+        u = sum(qs[t][l].float().sum(dim=2) for t in range(steps))          # [B, Hq, D]
+        u = u.view(B, Hkv, G, D).sum(dim=2)
+        u = u / u.norm(dim=-1, keepdim=True)
+        k[:, :, :n_img] += boost[l] * 4.0 * u[:, :, None, :]
+        ks.append(k.to(torch.bfloat16))
+        vs.append(rnd((B, Hkv, T, D), 180 + l, 2))
+    mass = [torch.zeros((B, Hkv), dtype=torch.float32, device="cuda") for _ in range(n_layers)]
+    ref = [np.zeros((B, Hkv)) for _ in range(n_layers)]
+    for t in range(steps):
+        for l in range(n_layers):
+            _, sc = fx.fx_focal_attn_scores(dev(ks[l]), dev(vs[l]), dev(length), dev(qs[t][l]), cand=(0, n_img),
+                                            want_out=False)
+            fx.fx_focal_mass(sc, G, mass=mass[l], accumulate=t > 0)
+            _, rsc = oracle.focal(ks[l], vs[l], length, qs[t][l], cand=(0, n_img), want_out=False)
+            ref[l] += oracle.focal_mass(rsc, G)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    for l in range(n_layers):
+        got = mass[l].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref[l]) <= 1e-4 * np.abs(ref[l]) + 1e-7), (l, got, ref[l])
+    ratio = [float(mass[l].mean()) / steps for l in range(n_layers)]
+    ref_ratio = [float(ref[l].mean()) / steps for l in range(n_layers)]
+    assert fx.fx_choose_focal_layers(ratio, C) == oracle.choose_focal_layers(ref_ratio, C) == [1, 3]
+
+
 def test_compaction_capacity_is_flagged(fx):
     B, Hkv, T = 1, 1, 50
     k, v = kv_case(B, Hkv, T, 60)

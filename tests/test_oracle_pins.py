@@ -224,6 +224,77 @@ def pin_shared_prefix_equals_concatenation(lib=None):
             assert np.max(np.abs(got[b] - ref[0])) < TOL, (b, pi is None)
 
 
+# Focal-layer profiling (FastOCR, Focal-Guided Pruning: Focal Layer Selection), pinned without
+# reference to how focal_mass / choose_focal_layers are written.
+
+def pin_focal_mass_whole_range_is_one(lib=None, mass_fn=None):
+    """With every visible token a candidate, each of the R softmax rows puts all of its attention on the
+    candidates: the share is exactly 1."""
+    mass_fn = mass_fn or oracle.focal_mass
+    B, Hkv, G, Mq, T = 2, 2, 2, 3, 37
+    k, v = _rand_bf16((B, Hkv, T, 128), 31, 1), _rand_bf16((B, Hkv, T, 128), 31, 2)
+    q = _rand_bf16((B, Hkv * G, Mq, 128), 31, 3)
+    length = torch.tensor([T, 20], dtype=torch.int32)
+    _, sc = oracle.focal(k, v, length, q, cand=(0, T), want_out=False, lib=lib)
+    m = mass_fn(sc, G * Mq)
+    assert np.all(np.abs(m - 1.0) < 1e-12), m
+
+
+def pin_focal_mass_uniform_attention(lib=None, mass_fn=None):
+    """q = 0 gives uniform attention over the len visible tokens: the share of the first n_img of them
+    is n_img / len."""
+    mass_fn = mass_fn or oracle.focal_mass
+    B, Hkv, G, Mq, T, n_img = 1, 2, 4, 2, 50, 30
+    k, v = _rand_bf16((B, Hkv, T, 128), 32, 1), _rand_bf16((B, Hkv, T, 128), 32, 2)
+    q = torch.zeros((B, Hkv * G, Mq, 128), dtype=torch.bfloat16)
+    length = torch.tensor([40], dtype=torch.int32)
+    _, sc = oracle.focal(k, v, length, q, cand=(0, n_img), want_out=False, lib=lib)
+    m = mass_fn(sc, G * Mq)
+    assert np.all(np.abs(m - n_img / 40.0) < 1e-12), m
+
+
+def pin_choose_focal_layers_brute_force(lib=None, choose_fn=None):
+    """Every chosen layer outranks every other layer (higher ratio, or equal ratio and lower index);
+    exhaustive over small ratio vectors with ties."""
+    choose_fn = choose_fn or oracle.choose_focal_layers
+    levels = (0.1, 0.4, 0.4, 0.7)
+    for n in range(1, 6):
+        for ratio in itertools.product(levels, repeat=n):
+            for C in range(1, n + 1):
+                got = choose_fn(list(ratio), C)
+                assert len(got) == C and got == sorted(got) and len(set(got)) == C, (ratio, C, got)
+                rest = [l for l in range(n) if l not in got]
+                for i in got:
+                    for j in rest:
+                        assert ratio[i] > ratio[j] or (ratio[i] == ratio[j] and i < j), (ratio, C, got)
+
+
+PROFILE_PINS = [pin_focal_mass_whole_range_is_one, pin_focal_mass_uniform_attention,
+                pin_choose_focal_layers_brute_force]
+
+
+@pytest.mark.parametrize("pin", PROFILE_PINS, ids=[p.__name__ for p in PROFILE_PINS])
+def test_profile_pin(pin, oracle_mod):
+    pin()
+
+
+def test_profile_pins_catch_planted_mistakes(oracle_mod):
+    """Plausible mistakes in the profiling functions each fail a pin (planted here, on the CPU)."""
+    wrong_mass = [lambda s, R: np.asarray(s, np.float64).sum(axis=-1),            # R not divided out
+                  lambda s, R: np.asarray(s, np.float64).mean(axis=-1),           # mean over tokens
+                  lambda s, R: np.asarray(s, np.float64).max(axis=-1) / R]        # max instead of sum
+    for fn in wrong_mass:
+        with pytest.raises(AssertionError):
+            pin_focal_mass_whole_range_is_one(mass_fn=fn)
+            pin_focal_mass_uniform_attention(mass_fn=fn)
+    wrong_choose = [lambda r, C: sorted(sorted(range(len(r)), key=lambda l: (r[l], l))[:C]),      # smallest
+                    lambda r, C: sorted(sorted(range(len(r)), key=lambda l: (-r[l], -l))[:C]),    # ties high
+                    lambda r, C: sorted(range(len(r)), key=lambda l: (-r[l], l))[:C]]            # unsorted
+    for fn in wrong_choose:
+        with pytest.raises(AssertionError):
+            pin_choose_focal_layers_brute_force(choose_fn=fn)
+
+
 PINS = [pin_golden_focal, pin_golden_topk, pin_golden_sparse, pin_golden_shared_prefix,
         pin_uniform_keys_give_mean, pin_importance_sums_to_rows, pin_single_key_and_dominant_key,
         pin_topk_brute_force, pin_sparse_full_set_equals_dense, pin_compaction_equals_sparse,
