@@ -70,8 +70,8 @@ def open_library(path: str):
     lib.oracle_kv_compact.restype = None
     lib.oracle_shared_prefix.argtypes = [c_vp, c_vp, c_i64, c_i64, c_int, c_vp, c_vp, c_i64,
                                          c_i64, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp,
-                                         c_int, c_int, c_int, c_int, c_int, c_vp, c_int, c_dbl,
-                                         c_vp]
+                                         c_int, c_int, c_int, c_int, c_int, c_vp, c_int, c_vp, c_vp,
+                                         c_dbl, c_vp]
     lib.oracle_shared_prefix.restype = None
     return lib
 
@@ -217,12 +217,15 @@ def kv_compact(k, v, length, idx, tail_lo: int, cap: int, *, lib=None):
     return dk, dv, dl
 
 
-def shared_prefix(pk, pv, sk, sv, off, dk, dv, q, prefix_idx=None, *, scale=None, lib=None):
+def shared_prefix(pk, pv, sk, sv, off, dk, dv, q, prefix_idx=None, *, pre_len=None, suf_len=None, scale=None,
+                  lib=None):
     """Shared-prefix draft verification.
 
     pk, pv : bf16 [Hkv, P, d]            one prefix shared by every branch
-    sk, sv : bf16 [Hkv, sum L_b, d]      private suffixes; branch b owns rows off[b] .. off[b+1]-1
-    off    : int32 [Br + 1]
+    sk, sv : bf16 [Hkv, S, d]            private suffixes; branch b owns rows off[b] .. off[b]+L_b-1
+    off    : int32 [Br + 1] (L_b = off[b+1] - off[b]), or [Br] starts when suf_len gives the L_b
+    pre_len: int32 [Br] or None          rows of the prefix branch b sees (its fork position); None: all P
+    suf_len: int32 [Br] or None
     dk, dv : bf16 [Br, Mq, Hkv, d]       draft rows; draft position i sees draft rows 0 .. i
     q      : bf16 [Br, Hq, Mq, d]
     prefix_idx : int32 [Br, Hkv, kp] or None (dense prefix)
@@ -242,11 +245,15 @@ def shared_prefix(pk, pv, sk, sv, off, dk, dv, q, prefix_idx=None, *, scale=None
     scale = default_scale(d) if scale is None else float(scale)
     out = np.zeros((Br, Hq, Mq, d), np.float64)
     qb = _bits(q.contiguous())
+    pl = _i32(pre_len) if pre_len is not None else None
+    sl = _i32(suf_len) if suf_len is not None else None
     lib.oracle_shared_prefix(_bits(pk).data_ptr(), _bits(pv).data_ptr(), pk.stride(0), pk.stride(1), P,
                              _bits(sk).data_ptr(), _bits(sv).data_ptr(), sk.stride(0), sk.stride(1),
                              o.data_ptr(), _bits(dk).data_ptr(), _bits(dv).data_ptr(), dk.stride(0),
                              dk.stride(1), dk.stride(2), qb.data_ptr(), Br, Hkv, Hq, Mq, d,
-                             pi.data_ptr() if pi is not None else None, kp, scale, out.ctypes.data)
+                             pi.data_ptr() if pi is not None else None, kp,
+                             pl.data_ptr() if pl is not None else None, sl.data_ptr() if sl is not None else None,
+                             scale, out.ctypes.data)
     return out
 
 

@@ -356,8 +356,10 @@ void oracle_kv_compact(const uint16_t* sk, const uint16_t* sv, const int32_t* le
 
 /* ------------------------------------------------------------------------------------------ */
 /* Shared-prefix draft verification (HPD-Parsing parts 2 and 3).  Branch b's draft position i    */
-/* attends over: the shared prefix (every row, or the rows prefix_idx[b, h, 0..kp) when given),  */
-/* then its own suffix rows off[b] .. off[b+1]-1, then its own draft rows 0 .. i (causal).       */
+/* attends over: the shared prefix it forked from -- its first pre_len[b] rows (all P without     */
+/* pre_len), or the rows prefix_idx[b, h, 0..kp) when given -- then its own suffix rows off[b] ..  */
+/* off[b]+L_b-1 (L_b = suf_len[b], or off[b+1]-off[b] without suf_len), then its own draft rows    */
+/* 0 .. i (causal).                                                                                */
 
 typedef struct {
     const uint16_t *pk, *pv;
@@ -372,6 +374,8 @@ typedef struct {
     int Br, Hkv, Hq, Mq, d;
     const int32_t* pidx;
     int kp;
+    const int32_t* pre_len;
+    const int32_t* suf_len;
     double scale;
     double* out;
 } prefix_ctx;
@@ -381,8 +385,9 @@ static void prefix_item(void* vctx, int item, double* scratch)
     prefix_ctx* c = (prefix_ctx*)vctx;
     int b = item / c->Hkv, h = item % c->Hkv;
     int G = c->Hq / c->Hkv, d = c->d;
-    int np = c->pidx ? c->kp : c->P;
-    int ns = c->off[b + 1] - c->off[b];
+    int np = c->pidx ? c->kp : (c->pre_len ? c->pre_len[b] : c->P);
+    int s0 = c->off[b];
+    int ns = c->suf_len ? c->suf_len[b] : c->off[b + 1] - c->off[b];
     int nmax = np + ns + c->Mq;
     const uint16_t** kr = (const uint16_t**)malloc(sizeof(void*) * (size_t)nmax);
     const uint16_t** vr = (const uint16_t**)malloc(sizeof(void*) * (size_t)nmax);
@@ -392,7 +397,7 @@ static void prefix_item(void* vctx, int item, double* scratch)
         kr[m] = c->pk + h * c->p_sh + (int64_t)t * c->p_st;
         vr[m] = c->pv + h * c->p_sh + (int64_t)t * c->p_st;
     }
-    for (int t = c->off[b]; t < c->off[b + 1]; ++t, ++m) {
+    for (int t = s0; t < s0 + ns; ++t, ++m) {
         kr[m] = c->sk + h * c->s_sh + (int64_t)t * c->s_st;
         vr[m] = c->sv + h * c->s_sh + (int64_t)t * c->s_st;
     }
@@ -417,20 +422,24 @@ static void prefix_item(void* vctx, int item, double* scratch)
 
 /*
  * prefix: rows (h, t) at pk + h*p_sh + t*p_st, t < P;   suffix: rows (h, t) at sk + h*s_sh + t*s_st
- * with branch b owning t in [off[b], off[b+1]);  draft: rows (b, i, h) at dk + b*d_sb + i*d_si + h*d_sh;
- * q, out: [Br, Hq, Mq, d];  prefix_idx: [Br, Hkv, kp] or NULL (dense prefix).
+ * with branch b owning t in [off[b], off[b] + L_b);  draft: rows (b, i, h) at dk + b*d_sb + i*d_si + h*d_sh;
+ * q, out: [Br, Hq, Mq, d];  prefix_idx: [Br, Hkv, kp] or NULL (dense prefix);
+ * pre_len: [Br] visible prefix rows per branch (its fork position) or NULL (all P);
+ * suf_len: [Br] suffix rows per branch or NULL (L_b = off[b+1] - off[b]).
  */
 void oracle_shared_prefix(const uint16_t* pk, const uint16_t* pv, int64_t p_sh, int64_t p_st, int P,
                           const uint16_t* sk, const uint16_t* sv, int64_t s_sh, int64_t s_st,
                           const int32_t* off, const uint16_t* dk, const uint16_t* dv, int64_t d_sb,
                           int64_t d_si, int64_t d_sh, const uint16_t* q, int Br, int Hkv, int Hq,
-                          int Mq, int d, const int32_t* prefix_idx, int kp, double scale, double* out)
+                          int Mq, int d, const int32_t* prefix_idx, int kp, const int32_t* pre_len,
+                          const int32_t* suf_len, double scale, double* out)
 {
     prefix_ctx c = {pk, pv, p_sh, p_st, P, sk, sv, s_sh, s_st, off, dk, dv, d_sb, d_si, d_sh,
-                    q, Br, Hkv, Hq, Mq, d, prefix_idx, kp, scale, out};
+                    q, Br, Hkv, Hq, Mq, d, prefix_idx, kp, pre_len, suf_len, scale, out};
     int nmax = 0;
     for (int b = 0; b < Br; ++b) {
-        int n = (prefix_idx ? kp : P) + (off[b + 1] - off[b]) + Mq;
+        int np = prefix_idx ? kp : (pre_len ? pre_len[b] : P);
+        int n = np + (suf_len ? suf_len[b] : off[b + 1] - off[b]) + Mq;
         if (n > nmax) nmax = n;
     }
     parallel_for(Br * Hkv, prefix_item, &c, (size_t)nmax + 2 * (size_t)d);

@@ -224,6 +224,32 @@ def pin_shared_prefix_equals_concatenation(lib=None):
             assert np.max(np.abs(got[b] - ref[0])) < TOL, (b, pi is None)
 
 
+def pin_forked_branches_equal_concatenation(lib=None):
+    """Branches forked at different prefix positions (HPD-Parsing part 2: a content branch sees the
+    shared context up to its fork position) with suffixes in fixed, non-adjacent slots equal attention
+    over each branch's explicitly concatenated cache."""
+    Hkv, G, P, Mq, Br, d, slot = 2, 2, 15, 2, 4, 128, 6
+    pre_len = [15, 4, 0, 9]
+    suf_len = [0, 6, 3, 1]
+    off = [b * slot for b in range(Br)]
+    pk, pv = _rand_bf16((Hkv, P, d), 8, 1), _rand_bf16((Hkv, P, d), 8, 2)
+    sk, sv = _rand_bf16((Hkv, Br * slot, d), 8, 3), _rand_bf16((Hkv, Br * slot, d), 8, 4)
+    dk, dv = _rand_bf16((Br, Mq, Hkv, d), 8, 5), _rand_bf16((Br, Mq, Hkv, d), 8, 6)
+    q = _rand_bf16((Br, Hkv * G, Mq, d), 8, 7)
+    got = oracle.shared_prefix(pk, pv, sk, sv, torch.tensor(off, dtype=torch.int32), dk, dv, q,
+                               pre_len=torch.tensor(pre_len, dtype=torch.int32),
+                               suf_len=torch.tensor(suf_len, dtype=torch.int32), lib=lib)
+    for b in range(Br):
+        ck = torch.stack([torch.cat([pk[h, :pre_len[b]], sk[h, off[b]:off[b] + suf_len[b]], dk[b, :, h]])
+                          for h in range(Hkv)]).unsqueeze(0).contiguous()
+        cv = torch.stack([torch.cat([pv[h, :pre_len[b]], sv[h, off[b]:off[b] + suf_len[b]], dv[b, :, h]])
+                          for h in range(Hkv)]).unsqueeze(0).contiguous()
+        n = ck.shape[2]
+        ref, _ = oracle.focal(ck, cv, torch.tensor([n], dtype=torch.int32), q[b:b + 1].contiguous(),
+                              q_pos0=n - Mq, want_scores=False, lib=lib)
+        assert np.max(np.abs(got[b] - ref[0])) < TOL, b
+
+
 # Focal-layer profiling (FastOCR, Focal-Guided Pruning: Focal Layer Selection), pinned without
 # reference to how focal_mass / choose_focal_layers are written.
 
@@ -298,7 +324,7 @@ def test_profile_pins_catch_planted_mistakes(oracle_mod):
 PINS = [pin_golden_focal, pin_golden_topk, pin_golden_sparse, pin_golden_shared_prefix,
         pin_uniform_keys_give_mean, pin_importance_sums_to_rows, pin_single_key_and_dominant_key,
         pin_topk_brute_force, pin_sparse_full_set_equals_dense, pin_compaction_equals_sparse,
-        pin_shared_prefix_equals_concatenation]
+        pin_shared_prefix_equals_concatenation, pin_forked_branches_equal_concatenation]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -322,8 +348,9 @@ MUTATIONS = {
     "compact_tail_shift": ("tail_lo + (r - kk);", "tail_lo + (r - kk) + (r > kk);"),
     "draft_not_causal": ("attend(qrow, d, c->scale, m + i + 1, kr, vr, p, orow);",
                          "attend(qrow, d, c->scale, m + c->Mq, kr, vr, p, orow);"),
-    "suffix_wrong_branch": ("for (int t = c->off[b]; t < c->off[b + 1]; ++t, ++m) {",
-                            "for (int t = c->off[b > 0 ? b - 1 : 0]; t < c->off[b + 1]; ++t, ++m) {"),
+    "suffix_wrong_branch": ("int s0 = c->off[b];", "int s0 = c->off[b > 0 ? b - 1 : 0];"),
+    "fork_position_ignored": ("int np = c->pidx ? c->kp : (c->pre_len ? c->pre_len[b] : c->P);",
+                              "int np = c->pidx ? c->kp : c->P;"),
     "value_uses_key": ("out[c] += p[j] * bf(v[c]);", "out[c] += p[j] * bf(kr[j][c]);"),
     "normaliser_dropped": ("for (int j = 0; j < n; ++j) p[j] /= z;", ";"),
     "len_ignored": ("int visible = n;", "int visible = c->Tcap;"),
