@@ -260,19 +260,25 @@ FX_API fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride
 /* fx_shared_prefix_decode -- parallel draft verification over a shared prefix.  [HPD] parts 2
  * (shared-prefix KV reuse with context isolation) and 3 (P-MTP parallel verification).
  *
- * Br branches share one prefix KV.  Branch b owns suffix rows off[b] .. off[b+1]-1 and Mq draft
- * rows.  For branch b, KV head h and query row (gi, i) (query head h*G + gi, draft position i):
- *   S = prefix rows (all P of them, or prefix_idx[b, h, 0..kp) when prefix_idx != NULL)
+ * Br branches share one prefix KV; branch b sees its first P_b rows (P_b = len[b], the branch's fork
+ * position, or P when len == NULL) -- zero-copy reuse of the context visible where it forked.  It
+ * owns suffix rows off[b] .. off[b]+L_b-1 and Mq draft rows.  For branch b, KV head h and query row
+ * (gi, i) (query head h*G + gi, draft position i):
+ *   S = prefix rows 0..P_b-1 (or prefix_idx[b, h, 0..kp) when prefix_idx != NULL)
  *       ++ the branch's suffix rows ++ the branch's draft rows 0..i         (causal inside the draft)
  *   out[b, h*G+gi, i, :] = sum_{j in S} softmax_S(scale * q . k_j) v_j
  *
- *   prefix      rows (h, t) at k + h*stride_h + t*stride_t, t < P (k and v non-NULL even when P == 0)
+ *   prefix      rows (h, t) at k + h*stride_h + t*stride_t, t < P (k and v non-NULL even when P == 0);
+ *               len: NULL or device [Br] int32 in [0, P] (outside: FX_DEVERR_LEN, clamped)
  *   suffix      rows (h, t) at suf_k + h*suf_stride_h + t*suf_stride_t, t < suf_rows
- *   suf_off     device [Br + 1] int32, non-decreasing, suf_off[Br] <= suf_rows; max_suffix bounds
- *               every suf_off[b+1] - suf_off[b] (longer suffixes set FX_DEVERR_OFFSETS and are cut)
+ *   suf_off     suf_len == NULL: device [Br + 1] int32, non-decreasing, L_b = suf_off[b+1] - suf_off[b];
+ *               suf_len != NULL: device [Br] starts and L_b = suf_len[b] (ranges anywhere, e.g. fixed
+ *               slots of a branch pool); every range must lie in [0, suf_rows) and L_b <= max_suffix
+ *               (else FX_DEVERR_OFFSETS: an out-of-range suffix is skipped, a long one cut)
  *   draft       rows (b, i, h) at draft_k + b*draft_stride_b + i*draft_stride_i + h*draft_stride_h
  *   q           [Br, Hq, Mq, 128] bf16;  out [Br, Hq, Mq, 128] fp32;  G*Mq <= 64
- *   prefix_idx  NULL (dense prefix) or [Br, Hkv, kp] int32 prefix positions in [0, P)
+ *   prefix_idx  NULL (dense prefix) or [Br, Hkv, kp] int32 prefix positions in [0, P_b) (others set
+ *               FX_DEVERR_INDEX and are skipped)
  * Workspace: fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np, max_suffix) bytes, where np is
  * P (dense) or kp (sparse).
  */
@@ -281,6 +287,7 @@ typedef struct {
     const fx_bf16* v;
     int64_t stride_h, stride_t;
     int32_t P, Hkv, d;
+    const int32_t* len;   /* [Br] visible prefix rows per branch (fork positions), or NULL: all P */
 } fx_prefix_desc;
 
 typedef struct {
@@ -293,6 +300,7 @@ typedef struct {
     const fx_bf16* draft_v;
     int64_t draft_stride_b, draft_stride_i, draft_stride_h;
     int32_t Br, Mq;
+    const int32_t* suf_len;   /* [Br] suffix rows per branch (suf_off then holds starts), or NULL */
 } fx_branch_desc;
 
 FX_API size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np, int max_suffix);
@@ -300,6 +308,42 @@ FX_API fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_
                                   const fx_bf16* q, int Hq, const int32_t* prefix_idx, int kp,
                                   float scale, float* out, void* ws, size_t ws_bytes, unsigned flags,
                                   void* stream);
+
+/* ------------------------------------------------------------------------------------------- */
+/* Branch pool -- host-side bookkeeping for layout-coordinated parallel decoding.  [HPD] part 2
+ * (content branches fork at <FORK>, reuse the shared prefix KV visible at the fork position without a
+ * copy, and the shared KV is released by reference count when every child is done).
+ *
+ * One shared prefix of at most prefix_cap rows (the parent's context; it grows as the layout branch
+ * decodes) and at most max_branches content branches, each owning the fixed slot of suffix rows
+ * [id*slot_rows, (id+1)*slot_rows) of a caller-owned suffix buffer.  The pool does no GPU work and
+ * owns no device memory: it hands out rows and fills the branch arrays of fx_shared_prefix_decode.
+ * Calls returning int give -1 on error (message in fx_last_error); the pool is thread-safe.
+ *   create           NULL on bad sizes
+ *   extend_prefix    the parent appends n prefix rows: first new row (-1 past prefix_cap)
+ *   fork             a new branch whose fork position is the current prefix length: its id (= slot),
+ *                    -1 when every slot is taken; the prefix gains a reference
+ *   append           reserve n more suffix rows of branch id: the first row to write (-1 when the
+ *                    slot would overflow or the branch is not live)
+ *   release          branch id done: its slot is free; returns the prefix references left
+ *   release_parent   the parent is done (no more extend/fork); returns the references left -- at 0
+ *                    the prefix buffer may be freed
+ *   batch            the live branches in ascending id order: ids, suffix starts (suf_off with
+ *                    suf_len), suffix lengths and fork positions (fx_prefix_desc.len), host arrays of
+ *                    max_branches entries; returns how many
+ */
+typedef struct fx_branch_pool fx_branch_pool;
+FX_API fx_branch_pool* fx_branch_pool_create(int prefix_cap, int max_branches, int slot_rows);
+FX_API void fx_branch_pool_destroy(fx_branch_pool* pool);
+FX_API int fx_branch_pool_extend_prefix(fx_branch_pool* pool, int n);
+FX_API int fx_branch_pool_fork(fx_branch_pool* pool);
+FX_API int fx_branch_pool_append(fx_branch_pool* pool, int branch, int n);
+FX_API int fx_branch_pool_release(fx_branch_pool* pool, int branch);
+FX_API int fx_branch_pool_release_parent(fx_branch_pool* pool);
+FX_API int fx_branch_pool_prefix_refs(fx_branch_pool* pool);
+FX_API int fx_branch_pool_prefix_len(fx_branch_pool* pool);
+FX_API int fx_branch_pool_batch(fx_branch_pool* pool, int32_t* ids, int32_t* suf_start, int32_t* suf_len,
+                         int32_t* prefix_len);
 
 /* ------------------------------------------------------------------------------------------- */
 /* fx_focal_attn_scores_noalloc -- fx_focal_attn_scores for callers that cannot allocate device

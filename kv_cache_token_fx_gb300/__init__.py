@@ -23,7 +23,7 @@ __all__ = [
     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode", "fx_device_errors",
     "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
     "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
-    "FX_LAUNCH_PDL", "FX_LAUNCH_INPUTS_READY",
+    "FX_LAUNCH_PDL", "FX_LAUNCH_INPUTS_READY", "BranchPool",
 ]
 
 FX_OK, FX_ERR_INVALID_ARG, FX_ERR_UNSUPPORTED, FX_ERR_WORKSPACE, FX_ERR_CUDA, FX_ERR_DEVICE = range(6)
@@ -53,14 +53,14 @@ KVOutDesc = type("KVOutDesc", (ctypes.Structure,), {"_fields_": KVDesc._fields_}
 
 class PrefixDesc(ctypes.Structure):
     _fields_ = [("k", c_vp), ("v", c_vp), ("stride_h", c_i64), ("stride_t", c_i64), ("P", c_i32),
-                ("Hkv", c_i32), ("d", c_i32)]
+                ("Hkv", c_i32), ("d", c_i32), ("len", c_vp)]
 
 
 class BranchDesc(ctypes.Structure):
     _fields_ = [("suf_k", c_vp), ("suf_v", c_vp), ("suf_stride_h", c_i64), ("suf_stride_t", c_i64),
                 ("suf_off", c_vp), ("suf_rows", c_i32), ("max_suffix", c_i32), ("draft_k", c_vp),
                 ("draft_v", c_vp), ("draft_stride_b", c_i64), ("draft_stride_i", c_i64),
-                ("draft_stride_h", c_i64), ("Br", c_i32), ("Mq", c_i32)]
+                ("draft_stride_h", c_i64), ("Br", c_i32), ("Mq", c_i32), ("suf_len", c_vp)]
 
 
 _lib = None
@@ -105,6 +105,16 @@ def load_library():
         lib.fx_kv_retain_per_layer.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_int, c_vp, c_int, c_int, c_int,
                                                c_float, c_int, c_int, c_int, c_vp, ctypes.POINTER(KVOutDesc), c_i64,
                                                c_vp, c_size, ctypes.c_uint, c_vp]
+        lib.fx_branch_pool_create.argtypes = [c_int, c_int, c_int]
+        lib.fx_branch_pool_create.restype = c_vp
+        lib.fx_branch_pool_destroy.argtypes = [c_vp]
+        lib.fx_branch_pool_destroy.restype = None
+        for name, args in (("extend_prefix", [c_vp, c_int]), ("fork", [c_vp]), ("append", [c_vp, c_int, c_int]),
+                           ("release", [c_vp, c_int]), ("release_parent", [c_vp]), ("prefix_refs", [c_vp]),
+                           ("prefix_len", [c_vp]), ("batch", [c_vp] + [ctypes.POINTER(ctypes.c_int32)] * 4)):
+            f = getattr(lib, "fx_branch_pool_" + name)
+            f.argtypes = args
+            f.restype = c_int
         lib.fx_shared_prefix_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_shared_prefix_workspace_bytes.restype = c_size
         lib.fx_shared_prefix_decode.argtypes = [ctypes.POINTER(PrefixDesc), ctypes.POINTER(BranchDesc), c_vp, c_int,
@@ -375,11 +385,13 @@ def fx_kv_retain_per_layer(k, v, length, q, keep_k: int, cand_hi: int, tail_lo: 
 
 
 def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, prefix_idx=None, scale=None,
-                            out=None, ws=None, stream=None, flags: int = 0):
+                            prefix_len=None, suf_len=None, out=None, ws=None, stream=None, flags: int = 0):
     """Draft verification of Br branches over one shared prefix.
 
-    pk, pv [Hkv, P, 128]; sk, sv [Hkv, S, 128] (branch b owns rows off[b]..off[b+1]-1);
-    off int32 [Br + 1]; dk, dv [Br, Mq, Hkv, 128]; q [Br, Hq, Mq, 128]; prefix_idx [Br, Hkv, kp] or None.
+    pk, pv [Hkv, P, 128]; sk, sv [Hkv, S, 128]; dk, dv [Br, Mq, Hkv, 128]; q [Br, Hq, Mq, 128];
+    prefix_idx [Br, Hkv, kp] or None.  Branch b owns suffix rows off[b]..off[b+1]-1 (off int32 [Br+1]),
+    or off[b]..off[b]+suf_len[b]-1 when suf_len [Br] is given; it sees the first prefix_len[b] prefix
+    rows (its fork position; all P when prefix_len is None).
     """
     lib = load_library()
     for t, n in ((pk, "pk"), (pv, "pv"), (sk, "sk"), (sv, "sv"), (dk, "dk"), (dv, "dv"), (q, "q")):
@@ -391,9 +403,18 @@ def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, 
         raise FxError(FX_ERR_INVALID_ARG, "q must be contiguous")
     Hkv, P, d = pk.shape
     Br, Hq, Mq, _ = q.shape
-    pre = PrefixDesc(pk.data_ptr(), pv.data_ptr(), pk.stride(0), pk.stride(1), P, Hkv, d)
+    for t, n in ((prefix_len, "prefix_len"), (suf_len, "suf_len")):
+        if t is not None:
+            _need_cuda(t, n, torch.int32)
+            if t.numel() != Br or not t.is_contiguous():
+                raise FxError(FX_ERR_INVALID_ARG, f"{n} must be a contiguous [Br] int32 tensor")
+    if off.numel() != (Br if suf_len is not None else Br + 1):
+        raise FxError(FX_ERR_INVALID_ARG, "off must hold Br + 1 offsets (or Br starts with suf_len)")
+    pre = PrefixDesc(pk.data_ptr(), pv.data_ptr(), pk.stride(0), pk.stride(1), P, Hkv, d,
+                     prefix_len.data_ptr() if prefix_len is not None else None)
     brd = BranchDesc(sk.data_ptr(), sv.data_ptr(), sk.stride(0), sk.stride(1), off.data_ptr(), sk.shape[1],
-                     int(max_suffix), dk.data_ptr(), dv.data_ptr(), dk.stride(0), dk.stride(1), dk.stride(2), Br, Mq)
+                     int(max_suffix), dk.data_ptr(), dv.data_ptr(), dk.stride(0), dk.stride(1), dk.stride(2), Br, Mq,
+                     suf_len.data_ptr() if suf_len is not None else None)
     kp = 0
     if prefix_idx is not None:
         _need_cuda(prefix_idx, "prefix_idx", torch.int32)
@@ -409,6 +430,58 @@ def fx_shared_prefix_decode(pk, pv, sk, sv, off, dk, dv, q, *, max_suffix: int, 
     _check(lib.fx_shared_prefix_decode(ctypes.byref(pre), ctypes.byref(brd), _ptr(q), Hq, _ptr(prefix_idx), kp, sc,
                                        _ptr(out), _ptr(buf), buf.numel(), int(flags), _stream(stream)))
     return out
+
+
+class BranchPool:
+    """Host bookkeeping of content branches forked from one shared prefix (include/fx.h: branch pool).
+    Thin wrapper: every method is one C call; errors raise FxError."""
+
+    def __init__(self, prefix_cap: int, max_branches: int, slot_rows: int):
+        lib = load_library()
+        self._lib = lib
+        self._h = lib.fx_branch_pool_create(int(prefix_cap), int(max_branches), int(slot_rows))
+        if not self._h:
+            _check(FX_ERR_INVALID_ARG)
+        self.max_branches = int(max_branches)
+        self.slot_rows = int(slot_rows)
+
+    def _int(self, r):
+        if r < 0:
+            raise FxError(FX_ERR_INVALID_ARG, self._lib.fx_last_error().decode(errors="replace"))
+        return int(r)
+
+    def extend_prefix(self, n: int) -> int:
+        return self._int(self._lib.fx_branch_pool_extend_prefix(self._h, int(n)))
+
+    def fork(self) -> int:
+        return self._int(self._lib.fx_branch_pool_fork(self._h))
+
+    def append(self, branch: int, n: int) -> int:
+        return self._int(self._lib.fx_branch_pool_append(self._h, int(branch), int(n)))
+
+    def release(self, branch: int) -> int:
+        return self._int(self._lib.fx_branch_pool_release(self._h, int(branch)))
+
+    def release_parent(self) -> int:
+        return self._int(self._lib.fx_branch_pool_release_parent(self._h))
+
+    def prefix_refs(self) -> int:
+        return self._int(self._lib.fx_branch_pool_prefix_refs(self._h))
+
+    def prefix_len(self) -> int:
+        return self._int(self._lib.fx_branch_pool_prefix_len(self._h))
+
+    def batch(self):
+        """(ids, suf_start, suf_len, prefix_len) of the live branches, as int32 CPU tensors."""
+        m = self.max_branches
+        arrs = [(ctypes.c_int32 * m)() for _ in range(4)]
+        n = self._int(self._lib.fx_branch_pool_batch(self._h, *arrs))
+        return tuple(torch.tensor(list(a)[:n], dtype=torch.int32) for a in arrs)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.fx_branch_pool_destroy(h)
 
 
 def fx_device_errors(stream=None) -> int:

@@ -279,14 +279,24 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         n_keys = (MODE == kModeFocal) ? l : p.kk + max(0, l - p.tail_lo);
         src.lim_tok = l;
     } else {
-        src.np = p.idx ? p.kk : p.P;
+        // the prefix rows this branch sees: all P, or its fork position
+        int pb = p.P;
+        if (p.pre_len != nullptr) {
+            pb = p.pre_len[b];
+            if (pb < 0 || pb > p.P) {
+                if (tid == 0) flag(p.err, FX_DEVERR_LEN);
+                pb = pb < 0 ? 0 : p.P;
+            }
+        }
+        src.np = p.idx ? p.kk : pb;
+        src.lim_tok = pb;
         const int o0 = p.suf_off[b];
-        const int o1 = p.suf_off[b + 1];
+        const int64_t o1 = p.suf_len != nullptr ? (int64_t)o0 + p.suf_len[b] : (int64_t)p.suf_off[b + 1];
         int L = 0;
         if (o0 < 0 || o1 < o0 || o1 > p.suf_rows) {
             if (tid == 0) flag(p.err, FX_DEVERR_OFFSETS);
         } else {
-            L = o1 - o0;
+            L = (int)(o1 - o0);
             if (L > p.max_suffix) {
                 if (tid == 0) flag(p.err, FX_DEVERR_OFFSETS);
                 L = p.max_suffix;

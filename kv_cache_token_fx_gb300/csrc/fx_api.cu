@@ -628,6 +628,8 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     p.suf_sh = br->suf_stride_h;
     p.suf_st = br->suf_stride_t;
     p.suf_off = br->suf_off;
+    p.suf_len = br->suf_len;
+    p.pre_len = prefix->len;
     p.suf_rows = br->suf_rows;
     p.max_suffix = br->max_suffix;
     p.dr_k = br->draft_k;

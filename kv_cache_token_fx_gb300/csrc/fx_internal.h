@@ -67,6 +67,8 @@ struct AttnParams {
     const uint16_t* suf_v;
     int64_t suf_sh, suf_st;
     const int32_t* suf_off;
+    const int32_t* suf_len;   // [Br] suffix rows (suf_off holds starts), or nullptr (suf_off[b+1] - suf_off[b])
+    const int32_t* pre_len;   // [Br] visible prefix rows (fork positions), or nullptr (all P)
     int suf_rows, max_suffix;
     const uint16_t* dr_k;
     const uint16_t* dr_v;

@@ -384,6 +384,45 @@ def test_shared_prefix_matches_oracle(fx, sparse):
     pu.assert_out_close(out, ref, vmax)
 
 
+@pytest.mark.parametrize("sparse", [False, True])
+def test_forked_branches_from_pool_match_oracle(fx, sparse):
+    """Branches forked from a growing shared prefix (branch pool: fork positions, fixed suffix slots)
+    verified in one fx_shared_prefix_decode call, against the oracle with the same fork positions."""
+    Hkv, G, Mq, slot, cap = 2, 2, 3, 40, 300
+    pool = fx.BranchPool(prefix_cap=cap, max_branches=6, slot_rows=slot)
+    pool.extend_prefix(120)
+    ids = [pool.fork(), pool.fork()]
+    pool.extend_prefix(60)
+    ids.append(pool.fork())
+    pool.extend_prefix(100)
+    ids.append(pool.fork())
+    pool.release(ids[1])                       # a finished branch leaves a hole
+    for b, n in zip((ids[0], ids[2], ids[3]), (25, 0, 40)):
+        if n:
+            pool.append(b, n)
+    live, start, slen, plen = pool.batch()
+    Br = live.numel()
+    P = pool.prefix_len()
+    pk, pv = rnd((Hkv, P, D), 190, 1), rnd((Hkv, P, D), 190, 2)
+    sk, sv = rnd((Hkv, 6 * slot, D), 190, 3), rnd((Hkv, 6 * slot, D), 190, 4)
+    dk, dv = rnd((Br, Mq, Hkv, D), 190, 5), rnd((Br, Mq, Hkv, D), 190, 6)
+    q = rnd((Br, Hkv * G, Mq, D), 190, 7)
+    pidx = None
+    if sparse:
+        # each branch picks 16 prefix positions among the ones it can see
+        g = np.random.default_rng(190)
+        pidx = torch.from_numpy(np.stack([np.stack([np.sort(g.choice(int(plen[b]), 16, replace=False))
+                                                    for _ in range(Hkv)]) for b in range(Br)]).astype(np.int32))
+    ref = oracle.shared_prefix(pk, pv, sk, sv, start, dk, dv, q, pidx, pre_len=plen, suf_len=slen)
+    out = fx.fx_shared_prefix_decode(dev(pk), dev(pv), dev(sk), dev(sv), dev(start), dev(dk), dev(dv), dev(q),
+                                     max_suffix=slot, prefix_idx=dev(pidx) if sparse else None,
+                                     prefix_len=dev(plen), suf_len=dev(slen))
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    vmax = max(float(t.float().abs().max()) for t in (pv, sv, dv))
+    pu.assert_out_close(out, ref, vmax)
+
+
 def test_sparse_long_dense_tail_uses_global_merge(fx):
     """More than 16 x 4096 keys in one row: the splits are merged through the workspace (not inside a
     thread-block cluster)."""
