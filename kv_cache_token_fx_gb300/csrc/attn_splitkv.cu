@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* sQ = smem + 128;                                      // [16][kPitch] bf16
-    unsigned char* sKV = sQ + kQTileBytes;                               // [kWarps][kWarpStages][K, V]
+    unsigned char* sKV = sQ + attn_q_rows(NR) * kPitch;                  // [kWarps][kWarpStages][K, V]
     __shared__ uint32_t s_vmask[kWarps][kWarpStages];   // valid-row bits of each staged sub-tile
 
     const int tid = threadIdx.x;
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     // means "the oldest sub-tile has landed".  No CTA-wide barrier is needed inside the loop.
     unsigned char* wbuf = sKV + (size_t)warp * kWarpBytes;
     // a focal call that only scores (no output rows) needs no V rows and no P V products
-    const bool need_v = !(MODE == kModeFocal && p.no_v);
+    const bool need_v = NR != 32 && !(MODE == kModeFocal && p.no_v);
     auto issue = [&](int j, int mytok) {
         if (j < nsub) {
             const int c16 = lane & 15;
@@ -403,11 +403,29 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     //   NR == 8 (narrow, at most 8 query rows): the keys are the M side.  S^T = K Q^T is 16 keys x 8 rows
     //     (one tile per k-step), O^T = V^T P^T accumulates 128 dims x 8 rows; P^T reaches the B operand
     //     through movmatrix.trans.  24 MMAs per 16 keys -- half the tensor work when few rows exist.
-    constexpr int kOT = NR == 8 ? 8 : 16;   // accumulator tiles of O (wide) / O^T (narrow)
-    constexpr int kQF = NR == 8 ? 2 : 4;    // registers of one k-step's Q fragment
-    int lim[2];
+    //   NR == 32 (scores only: no output rows): keys on M as for 8 rows, with 4 n-tiles of 8 query rows
+    //     sharing every K fragment, so K is read once for up to 32 rows.  32 MMAs per 16 keys, no P V.
+    constexpr int kNT = NR == 32 ? 4 : 1;                       // query n-tiles of the narrow layouts
+    constexpr int kOT = NR == 8 ? 8 : (NR == 32 ? 1 : 16);      // accumulator tiles of O (wide) / O^T (narrow)
+    constexpr int kQF = NR == 16 ? 4 : 2 * kNT;                 // registers of one k-step's Q fragment
+    int lim[2 * kNT];
     uint32_t qf[8][kQF];
-    if constexpr (NR == 8) {
+    if constexpr (NR == 32) {
+        // n-tile nt, column qc: query row 8*nt + 2*t4 + qc
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+            lim[2 * nt] = row_limit(r0 + 8 * nt + 2 * t4);
+            lim[2 * nt + 1] = row_limit(r0 + 8 * nt + 2 * t4 + 1);
+        }
+        const int qrow = lane & 7;
+        const int qcol = 8 * (lane >> 3);
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int kp = 0; kp < 4; ++kp)
+                ldsm_x4(smem_addr(sQ + (8 * nt + qrow) * kPitch + (32 * kp + qcol) * 2), qf[2 * kp][2 * nt],
+                        qf[2 * kp][2 * nt + 1], qf[2 * kp + 1][2 * nt], qf[2 * kp + 1][2 * nt + 1]);
+    } else if constexpr (NR == 8) {
         // this thread's accumulator columns are query rows 2*t4 and 2*t4 + 1
         lim[0] = row_limit(r0 + 2 * t4);
         lim[1] = row_limit(r0 + 2 * t4 + 1);
@@ -435,8 +453,12 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     for (int n = 0; n < kOT; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};   // per accumulator row (wide) / query column (narrow)
-    float l_run[2] = {0.f, 0.f};
+    float m_run[2 * kNT], l_run[2 * kNT];      // per accumulator row (wide) / query column (narrow)
+#pragma unroll
+    for (int i = 0; i < 2 * kNT; ++i) {
+        m_run[i] = -INFINITY;
+        l_run[i] = 0.f;
+    }
     for (int j = 0; j < nsub; ++j) {
         const int base = ws + j * kSub;   // first key of this sub-tile
         const int tnext = src.token(base + kWarpStages * kSub + (lane & 15));   // for the refill below
@@ -446,7 +468,59 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         const unsigned char* sv = sk + kSub * kPitch;
         const uint32_t vmask = s_vmask[warp][j % kWarpStages];
 
-        if constexpr (NR == 8) {
+        if constexpr (NR == 32) {
+            // S^T = K Q^T for 4 n-tiles of 8 query rows; each K fragment serves all four
+            float acc[kNT][4];
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            {
+                const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int kcol = 8 * (lane >> 4);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(smem_addr(sk + krow * kPitch + (16 * ks + kcol) * 2), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < kNT; ++nt) mma_bf16(acc[nt], a0, a1, a2, a3, qf[ks][2 * nt], qf[ks][2 * nt + 1]);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+                // element e: key g + 8*(e >> 1) of the sub-tile, query row 8*nt + 2*t4 + (e & 1)
+                float x[4];
+                float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kr = g + 8 * (e >> 1);
+                    const int qc = e & 1;
+                    const bool ok = ((vmask >> kr) & 1u) && base + kr <= lim[2 * nt + qc];
+                    x[e] = ok ? acc[nt][e] * p.qscale : -INFINITY;
+                    mx[qc] = fmaxf(mx[qc], x[e]);
+                }
+                if (p.logits != nullptr) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = r0 + 8 * nt + 2 * t4 + (e & 1);
+                        const int pos = base + g + 8 * (e >> 1);
+                        if (row < p.R && pos < we) p.logits[(int64_t)(bh * p.R + row) * p.Tcap + pos] = x[e];
+                    }
+                }
+#pragma unroll
+                for (int qc = 0; qc < 2; ++qc) {   // max over the 16 keys: the 8 lanes of this t4
+                    mx[qc] = fmaxf(mx[qc], __shfl_xor_sync(kFull, mx[qc], 4));
+                    mx[qc] = fmaxf(mx[qc], __shfl_xor_sync(kFull, mx[qc], 8));
+                    mx[qc] = fmaxf(mx[qc], __shfl_xor_sync(kFull, mx[qc], 16));
+                    const float mn = fmaxf(m_run[2 * nt + qc], mx[qc]);
+                    const float ms = (mn == -INFINITY) ? 0.f : mn;
+                    l_run[2 * nt + qc] *= fast_exp2(m_run[2 * nt + qc] - ms);
+                    m_run[2 * nt + qc] = mn;
+#pragma unroll
+                    for (int e = qc; e < 4; e += 2) l_run[2 * nt + qc] += fast_exp2(x[e] - ms);
+                }
+            }
+        } else if constexpr (NR == 8) {
             // S^T = K Q^T: 16 keys x 8 rows; two accumulators (even / odd k-steps) for independent chains
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
             {
@@ -627,10 +701,27 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 
     // ---- combine the warps into this CTA's partial (the stage buffers are free now) -------------
     const int nr = min(NR, p.R - r0);   // rows of this group that exist
-    __shared__ float sm_m[kWarps][kRowsPerCta];
-    __shared__ float sm_l[kWarps][kRowsPerCta];
+    __shared__ float sm_m[kWarps][kMaxRowsPerCta];
+    __shared__ float sm_l[kWarps][kMaxRowsPerCta];
     float* sm_o = reinterpret_cast<float*>(sKV);   // [kWarps][16][128]
-    if constexpr (NR == 8) {
+    if constexpr (NR == 32) {
+#pragma unroll
+        for (int i = 0; i < 2 * kNT; ++i) {   // sums over the 16 keys: the 8 lanes of this t4
+            l_run[i] += __shfl_xor_sync(kFull, l_run[i], 4);
+            l_run[i] += __shfl_xor_sync(kFull, l_run[i], 8);
+            l_run[i] += __shfl_xor_sync(kFull, l_run[i], 16);
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int i = 0; i < 2 * kNT; ++i) {
+                const int r = 8 * (i >> 1) + 2 * t4 + (i & 1);
+                if (r < nr) {
+                    sm_m[warp][r] = m_run[i];
+                    sm_l[warp][r] = l_run[i];
+                }
+            }
+        }
+    } else if constexpr (NR == 8) {
 #pragma unroll
         for (int qc = 0; qc < 2; ++qc) {   // sums over the 16 keys: the 8 lanes of this t4
             l_run[qc] += __shfl_xor_sync(kFull, l_run[qc], 4);
@@ -676,9 +767,23 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
     __syncthreads();
 
-    __shared__ float c_m[kRowsPerCta];
-    __shared__ float c_l[kRowsPerCta];
+    __shared__ float c_m[kMaxRowsPerCta];
+    __shared__ float c_l[kMaxRowsPerCta];
     float* c_o = sm_o;   // [16][128]: combined in place over warp 0's slice (each element by its own thread)
+    if (!need_v) {
+        // scores only: the row maxima and sums are all that is merged
+        for (int r = tid; r < nr; r += kThreads) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][r]);
+            const float Ms = (M == -INFINITY) ? 0.f : M;
+            float Ls = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) Ls = fmaf(sm_l[w][r], fast_exp2(sm_m[w][r] - Ms), Ls);
+            c_m[r] = M;
+            c_l[r] = Ls;
+        }
+    } else
     for (int e = tid; e < nr * kHeadDim; e += kThreads) {
         const int r = e >> 7;
         const int c = e & (kHeadDim - 1);
@@ -801,7 +906,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     __syncthreads();
     for (int r = 0; r < nr; ++r) {
         const int64_t pi = (int64_t)(bh * p.R + r0 + r) * p.nsplit + split;
-        for (int c = tid; c < kHeadDim; c += kThreads) p.part_o[pi * kHeadDim + c] = c_o[r * kHeadDim + c];
+        if (need_v)
+            for (int c = tid; c < kHeadDim; c += kThreads) p.part_o[pi * kHeadDim + c] = c_o[r * kHeadDim + c];
         if (tid == 0) {
             p.part_m[pi] = c_m[r];
             p.part_l[pi] = c_l[r];
@@ -908,7 +1014,7 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
     const bool cluster = MERGE != kMergeWorkspace;
     if (configured != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_smem_bytes());
+                                             (int)attn_smem_bytes(NR));
         if (e != cudaSuccess) return e;
         if (cluster) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -916,7 +1022,7 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
         }
         configured = dev;
     }
-    const size_t smem = attn_smem_bytes();
+    const size_t smem = attn_smem_bytes(NR);
     dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
     // merged in a cluster: every split of one (b, h, row group) is one CTA of a (1, nsplit, 1) cluster
     return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, cluster ? (unsigned)p.nsplit : 0u, p);
@@ -940,6 +1046,9 @@ cudaError_t launch_rows(const AttnParams& p, bool pdl, cudaStream_t s)
 template <int MODE>
 cudaError_t launch_mode(const AttnParams& p, bool pdl, cudaStream_t s)
 {
+    if constexpr (MODE == kModeFocal) {
+        if (p.rb == 32) return p.no_v ? launch_rows<MODE, 32>(p, pdl, s) : cudaErrorInvalidValue;
+    }
     return p.rb == 8 ? launch_rows<MODE, 8>(p, pdl, s) : launch_rows<MODE, 16>(p, pdl, s);
 }
 
@@ -947,7 +1056,7 @@ cudaError_t launch_mode(const AttnParams& p, bool pdl, cudaStream_t s)
 
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s)
 {
-    if (p.rb != 8 && p.rb != 16) return cudaErrorInvalidValue;
+    if (p.rb != 8 && p.rb != 16 && p.rb != 32) return cudaErrorInvalidValue;
     if (mode == kModeFocal) return launch_mode<kModeFocal>(p, pdl, s);
     if (mode == kModeSparse) return launch_mode<kModeSparse>(p, pdl, s);
     return launch_mode<kModePrefix>(p, pdl, s);

@@ -88,10 +88,11 @@ struct Plan {
 // (sparse and prefix calls), which needs at most kMaxClusterSplits splits.  Gathered modes also keep
 // each split within kMaxSplitTokens keys (the index table lives in shared memory).  Small calls get
 // about two CTAs per SM in a single wave; large ones at least four full waves.
-Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_cluster = false, bool gathered = false)
+Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_cluster = false, bool gathered = false,
+               bool scores_only = false)
 {
     Plan pl;
-    pl.rb = rows_per_block(R);
+    pl.rb = rows_per_block(R, scores_only);
     pl.nrg = cdiv(R, pl.rb);
     const int keys = max_keys > 0 ? max_keys : 1;
     const int per_split = pairs * pl.nrg;
@@ -227,8 +228,10 @@ size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap)
 {
     if (B < 1 || Hkv < 1 || Hq < Hkv || Mq < 1 || Tcap < 0) return 0;
     const int R = (Hq / Hkv) * Mq;
+    // enough for both plans: with output rows, and scores only (which may use wider row groups)
     const Plan pl = make_plan(B * Hkv, R, Tcap, sm_count_or_default());
-    return make_layout(B * Hkv, R, pl, Tcap, false).total;
+    const Plan ps = make_plan(B * Hkv, R, Tcap, sm_count_or_default(), false, false, true);
+    return std::max(make_layout(B * Hkv, R, pl, Tcap, false).total, make_layout(B * Hkv, R, ps, Tcap, false).total);
 }
 
 fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,
@@ -251,7 +254,7 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     const int pairs = kv->B * kv->Hkv;
     const int G = Hq / kv->Hkv;
     const int R = G * Mq;
-    const Plan pl = make_plan(pairs, R, kv->Tcap, ds->sm_count);
+    const Plan pl = make_plan(pairs, R, kv->Tcap, ds->sm_count, false, false, out == nullptr);
     const Layout L = make_layout(pairs, R, pl, kv->Tcap, false);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
     if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");

@@ -20,7 +20,6 @@ constexpr int kWarpStages = 3;                          // sub-tiles in flight p
 constexpr int kRowsPerCta = 16;                         // query rows per CTA: one m16 MMA tile
 constexpr int kPitch = kRowBytes + 16;                  // staged row pitch: the 16-byte pad puts the 8
                                                         // rows of an ldmatrix on 8 distinct bank groups
-constexpr int kQTileBytes = kRowsPerCta * kPitch;       // bf16 query tile
 constexpr int kSubBytes = 2 * kSub * kPitch;            // K and V rows of one sub-tile (8.5 KB)
 constexpr int kWarpBytes = kWarpStages * kSubBytes;     // one warp's ring of sub-tile buffers
 constexpr int kTile = kWarps * kSub;                    // split lengths are multiples of this (whole sub-tiles per warp)
@@ -35,8 +34,11 @@ constexpr int kResidentPerSm = 2;                       // attention CTAs that f
 constexpr size_t kCounterSlots = 65536u * 4u;
 constexpr size_t kCounterBytes = kCounterSlots * sizeof(unsigned);
 
+constexpr int kMaxRowsPerCta = 32;                      // query rows of the widest (scores-only) CTA
+// Query-tile rows held in shared memory for a CTA of nr rows (16 at least: the 16-row MMA tile).
+__host__ __device__ constexpr int attn_q_rows(int nr) { return nr > kRowsPerCta ? nr : kRowsPerCta; }
 // Dynamic shared memory of one attention CTA: the query tile and each warp's ring of sub-tile buffers.
-inline size_t attn_smem_bytes() { return 128 + (size_t)kQTileBytes + (size_t)kWarps * kWarpBytes; }
+inline size_t attn_smem_bytes(int nr) { return 128 + (size_t)attn_q_rows(nr) * kPitch + (size_t)kWarps * kWarpBytes; }
 
 // Which key sequence an attention CTA walks.
 enum AttnMode : int {
@@ -220,7 +222,13 @@ __device__ __forceinline__ void cluster_wait_acquire()
 }
 #endif
 
-// Query rows per attention CTA: 8 (keys on the MMA's M side) when at most 8 rows exist, else 16.
-inline int rows_per_block(int R) { return R <= 8 ? 8 : kRowsPerCta; }
+// Query rows per attention CTA: 8 (keys on the MMA's M side) when at most 8 rows exist; for calls that
+// only score (no output rows) and have more than 16 rows, 32 (keys on M, four query n-tiles); else 16.
+inline int rows_per_block(int R, bool scores_only = false)
+{
+    if (R <= 8) return 8;
+    if (scores_only && R > kRowsPerCta) return 32;
+    return kRowsPerCta;
+}
 
 }  // namespace fx

@@ -91,6 +91,22 @@ def test_focal_strided_cache(fx):
     pu.assert_scores_close(sc, ref_sc)
 
 
+@pytest.mark.parametrize("G,Mq,q_pos0", [(4, 8, 690), (2, 12, 650), (8, 6, -1), (2, 4, 690), (4, 3, -1)])
+def test_focal_scores_only_matches_oracle(fx, G, Mq, q_pos0):
+    """Scoring-only focal calls (no output rows: V is not read; more than 16 rows use the 32-row
+    layout) give the oracle's importance scores."""
+    B, Hkv, T = 3, 2, 700
+    k, v = kv_case(B, Hkv, T, 40 + G * Mq)
+    q = rnd((B, Hkv * G, Mq, D), 41 + G * Mq, 3)
+    length = torch.tensor([700, 523, 64], dtype=torch.int32)
+    cand = (5, 600)
+    _, ref_sc = oracle.focal(k, v, length, q, q_pos0=q_pos0, cand=cand, want_out=False)
+    _, sc = fx.fx_focal_attn_scores(dev(k), dev(v), dev(length), dev(q), q_pos0=q_pos0, cand=cand, want_out=False)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    pu.assert_scores_close(sc, ref_sc)
+
+
 # ----------------------------------------------------------------------------------------------
 def _quantised_scores(rows, n, seed, levels):
     g = np.random.default_rng(seed)
