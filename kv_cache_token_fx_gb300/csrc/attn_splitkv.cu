@@ -208,6 +208,26 @@ struct KeySource {
 };
 
 // ---- the kernel -----------------------------------------------------------------------------------
+// Output value of column c of row `row` of this (b, h) from the split-merged (M, and Ls, O relative to
+// Ms).  A partial over other keys of the row computed by another kernel (ext: the dense shared prefix of
+// the verify call) is folded in first.
+__device__ __forceinline__ float finish_row(const AttnParams& p, int b, int h, int row, int c, float M, float Ms,
+                                            float Ls, float O)
+{
+    if (p.ext_m != nullptr) {
+        const int64_t er = ((int64_t)h * p.B + b) * p.R + row;
+        const float me = p.ext_m[er];
+        if (me != -INFINITY) {
+            const float mn = fmaxf(M, me);
+            const float a = M == -INFINITY ? 0.f : fast_exp2(Ms - mn);
+            const float e = fast_exp2(me - mn);
+            Ls = fmaf(Ls, a, p.ext_l[er] * e);
+            O = fmaf(O, a, p.ext_o[er * kHeadDim + c] * e);
+        }
+    }
+    return Ls > 0.f ? O / Ls : 0.f;
+}
+
 // How the splits of one (b, h, row group) are merged.
 enum Merge {
     kMergeWorkspace = 0,   // partials through the workspace; the last-arriving CTA merges
@@ -855,7 +875,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             const int row = r0 + r;
             const int gi = row / p.Mq;
             const int i = row - gi * p.Mq;
-            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = Ls > 0.f ? O / Ls : 0.f;
+            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = finish_row(p, b, h, row, c, M, Ms, Ls, O);
         }
         return;
     }
@@ -897,7 +917,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             const int row = r0 + r;
             const int gi = row / p.Mq;
             const int i = row - gi * p.Mq;
-            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = Ls > 0.f ? O / Ls : 0.f;
+            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = finish_row(p, b, h, row, c, M, Ms, Ls, O);
         }
         cluster_sync();   // keep every CTA's shared memory alive until all reads are done
         return;
@@ -943,7 +963,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 Ls = fmaf(__ldcg(p.part_l + base + s), sc, Ls);
                 O = fmaf(__ldcg(p.part_o + (base + s) * kHeadDim + c), sc, O);
             }
-            orow[c] = Ls > 0.f ? O / Ls : 0.f;
+            orow[c] = finish_row(p, b, h, row, c, M, Ms, Ls, O);
         }
     }
     if (tid == 0) p.counters[bh * p.nrg + rg] = 0u;

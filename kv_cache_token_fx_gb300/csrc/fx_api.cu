@@ -553,13 +553,23 @@ fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer,
 }
 
 // ---------------------------------------------------------------------------------------------
+// The dense prefix runs on the tensor cores (its own kernel, partials folded into the verify merge)
+// when it fills at least one 128-row by 128-key tile.
+bool prefix_on_tensor_cores(bool dense, int P, int Br, int R) { return dense && P >= 128 && (int64_t)Br * R >= 128; }
+
+size_t prefix_ext_bytes(int Br, int Hkv, int R) { return round_up((size_t)Hkv * Br * R * (2 + kHeadDim) * sizeof(float)); }
+
 size_t fx_shared_prefix_workspace_bytes(int Br, int Hkv, int Hq, int Mq, int np, int max_suffix)
 {
     if (Br < 1 || Hkv < 1 || Hq < Hkv || Mq < 1 || np < 0 || max_suffix < 0) return 0;
     const int R = (Hq / Hkv) * Mq;
-    const int max_keys = np + max_suffix + Mq;
-    const Plan pl = make_plan(Br * Hkv, R, max_keys, sm_count_or_default(), true, np > 0);
-    return make_layout(Br * Hkv, R, pl, 0, true).total;
+    const Plan pl = make_plan(Br * Hkv, R, np + max_suffix + Mq, sm_count_or_default(), true, np > 0);
+    size_t need = make_layout(Br * Hkv, R, pl, 0, true).total;
+    if (prefix_on_tensor_cores(true, np, Br, R)) {   // a dense prefix of np rows may take that route
+        const Plan pt = make_plan(Br * Hkv, R, max_suffix + Mq, sm_count_or_default(), true, false);
+        need = std::max(need, make_layout(Br * Hkv, R, pt, 0, true).total + prefix_ext_bytes(Br, Hkv, R));
+    }
+    return need;
 }
 
 fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_desc* br,
@@ -598,12 +608,15 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     const int pairs = br->Br * Hkv;
     const int G = Hq / Hkv;
     const int R = G * br->Mq;
-    const int np = prefix_idx ? kp : prefix->P;
+    const bool tc = prefix_on_tensor_cores(prefix_idx == nullptr, prefix->P, br->Br, R);
+    const int np = prefix_idx ? kp : (tc ? 0 : prefix->P);
     const int max_keys = np + br->max_suffix + br->Mq;
     const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true, prefix_idx != nullptr);
     const Layout L = make_layout(pairs, R, pl, 0, true);
-    if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
+    const size_t ext_off = L.total;
+    if ((st = check_ws(ws, ws_bytes, L.total + (tc ? prefix_ext_bytes(br->Br, Hkv, R) : 0))) != FX_OK) return st;
     if (pairs > 65535 || pl.nsplit > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
+    if (tc && (int64_t)br->Br * R / 128 + 1 > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
 
     char* w = static_cast<char*>(ws);
     AttnParams p;
@@ -651,9 +664,46 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
     p.counters = reinterpret_cast<unsigned*>(w + L.counters);
     p.out = out;
     p.err = ds->err;
-    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+    bool pdl = (flags & FX_LAUNCH_PDL) != 0;
     p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
-    cudaError_t e = launch_attn_partial(p, kModePrefix, pdl, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tc) {
+        // the dense prefix of every branch on the tensor cores first; the verify kernel then covers the
+        // suffix and draft keys and folds the prefix partials into its merge
+        float* ext = reinterpret_cast<float*>(w + ext_off);
+        const size_t nrows = (size_t)Hkv * br->Br * R;
+        PrefixTcParams t;
+        t.pk = reinterpret_cast<const uint16_t*>(prefix->k);
+        t.pv = reinterpret_cast<const uint16_t*>(prefix->v);
+        t.p_sh = prefix->stride_h;
+        t.p_st = prefix->stride_t;
+        t.P = prefix->P;
+        t.pre_len = prefix->len;
+        t.q = reinterpret_cast<const uint16_t*>(q);
+        t.Br = br->Br;
+        t.Hkv = Hkv;
+        t.Hq = Hq;
+        t.G = G;
+        t.Mq = br->Mq;
+        t.R = R;
+        t.qscale = p.qscale;
+        t.ext_o = ext;   // first: its rows are stored as 16-byte vectors
+        t.ext_m = ext + nrows * kHeadDim;
+        t.ext_l = t.ext_m + nrows;
+        t.err = ds->err;
+        cudaError_t e = launch_prefix_tc(t, pdl, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefix launch");
+        p.P = 0;
+        p.pre_len = nullptr;
+        p.ext_m = t.ext_m;
+        p.ext_l = t.ext_l;
+        p.ext_o = t.ext_o;
+        // the verify kernel's own inputs were all written before this call, so it may read them while
+        // the prefix kernel runs (every kernel here triggers only after its own dependency wait)
+        pdl = true;
+        p.prefetch = 1;
+    }
+    cudaError_t e = launch_attn_partial(p, kModePrefix, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e, "shared-prefix decode launch");
     return FX_OK;
 }

@@ -71,6 +71,11 @@ struct AttnParams {
     const int32_t* suf_off;
     const int32_t* suf_len;   // [Br] suffix rows (suf_off holds starts), or nullptr (suf_off[b+1] - suf_off[b])
     const int32_t* pre_len;   // [Br] visible prefix rows (fork positions), or nullptr (all P)
+    // prefix mode: the dense prefix's partial (m, l, O) per row, computed by the tensor-core prefix
+    // kernel ([Hkv][Br][R] rows) and folded into the final merge; nullptr when the prefix is in the keys
+    const float* ext_m;
+    const float* ext_l;
+    const float* ext_o;
     int suf_rows, max_suffix;
     const uint16_t* dr_k;
     const uint16_t* dr_v;
@@ -100,6 +105,22 @@ struct FocalCombineParams {
     int cand_lo, cand_hi;
     float* out;
     float* scores;
+    unsigned* err;
+};
+
+// Dense shared prefix on the tensor cores: the partial (m, l, O) of every (KV head, branch, row).
+struct PrefixTcParams {
+    const uint16_t* pk;
+    const uint16_t* pv;
+    int64_t p_sh, p_st;
+    int P;
+    const int32_t* pre_len;   // [Br] fork positions or nullptr
+    const uint16_t* q;        // [Br, Hq, Mq, 128]
+    int Br, Hkv, Hq, G, Mq, R;
+    float qscale;
+    float* ext_m;             // [Hkv][Br][R]
+    float* ext_l;
+    float* ext_o;             // [Hkv][Br][R][128]
     unsigned* err;
 };
 
@@ -136,6 +157,7 @@ fx_status set_error(fx_status st, const char* msg);
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s);
+cudaError_t launch_prefix_tc(const PrefixTcParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_mass(const float* scores, int rows, int n, float inv_r, int accumulate, float* mass,
                               bool pdl, cudaStream_t s);
 cudaError_t launch_compact(const CompactParams& p, bool pdl, cudaStream_t s);

@@ -439,6 +439,30 @@ def test_forked_branches_from_pool_match_oracle(fx, sparse):
     pu.assert_out_close(out, ref, vmax)
 
 
+@pytest.mark.parametrize("fork", [False, True])
+def test_dense_prefix_on_tensor_cores_matches_oracle(fx, fork):
+    """A dense prefix of at least one 128-key tile with at least 128 query rows per KV head takes the
+    tensor-core route (S = Q K^T and O = P V per 128 x 128 tile, partials folded into the verify
+    merge): 168 rows (one full and one ragged row tile), 700 prefix keys (a ragged last key tile), and
+    with fork positions 0, 1, 127, 128, 129, 640 and 700 (empty, one key, both sides of a tile edge)."""
+    Hkv, G, Mq, Br, P = 2, 2, 7, 12, 700
+    lens = [3, 0, 9, 1, 0, 12, 5, 7, 2, 0, 4, 6]
+    off = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    S = int(off[-1])
+    pk, pv = rnd((Hkv, P, D), 75, 1), rnd((Hkv, P, D), 75, 2)
+    sk, sv = rnd((Hkv, S, D), 75, 3), rnd((Hkv, S, D), 75, 4)
+    dk, dv = rnd((Br, Mq, Hkv, D), 75, 5), rnd((Br, Mq, Hkv, D), 75, 6)
+    q = rnd((Br, Hkv * G, Mq, D), 75, 7)
+    plen = torch.tensor([0, 1, 127, 128, 129, 640, 700, 700, 3, 255, 256, 511], dtype=torch.int32) if fork else None
+    ref = oracle.shared_prefix(pk, pv, sk, sv, off, dk, dv, q, None, pre_len=plen)
+    out = fx.fx_shared_prefix_decode(dev(pk), dev(pv), dev(sk), dev(sv), dev(off), dev(dk), dev(dv), dev(q),
+                                     max_suffix=16, prefix_len=dev(plen) if fork else None)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    vmax = max(float(t.float().abs().max()) for t in (pv, sv, dv))
+    pu.assert_out_close(out, ref, vmax)
+
+
 def test_sparse_long_dense_tail_uses_global_merge(fx):
     """More than 16 x 4096 keys in one row: the splits are merged through the workspace (not inside a
     thread-block cluster)."""
