@@ -284,11 +284,11 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     // this warp's contiguous share of the split (the host makes split_len a multiple of kWarps * kSub),
     // and the index loads of its first sub-tiles, issued before the length is known
     const int s0 = split * p.split_len;
-    const int wl = p.split_len / kWarps;
-    const int ws = s0 + warp * wl;
+    int wl = p.split_len / kWarps;
+    int ws = s0 + warp * wl;
     int tpre[kWarpStages];
 #pragma unroll
-    for (int j = 0; j < kWarpStages; ++j) tpre[j] = src.token(ws + j * kSub + (lane & 15));
+    for (int j = 0; j < kWarpStages; ++j) tpre[j] = MODE == kModePrefix ? 0 : src.token(ws + j * kSub + (lane & 15));
 
     if (MODE == kModeFocal || MODE == kModeSparse) {
         int l = p.len[b];
@@ -332,6 +332,15 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         n_keys = src.np + L + p.Mq;
     }
     const int s1 = min(n_keys, s0 + p.split_len);
+    if (MODE == kModePrefix) {
+        // verify rows differ in length (private suffixes): the warps share this split's actual keys, so
+        // a short row does not leave most of them idle
+        const int share = (max(0, s1 - s0) + kWarps * kSub - 1) / (kWarps * kSub) * kSub;
+        wl = share;
+        ws = s0 + warp * share;
+#pragma unroll
+        for (int j = 0; j < kWarpStages; ++j) tpre[j] = src.token(ws + j * kSub + (lane & 15));
+    }
     const int we = min(s1, ws + wl);
     const int nsub = we > ws ? (we - ws + kSub - 1) / kSub : 0;
 

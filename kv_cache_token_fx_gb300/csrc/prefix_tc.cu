@@ -6,9 +6,9 @@
 // a real matrix product, which this kernel runs as 128 x 128 tiles on the tensor cores:
 //   S = Q K^T       (M = 128 query rows, N = 128 prefix keys, K = 128 dims)        -> tensor memory
 //   O += P V        (M = 128 query rows, N = 128 dims, K = 128 prefix keys)        -> tensor memory
-// with P = exp2(S - m) from the exact row maximum m (a first pass over the prefix computes only S and
-// the maxima, so O never needs rescaling), P split into bf16 hi + lo parts (two products) so the
-// probabilities keep about 16 bits.  One thread owns one query row: it reads its S row from tensor
+// in one pass with an online softmax (P = exp2(S - m) against a running maximum m that moves only by
+// more than a fixed slack, so O is rescaled rarely), P split into bf16 hi + lo parts (two products) so
+// the probabilities keep about 16 bits.  One thread owns one query row: it reads its S row from tensor
 // memory, forms P, and writes it to shared memory as the next product's A operand.  Operand tiles are
 // K-major with the 128-byte swizzle; V is transposed into that layout through ldmatrix / stmatrix.trans.
 // The result per row is a partial (m, l, O) over the prefix, which the verify kernel folds into its
@@ -27,6 +27,7 @@ constexpr int kTcThreads = 128;
 constexpr int kTileBytes = kTcRows * kHeadDim * 2;  // one 128 x 128 bf16 operand tile
 constexpr int kVsPitch = 272;                      // V staging row pitch: conflict-free ldmatrix
 constexpr int kTmemCols = 256;                     // S in columns 0..127, O in 128..255
+constexpr float kRescale = 8.f;                    // running-maximum slack (log2 units) before O is rescaled
 // [Q | K | V^T | P_hi | P_lo] swizzled tiles, the V staging rows, and slack to align to 1024 bytes
 constexpr size_t kTcSmem = 5 * (size_t)kTileBytes + (size_t)kTcKeys * kVsPitch + 1024;
 
@@ -112,6 +113,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
 }
 
+// Store 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(addr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp16(uint32_t dst, const void* src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
@@ -150,7 +171,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     unsigned char* sPh = base + 3 * kTileBytes;
     unsigned char* sPl = base + 4 * kTileBytes;
     unsigned char* sVs = base + 5 * kTileBytes;
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bar_s;   // S = Q K^T of the current tile is in tensor memory
+    __shared__ __align__(8) uint64_t bar_o;   // O += P V of the previous tile is done
     __shared__ uint32_t s_tmem;
     __shared__ int s_lim_max;
 
@@ -181,7 +203,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     }
     if (tid == 0) {
         s_lim_max = 0;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_o)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -210,8 +233,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     const int ntiles = (s_lim_max + kTcKeys - 1) / kTcKeys;
     const uint16_t* kb = p.pk + (int64_t)h * p.p_sh;
     const uint16_t* vb = p.pv + (int64_t)h * p.p_sh;
-    unsigned phase = 0;
 
+    // K rows into the swizzled K tile, V rows into the staging rows; keys past P are zero
     auto load_k = [&](int j0) {
         for (int e = tid; e < kTcKeys * 16; e += kTcThreads) {
             const int key = e >> 4;
@@ -222,6 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
             else
                 *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
     auto load_v = [&](int j0) {
         for (int e = tid; e < kTcKeys * 16; e += kTcThreads) {
@@ -233,40 +257,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
             else
                 *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
-    // ---- pass 1: the exact maximum of each row's scaled logits over its visible prefix ---------------
+    // One pass over the prefix with an online softmax.  A row's running maximum m moves only when a
+    // tile's maximum exceeds it by more than kRescale (log2 units): O in tensor memory is then rescaled
+    // by the row's own thread (read, scale, write back), which happens a few times per row at most, and
+    // P = exp2(s - m) stays below 2^kRescale.  The next tile's K and V rows are in flight while this
+    // tile's softmax and P V run.
     float m = -INFINITY;
+    float l = 0.f;
+    unsigned ph_s = 0, ph_o = 0;
+    if (ntiles > 0) {
+        load_k(0);
+        load_v(0);
+    }
     for (int t = 0; t < ntiles; ++t) {
         const int j0 = t * kTcKeys;
-        load_k(j0);
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");   // K of this tile landed
         publish_to_tensor_core();
         if (tid == 0) {
             mma_tile(tmem_s, smem_addr(sQ), smem_addr(sK), false);
-            mma_commit(&bar);
+            mma_commit(&bar_s);
         }
-        mma_wait(&bar, phase, p.err);
-#pragma unroll
-        for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem_s + lane_base + c0, v);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                if (j0 + c0 + jj < lim) m = fmaxf(m, v[jj] * p.qscale);
-        }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();   // S read by every lane before the next product overwrites it
-    }
-
-    // ---- pass 2: P = exp2(S - m), l += sum P, O += P V ------------------------------------------------
-    const float ms = (m == -INFINITY) ? 0.f : m;
-    float l = 0.f;
-    for (int t = 0; t < ntiles; ++t) {
-        const int j0 = t * kTcKeys;
-        load_k(j0);
-        load_v(j0);
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");   // V of this tile landed
+        if (t > 0) mma_wait(&bar_o, ph_o, p.err);               // previous P V done: V^T, P tiles and O free
         __syncthreads();
         // V (keys x dims, staged row-major) -> V^T (dims x keys) in the swizzled K-major layout:
         // 8 x 8 blocks through ldmatrix and stmatrix.trans; warp w owns keys 32w .. 32w+31
@@ -290,12 +305,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
                 }
             }
         }
-        publish_to_tensor_core();
-        if (tid == 0) {
-            mma_tile(tmem_s, smem_addr(sQ), smem_addr(sK), false);
-            mma_commit(&bar);
+        mma_wait(&bar_s, ph_s, p.err);   // S of this tile in tensor memory; the K tile is consumed
+        __syncthreads();                 // and every warp is done with the V staging rows
+        if (t + 1 < ntiles) {
+            load_k(j0 + kTcKeys);
+            load_v(j0 + kTcKeys);
         }
-        mma_wait(&bar, phase, p.err);
+
+        // the row's maximum over this tile, and the rescale of O when the running maximum moves
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem_s + lane_base + c0, v);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+                if (j0 + c0 + jj < lim) mt = fmaxf(mt, v[jj] * p.qscale);
+        }
+        const bool grow = mt > m + kRescale;   // also when m is still -inf and the tile has keys
+        const float mnew = grow ? mt : m;
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {   // tensor-memory access is warp-wide
+            const float a = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_approx(m - mnew));
+#pragma unroll
+            for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem_o + lane_base + c0, v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) v[c] *= a;
+                tmem_st32(tmem_o + lane_base + c0, v);
+            }
+            l *= a;
+        }
+        m = mnew;
+        const float ms = (m == -INFINITY) ? 0.f : m;
+
+        // P = exp2(S - m) as bf16 hi + lo into the two P tiles, l += sum P
 #pragma unroll
         for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
             float v[32];
@@ -321,14 +365,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
                 *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        publish_to_tensor_core();
+        publish_to_tensor_core();   // also: every thread has read S before the next tile overwrites it
         if (tid == 0) {
             mma_tile(tmem_o, smem_addr(sPh), smem_addr(sVt), t > 0);
             mma_tile(tmem_o, smem_addr(sPl), smem_addr(sVt), true);
-            mma_commit(&bar);
+            mma_commit(&bar_o);
         }
-        mma_wait(&bar, phase, p.err);   // the tiles are reused by the next round
     }
+    if (ntiles > 0) mma_wait(&bar_o, ph_o, p.err);
 
     // ---- the partial of this row over the prefix (the loads are warp-wide: every lane takes part) -----
     const int64_t er = ((int64_t)h * p.Br + b) * p.R + r;
