@@ -8,8 +8,9 @@
 //   O += P V        (M = 128 query rows, N = 128 dims, K = 128 prefix keys)        -> tensor memory
 // in one pass with an online softmax (P = exp2(S - m) against a running maximum m that moves only by
 // more than a fixed slack, so O is rescaled rarely), P split into bf16 hi + lo parts (two products) so
-// the probabilities keep about 16 bits.  One thread owns one query row: it reads its S row from tensor
-// memory, forms P, and writes it to shared memory as the next product's A operand.  Operand tiles are
+// the probabilities keep about 16 bits.  Two threads own one query row, each for half of
+// the keys of a tile and half of O: they read their S columns from tensor memory, trade the row
+// maximum, form P, and write it to shared memory as the next product's A operand.  Operand tiles are
 // K-major with the 128-byte swizzle; V is transposed into that layout through ldmatrix / stmatrix.trans.
 // The result per row is a partial (m, l, O) over the prefix, which the verify kernel folds into its
 // merge of the suffix and draft keys.
@@ -23,7 +24,7 @@ namespace {
 
 constexpr int kTcRows = 128;                       // query rows per CTA (one tensor-memory lane each)
 constexpr int kTcKeys = 128;                       // prefix keys per tile
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;                   // two threads per query row
 constexpr int kTileBytes = kTcRows * kHeadDim * 2;  // one 128 x 128 bf16 operand tile
 constexpr int kVsPitch = 272;                      // V staging row pitch: conflict-free ldmatrix
 constexpr int kTmemCols = 256;                     // S in columns 0..127, O in 128..255
@@ -175,13 +176,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     __shared__ __align__(8) uint64_t bar_o;   // O += P V of the previous tile is done
     __shared__ uint32_t s_tmem;
     __shared__ int s_lim_max;
+    __shared__ float s_xch[kTcThreads];       // the two halves of a row trade their maxima / sums
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const int lrow = tid & (kTcRows - 1);     // query row within the tile = tensor-memory lane
+    const int half = tid >> 7;                // this thread's 64 keys of each tile and 64 dims of O
+    const int col0 = half * 64;
     const int h = blockIdx.y;
     const int rows_total = p.Br * p.R;
-    const int row = blockIdx.x * kTcRows + tid;   // this thread's query row = its tensor-memory lane
+    const int row = blockIdx.x * kTcRows + lrow;
     const bool live = row < rows_total;
     const int b = live ? row / p.R : 0;
     const int r = live ? row - b * p.R : 0;
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         if (p.pre_len != nullptr) {
             lim = p.pre_len[b];
             if (lim < 0 || lim > p.P) {
-                atomicOr(p.err, FX_DEVERR_LEN);
+                if (half == 0) atomicOr(p.err, FX_DEVERR_LEN);
                 lim = lim < 0 ? 0 : p.P;
             }
         }
@@ -212,24 +217,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    // this thread's query row into the Q tile (zero past the last row)
+    // this row's query into the Q tile (zero past the last row); each half copies 64 dims
     {
         const int gi = r / p.Mq;
         const int i = r - gi * p.Mq;
         const uint16_t* qrow = p.q + ((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sQ + sw128(tid, 8 * c, kTcRows)) = v;
+        for (int c = 0; c < 8; ++c) {
+            const int d = col0 + 8 * c;
+            const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + d) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sQ + sw128(lrow, d, kTcRows)) = v;
         }
     }
     __syncthreads();
     atomicMax(&s_lim_max, lim);
     publish_to_tensor_core();
     const uint32_t tmem = s_tmem;
-    const uint32_t tmem_s = tmem;          // S: columns 0..127
-    const uint32_t tmem_o = tmem + 128;    // O: columns 128..255
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tmem_s = tmem + col0;          // this thread's S columns (S: columns 0..127)
+    const uint32_t tmem_o = tmem + 128 + col0;    // this thread's O columns (O: columns 128..255)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int ntiles = (s_lim_max + kTcKeys - 1) / kTcKeys;
     const uint16_t* kb = p.pk + (int64_t)h * p.p_sh;
     const uint16_t* vb = p.pv + (int64_t)h * p.p_sh;
@@ -262,11 +268,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
 
     // One pass over the prefix with an online softmax.  A row's running maximum m moves only when a
     // tile's maximum exceeds it by more than kRescale (log2 units): O in tensor memory is then rescaled
-    // by the row's own thread (read, scale, write back), which happens a few times per row at most, and
+    // by the row's own threads (read, scale, write back), which happens a few times per row at most, and
     // P = exp2(s - m) stays below 2^kRescale.  The next tile's K and V rows are in flight while this
     // tile's softmax and P V run.
     float m = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;   // this half's share of the row sum
     unsigned ph_s = 0, ph_o = 0;
     if (ntiles > 0) {
         load_k(0);
@@ -277,20 +283,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         asm volatile("cp.async.wait_group 1;" ::: "memory");   // K of this tile landed
         publish_to_tensor_core();
         if (tid == 0) {
-            mma_tile(tmem_s, smem_addr(sQ), smem_addr(sK), false);
+            mma_tile(tmem, smem_addr(sQ), smem_addr(sK), false);
             mma_commit(&bar_s);
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");   // V of this tile landed
         if (t > 0) mma_wait(&bar_o, ph_o, p.err);               // previous P V done: V^T, P tiles and O free
         __syncthreads();
         // V (keys x dims, staged row-major) -> V^T (dims x keys) in the swizzled K-major layout:
-        // 8 x 8 blocks through ldmatrix and stmatrix.trans; warp w owns keys 32w .. 32w+31
+        // 8 x 8 blocks through ldmatrix and stmatrix.trans; warp w owns keys 16w .. 16w+15
         {
             const int j = lane >> 3;
             const int i = lane & 7;
 #pragma unroll
-            for (int kg = 0; kg < 4; ++kg) {
-                const int k0 = warp * 32 + kg * 8;
+            for (int kg = 0; kg < 2; ++kg) {
+                const int k0 = warp * 16 + kg * 8;
 #pragma unroll
                 for (int dq = 0; dq < 4; ++dq) {
                     const int d0 = dq * 32;
@@ -312,75 +318,81 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
             load_v(j0 + kTcKeys);
         }
 
-        // the row's maximum over this tile, and the rescale of O when the running maximum moves
+        // this half's 64 scaled logits, the row's maximum over the tile, and the rescale of O when the
+        // running maximum moves
+        float sv[2][32];
+        tmem_ld32(tmem_s + lane_base, sv[0]);
+        tmem_ld32(tmem_s + lane_base + 32, sv[1]);
+        const int nv = lim - (j0 + col0);   // keys of this half that the row sees
         float mt = -INFINITY;
 #pragma unroll
-        for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem_s + lane_base + c0, v);
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                if (j0 + c0 + jj < lim) mt = fmaxf(mt, v[jj] * p.qscale);
-        }
+            for (int jj = 0; jj < 32; ++jj) {
+                const float x = sv[u][jj] * p.qscale;
+                sv[u][jj] = x;
+                if (32 * u + jj < nv) mt = fmaxf(mt, x);
+            }
+        s_xch[tid] = mt;
+        __syncthreads();
+        mt = fmaxf(mt, s_xch[tid ^ kTcRows]);
         const bool grow = mt > m + kRescale;   // also when m is still -inf and the tile has keys
         const float mnew = grow ? mt : m;
         if (t > 0 && __any_sync(0xffffffffu, grow)) {   // tensor-memory access is warp-wide
             const float a = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_approx(m - mnew));
 #pragma unroll
-            for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+            for (int u = 0; u < 2; ++u) {
                 float v[32];
-                tmem_ld32(tmem_o + lane_base + c0, v);
+                tmem_ld32(tmem_o + lane_base + 32 * u, v);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) v[c] *= a;
-                tmem_st32(tmem_o + lane_base + c0, v);
+                tmem_st32(tmem_o + lane_base + 32 * u, v);
             }
             l *= a;
         }
         m = mnew;
         const float ms = (m == -INFINITY) ? 0.f : m;
 
-        // P = exp2(S - m) as bf16 hi + lo into the two P tiles, l += sum P
+        // P = exp2(s - m) as bf16 hi + lo into the two P tiles, l += sum P
 #pragma unroll
-        for (int c0 = 0; c0 < kTcKeys; c0 += 32) {
-            float v[32];
-            tmem_ld32(tmem_s + lane_base + c0, v);
+        for (int q = 0; q < 8; ++q) {   // 8 keys = one 16-byte chunk of the P tiles
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {   // 8 keys = one 16-byte chunk of the P tiles
-                uint32_t hi[4], lo[4];
+            for (int u = 0; u < 4; ++u) {
+                float pv[2];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float pv[2];
-#pragma unroll
-                    for (int w2 = 0; w2 < 2; ++w2) {
-                        const int jj = 8 * q + 2 * u + w2;
-                        pv[w2] = (j0 + c0 + jj < lim) ? exp2_approx(v[jj] * p.qscale - ms) : 0.f;
-                        l += pv[w2];
-                    }
-                    __nv_bfloat162 hv = __floats2bfloat162_rn(pv[0], pv[1]);
-                    hi[u] = *reinterpret_cast<uint32_t*>(&hv);
-                    lo[u] = pack2_bf16(pv[0] - __low2float(hv), pv[1] - __high2float(hv));
+                for (int w2 = 0; w2 < 2; ++w2) {
+                    const int e = 8 * q + 2 * u + w2;
+                    pv[w2] = (e < nv) ? exp2_approx(sv[e >> 5][e & 31] - ms) : 0.f;
+                    l += pv[w2];
                 }
-                const uint32_t off = sw128(tid, c0 + 8 * q, kTcRows);
-                *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                __nv_bfloat162 hv = __floats2bfloat162_rn(pv[0], pv[1]);
+                hi[u] = *reinterpret_cast<uint32_t*>(&hv);
+                lo[u] = pack2_bf16(pv[0] - __low2float(hv), pv[1] - __high2float(hv));
             }
+            const uint32_t off = sw128(lrow, col0 + 8 * q, kTcRows);
+            *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         publish_to_tensor_core();   // also: every thread has read S before the next tile overwrites it
         if (tid == 0) {
-            mma_tile(tmem_o, smem_addr(sPh), smem_addr(sVt), t > 0);
-            mma_tile(tmem_o, smem_addr(sPl), smem_addr(sVt), true);
+            mma_tile(tmem + 128, smem_addr(sPh), smem_addr(sVt), t > 0);
+            mma_tile(tmem + 128, smem_addr(sPl), smem_addr(sVt), true);
             mma_commit(&bar_o);
         }
     }
     if (ntiles > 0) mma_wait(&bar_o, ph_o, p.err);
 
     // ---- the partial of this row over the prefix (the loads are warp-wide: every lane takes part) -----
+    s_xch[tid] = l;
+    __syncthreads();
+    const float lt = l + s_xch[tid ^ kTcRows];
     const int64_t er = ((int64_t)h * p.Br + b) * p.R + r;
 #pragma unroll
-    for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+    for (int u = 0; u < 2; ++u) {
         float v[32];
         if (ntiles > 0) {
-            tmem_ld32(tmem_o + lane_base + c0, v);
+            tmem_ld32(tmem_o + lane_base + 32 * u, v);
         } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = 0.f;
@@ -388,13 +400,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         if (live) {
 #pragma unroll
             for (int c = 0; c < 32; c += 4)
-                *reinterpret_cast<float4*>(p.ext_o + er * kHeadDim + c0 + c) =
+                *reinterpret_cast<float4*>(p.ext_o + er * kHeadDim + col0 + 32 * u + c) =
                     make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
         }
     }
-    if (live) {
+    if (live && half == 0) {
         p.ext_m[er] = m;
-        p.ext_l[er] = l;
+        p.ext_l[er] = lt;
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
