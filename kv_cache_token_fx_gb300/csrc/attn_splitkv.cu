@@ -208,22 +208,17 @@ struct KeySource {
 };
 
 // ---- the kernel -----------------------------------------------------------------------------------
-// Output value of column c of row `row` of this (b, h) from the split-merged (M, and Ls, O relative to
-// Ms).  A partial over other keys of the row computed by another kernel (ext: the dense shared prefix of
-// the verify call) is folded in first.
-__device__ __forceinline__ float finish_row(const AttnParams& p, int b, int h, int row, int c, float M, float Ms,
-                                            float Ls, float O)
+// Output value from the split-merged (M, and Ls, O relative to Ms).  A partial over other keys of the
+// row computed by another kernel (ext: the dense shared prefix of the verify call; me = -inf when
+// absent) is folded in first.
+__device__ __forceinline__ float finish_row(float me, float le, float oe, float M, float Ms, float Ls, float O)
 {
-    if (p.ext_m != nullptr) {
-        const int64_t er = ((int64_t)h * p.B + b) * p.R + row;
-        const float me = p.ext_m[er];
-        if (me != -INFINITY) {
-            const float mn = fmaxf(M, me);
-            const float a = M == -INFINITY ? 0.f : fast_exp2(Ms - mn);
-            const float e = fast_exp2(me - mn);
-            Ls = fmaf(Ls, a, p.ext_l[er] * e);
-            O = fmaf(O, a, p.ext_o[er * kHeadDim + c] * e);
-        }
+    if (me != -INFINITY) {
+        const float mn = fmaxf(M, me);
+        const float a = M == -INFINITY ? 0.f : fast_exp2(Ms - mn);
+        const float e = fast_exp2(me - mn);
+        Ls = fmaf(Ls, a, le * e);
+        O = fmaf(O, a, oe * e);
     }
     return Ls > 0.f ? O / Ls : 0.f;
 }
@@ -673,23 +668,30 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                     }
                 }
             }
+            // the running maximum moves only when the sub-tile's maximum exceeds it by more than
+            // kMaxSlack, so O is rescaled a few times per row instead of every sub-tile (P <= 2^kMaxSlack)
             float alpha[2], ms[2];
+            bool grow_any = false;
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 1));
                 mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(kFull, mx[hr], 2));
-                const float mn = fmaxf(m_run[hr], mx[hr]);
+                const bool grow = mx[hr] > m_run[hr] + kMaxSlack;   // also: first keys of the row
+                const float mn = grow ? mx[hr] : m_run[hr];
                 ms[hr] = (mn == -INFINITY) ? 0.f : mn;
-                alpha[hr] = fast_exp2(m_run[hr] - ms[hr]);
+                alpha[hr] = grow ? fast_exp2(m_run[hr] - ms[hr]) : 1.f;
                 m_run[hr] = mn;
                 l_run[hr] *= alpha[hr];
+                grow_any |= grow;
             }
+            if (__any_sync(kFull, grow_any)) {
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                o[n][0] *= alpha[0];
-                o[n][1] *= alpha[0];
-                o[n][2] *= alpha[1];
-                o[n][3] *= alpha[1];
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= alpha[0];
+                    o[n][1] *= alpha[0];
+                    o[n][2] *= alpha[1];
+                    o[n][3] *= alpha[1];
+                }
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -724,6 +726,28 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 
         __syncwarp();      // every lane is done with this buffer before it is refilled
         issue(j + kWarpStages, tnext);
+    }
+    // the external partial of these rows (column tid of each; kThreads == kHeadDim), loaded now so its
+    // latency overlaps the combine below
+    static_assert(kThreads == kHeadDim, "one output column per thread");
+    constexpr int kExtRows = NR == 32 ? 1 : NR;
+    float ext_oc[kExtRows];
+    __shared__ float s_ext_m[kMaxRowsPerCta];
+    __shared__ float s_ext_l[kMaxRowsPerCta];
+#pragma unroll
+    for (int r = 0; r < kExtRows; ++r) ext_oc[r] = 0.f;
+    if (NR != 32 && p.ext_m != nullptr) {
+        const int64_t er0 = ((int64_t)h * p.B + b) * p.R + r0;
+#pragma unroll
+        for (int r = 0; r < kExtRows; ++r)
+            if (r0 + r < p.R) ext_oc[r] = __ldcg(p.ext_o + (er0 + r) * kHeadDim + tid);
+        if (tid < NR && r0 + tid < p.R) {
+            s_ext_m[tid] = __ldcg(p.ext_m + er0 + tid);
+            s_ext_l[tid] = __ldcg(p.ext_l + er0 + tid);
+        }
+    } else if (tid < kMaxRowsPerCta) {
+        s_ext_m[tid] = -INFINITY;
+        s_ext_l[tid] = 0.f;
     }
     cp_async_wait_all_groups();
     __syncthreads();       // all warps are done with their buffers (reused below)
@@ -835,6 +859,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
 
     if constexpr (MERGE == kMergePush) {
+        static_assert(NR != 32, "scoring-only tiles merge through the workspace");
         // CTAs 1 .. cs-1 send their partial into CTA 0's receive area with asynchronous remote stores
         // that count their bytes on CTA 0's barrier, and exit at once; CTA 0 announces the bytes it
         // expects, waits for them and merges alone.
@@ -867,9 +892,10 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 }
             }
         }
-        for (int e = tid; e < nr * kHeadDim; e += kThreads) {
-            const int r = e >> 7;
-            const int c = e & (kHeadDim - 1);
+        const int c = tid;
+#pragma unroll
+        for (int r = 0; r < kExtRows; ++r) {
+            if (r >= nr) break;
             float M = c_m[r];
             for (int q = 0; q < npeer; ++q) M = fmaxf(M, recv_m[q * nr + r]);
             const float Ms = (M == -INFINITY) ? 0.f : M;
@@ -884,7 +910,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             const int row = r0 + r;
             const int gi = row / p.Mq;
             const int i = row - gi * p.Mq;
-            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = finish_row(p, b, h, row, c, M, Ms, Ls, O);
+            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] =
+                finish_row(s_ext_m[r], s_ext_l[r], ext_oc[r], M, Ms, Ls, O);
         }
         return;
     }
@@ -892,12 +919,17 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     if constexpr (MERGE == kMergePull) {
         // every split of this (b, h, row group) is one CTA of the cluster: merge through distributed
         // shared memory, each CTA producing a slice of the output rows
+        static_assert(NR != 32, "scoring-only tiles merge through the workspace");
         cluster_sync();
         const unsigned cs = cluster_size();
         const unsigned me = cluster_rank();
-        for (int e = (int)me * kThreads + tid; e < nr * kHeadDim; e += (int)cs * kThreads) {
-            const int r = e >> 7;
-            const int c = e & (kHeadDim - 1);
+        const int c = tid;
+        int rn = (int)me;   // CTA q of the cluster produces rows q, q + cs, q + 2 cs, ...
+#pragma unroll
+        for (int r = 0; r < kExtRows; ++r) {
+            if (r >= nr) break;
+            if (r != rn) continue;
+            rn += (int)cs;
             // one batch of independent remote loads, then the arithmetic
             float mq[kMaxClusterSplits], lq[kMaxClusterSplits], oq[kMaxClusterSplits];
 #pragma unroll
@@ -926,7 +958,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             const int row = r0 + r;
             const int gi = row / p.Mq;
             const int i = row - gi * p.Mq;
-            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] = finish_row(p, b, h, row, c, M, Ms, Ls, O);
+            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] =
+                finish_row(s_ext_m[r], s_ext_l[r], ext_oc[r], M, Ms, Ls, O);
         }
         cluster_sync();   // keep every CTA's shared memory alive until all reads are done
         return;
@@ -956,7 +989,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     __syncthreads();
     if (s_last == 0u) return;
     __threadfence();
-    for (int r = 0; r < nr; ++r) {
+#pragma unroll
+    for (int r = 0; r < kExtRows; ++r) {
+        if (r >= nr) break;
         const int row = r0 + r;
         const int64_t base = (int64_t)(bh * p.R + row) * p.nsplit;
         float M = -INFINITY;
@@ -965,15 +1000,14 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         const int gi = row / p.Mq;
         const int i = row - gi * p.Mq;
         float* orow = p.out + ((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7);
-        for (int c = tid; c < kHeadDim; c += kThreads) {
-            float Ls = 0.f, O = 0.f;
-            for (int s = 0; s < p.nsplit; ++s) {
-                const float sc = fast_exp2(__ldcg(p.part_m + base + s) - Ms);
-                Ls = fmaf(__ldcg(p.part_l + base + s), sc, Ls);
-                O = fmaf(__ldcg(p.part_o + (base + s) * kHeadDim + c), sc, O);
-            }
-            orow[c] = finish_row(p, b, h, row, c, M, Ms, Ls, O);
+        const int c = tid;
+        float Ls = 0.f, O = 0.f;
+        for (int s = 0; s < p.nsplit; ++s) {
+            const float sc = fast_exp2(__ldcg(p.part_m + base + s) - Ms);
+            Ls = fmaf(__ldcg(p.part_l + base + s), sc, Ls);
+            O = fmaf(__ldcg(p.part_o + (base + s) * kHeadDim + c), sc, O);
         }
+        orow[c] = finish_row(s_ext_m[r], s_ext_l[r], ext_oc[r], M, Ms, Ls, O);
     }
     if (tid == 0) p.counters[bh * p.nrg + rg] = 0u;
 }

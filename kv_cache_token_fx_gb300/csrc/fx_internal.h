@@ -16,6 +16,7 @@ constexpr int kWarps = 4;                               // warps per attention C
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRowBytes = kHeadDim * 2;                 // one bf16 K or V row (256 bytes)
 constexpr int kSub = 16;                                // keys per warp sub-tile (two n-tiles of S = Q K^T)
+constexpr float kMaxSlack = 8.f;                       // online-softmax maximum slack (log2 units)
 constexpr int kWarpStages = 3;                          // sub-tiles in flight per warp
 constexpr int kRowsPerCta = 16;                         // query rows per CTA: one m16 MMA tile
 constexpr int kPitch = kRowBytes + 16;                  // staged row pitch: the 16-byte pad puts the 8

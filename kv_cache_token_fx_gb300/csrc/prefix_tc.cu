@@ -28,7 +28,6 @@ constexpr int kTcThreads = 256;                   // two threads per query row
 constexpr int kTileBytes = kTcRows * kHeadDim * 2;  // one 128 x 128 bf16 operand tile
 constexpr int kVsPitch = 272;                      // V staging row pitch: conflict-free ldmatrix
 constexpr int kTmemCols = 256;                     // S in columns 0..127, O in 128..255
-constexpr float kRescale = 8.f;                    // running-maximum slack (log2 units) before O is rescaled
 // [Q | K | V^T | P_hi | P_lo] swizzled tiles, the V staging rows, and slack to align to 1024 bytes
 constexpr size_t kTcSmem = 5 * (size_t)kTileBytes + (size_t)kTcKeys * kVsPitch + 1024;
 
@@ -267,9 +266,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     };
 
     // One pass over the prefix with an online softmax.  A row's running maximum m moves only when a
-    // tile's maximum exceeds it by more than kRescale (log2 units): O in tensor memory is then rescaled
+    // tile's maximum exceeds it by more than kMaxSlack (log2 units): O in tensor memory is then rescaled
     // by the row's own threads (read, scale, write back), which happens a few times per row at most, and
-    // P = exp2(s - m) stays below 2^kRescale.  The next tile's K and V rows are in flight while this
+    // P = exp2(s - m) stays below 2^kMaxSlack.  The next tile's K and V rows are in flight while this
     // tile's softmax and P V run.
     float m = -INFINITY;
     float l = 0.f;   // this half's share of the row sum
@@ -336,7 +335,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         s_xch[tid] = mt;
         __syncthreads();
         mt = fmaxf(mt, s_xch[tid ^ kTcRows]);
-        const bool grow = mt > m + kRescale;   // also when m is still -inf and the tile has keys
+        const bool grow = mt > m + kMaxSlack;   // also when m is still -inf and the tile has keys
         const float mnew = grow ? mt : m;
         if (t > 0 && __any_sync(0xffffffffu, grow)) {   // tensor-memory access is warp-wide
             const float a = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_approx(m - mnew));
