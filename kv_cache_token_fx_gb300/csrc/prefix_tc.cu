@@ -4,14 +4,17 @@
 // branch attends over the same prefix rows (up to its fork position) before its own suffix and drafts.
 // Per KV head the query rows of all branches (Br x R of them) therefore meet one shared set of keys --
 // a real matrix product, which this kernel runs as 128 x 128 tiles on the tensor cores:
-//   S = Q K^T       (M = 128 query rows, N = 128 prefix keys, K = 128 dims)        -> tensor memory
-//   O += P V        (M = 128 query rows, N = 128 dims, K = 128 prefix keys)        -> tensor memory
+//   S = Q K^T       (M = 128 query rows, N = 128 prefix keys, K = 128 dims)   smem x smem -> tensor memory
+//   O += P V        (M = 128 query rows, N = 128 dims, K = 128 prefix keys)   tensor memory x smem -> tensor memory
 // in one pass with an online softmax (P = exp2(S - m) against a running maximum m that moves only by
 // more than a fixed slack, so O is rescaled rarely), P split into bf16 hi + lo parts (two products) so
-// the probabilities keep about 16 bits.  Two threads own one query row, each for half of
-// the keys of a tile and half of O: they read their S columns from tensor memory, trade the row
-// maximum, form P, and write it to shared memory as the next product's A operand.  Operand tiles are
-// K-major with the 128-byte swizzle; V is transposed into that layout through ldmatrix / stmatrix.trans.
+// the probabilities keep about 16 bits.  Two threads own one query row, each for half of the keys of a
+// tile and half of O: they read their S columns from tensor memory, trade the row maximum, and write
+// P back into tensor memory, where the P V product takes it as its A operand.  Q and K tiles are
+// K-major operands with the 128-byte swizzle; V tiles are copied as they are stored (keys x dims) into
+// the same swizzled layout and used as an MN-major operand, so nothing is transposed.  S is double
+// buffered in tensor memory and K, V in shared memory: the next tile's Q K^T runs on the tensor cores
+// while this tile's softmax runs on the threads.
 // The result per row is a partial (m, l, O) over the prefix, which the verify kernel folds into its
 // merge of the suffix and draft keys.
 #include <cuda_bf16.h>
@@ -24,50 +27,70 @@ namespace {
 
 constexpr int kTcRows = 128;                       // query rows per CTA (one tensor-memory lane each)
 constexpr int kTcKeys = 128;                       // prefix keys per tile
-constexpr int kTcThreads = 256;                   // two threads per query row
+constexpr int kTcThreads = 256;                    // two threads per query row
 constexpr int kTileBytes = kTcRows * kHeadDim * 2;  // one 128 x 128 bf16 operand tile
-constexpr int kVsPitch = 272;                      // V staging row pitch: conflict-free ldmatrix
-constexpr int kTmemCols = 256;                     // S in columns 0..127, O in 128..255
-// [Q | K | V^T | P_hi | P_lo] swizzled tiles, the V staging rows, and slack to align to 1024 bytes
-constexpr size_t kTcSmem = 5 * (size_t)kTileBytes + (size_t)kTcKeys * kVsPitch + 1024;
+// tensor-memory columns: S of even and odd tiles, O, and P (bf16 pairs: hi then lo)
+constexpr int kTmemCols = 512;
+constexpr int kColS0 = 0, kColS1 = 128, kColO = 256, kColPh = 384, kColPl = 448;
+// [Q | K even | K odd | V even | V odd] swizzled tiles and slack to align to 1024 bytes
+constexpr size_t kTcSmem = 5 * (size_t)kTileBytes + 1024;
 
-// Byte offset of element (r, k) of a [rows x 128] bf16 tile stored K-major with the 128-byte swizzle:
-// two 64-wide K blocks of rows x 128 bytes each; 8-row groups of 1024 bytes; within a row the 16-byte
-// chunk index is XORed with (row % 8).
-__device__ __forceinline__ uint32_t sw128(int r, int k, int rows)
+// Byte offset of element (r, c) of a [rows x 128] bf16 tile stored with the 128-byte swizzle: two
+// 64-wide column blocks of rows x 128 bytes each; 8-row groups of 1024 bytes; within a row the 16-byte
+// chunk index is XORed with (row % 8).  Q and K tiles (row = query / key, c = dim) are K-major
+// operands; V tiles (row = key, c = dim) in the same layout are MN-major operands.
+__device__ __forceinline__ uint32_t sw128(int r, int c, int rows)
 {
-    const int kk = k & 63;
-    return (uint32_t)((k >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((kk >> 3) ^ (r & 7)) << 4) +
-                      (kk & 7) * 2);
+    const int cc = c & 63;
+    return (uint32_t)((c >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + (((cc >> 3) ^ (r & 7)) << 4) +
+                      (cc & 7) * 2);
 }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
+// Shared-memory matrix descriptor with the 128-byte swizzle.  K-major: 8-row groups 1024 bytes apart
+// (the leading offset is unused).  MN-major: 64-element column blocks `lbo` bytes apart, 8-row (K)
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo = 16)
 {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+// Instruction descriptor: bf16 x bf16 -> fp32, M x N, A K-major, B K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
-// D (tensor memory) (+)= A (smem tile) x B (smem tile)^T over 128 of K, as 8 products of K = 16.
-__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile, bool accumulate)
+// S (tensor memory) = Q (smem tile) x K (smem tile)^T over the 128 dims, as 8 products of K = 16.
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t q_tile, uint32_t k_tile)
 {
-    constexpr uint32_t idesc = idesc_bf16(128, 128);
+    constexpr uint32_t idesc = idesc_bf16(128, 128, false);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (uint32_t)((ks >> 2) * 128 * 128 + (ks & 3) * 32);
-        const uint64_t da = sdesc(a_tile + off);
-        const uint64_t db = sdesc(b_tile + off);
-        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+        const uint32_t off = (uint32_t)((ks >> 2) * kTileBytes / 2 + (ks & 3) * 32);
+        const uint64_t da = sdesc(q_tile + off);
+        const uint64_t db = sdesc(k_tile + off);
+        const uint32_t acc = ks > 0 ? 1u : 0u;
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
             "l"(da), "l"(db), "r"(idesc), "r"(acc));
+    }
+}
+
+// O (tensor memory) (+)= P (tensor memory, bf16 pairs) x V (smem tile, MN-major) over the 128 keys.
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_tile, bool accumulate)
+{
+    constexpr uint32_t idesc = idesc_bf16(128, 128, true);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t db = sdesc(v_tile + ks * 2048, kTileBytes / 2);   // 16 keys = two 8-row groups
+        const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(p_tmem + 8 * ks), "l"(db), "r"(idesc), "r"(acc));
     }
 }
 
@@ -77,22 +100,22 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar)
                  : "memory");
 }
 
-// Bounded wait for the products committed to `bar`; flags a timeout instead of hanging.
-__device__ __forceinline__ void mma_wait(uint64_t* bar, unsigned& phase, unsigned* err)
+// Bounded wait for the phase of `bar` with the given parity (the products committed to it); flags a
+// timeout instead of hanging.
+__device__ __forceinline__ void mma_wait_parity(uint64_t* bar, unsigned parity, unsigned* err)
 {
     unsigned spins = 0, done = 0;
     while (!done) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(smem_addr(bar)), "r"(phase)
+            : "r"(smem_addr(bar)), "r"(parity)
             : "memory");
         if (!done && ++spins == kSpinLimit) {
             if (threadIdx.x == 0) atomicOr(err, FX_DEVERR_TIMEOUT);
             break;
         }
     }
-    phase ^= 1u;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
@@ -113,22 +136,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
 }
 
-// Store 32 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32])
+// Store 32 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&u)[32])
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
         "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(addr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]),
+        "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]), "r"(u[16]), "r"(u[17]),
+        "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]),
+        "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]), "r"(u[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -166,22 +183,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     unsigned char* sQ = base;
-    unsigned char* sK = base + kTileBytes;
-    unsigned char* sVt = base + 2 * kTileBytes;
-    unsigned char* sPh = base + 3 * kTileBytes;
-    unsigned char* sPl = base + 4 * kTileBytes;
-    unsigned char* sVs = base + 5 * kTileBytes;
-    __shared__ __align__(8) uint64_t bar_s;   // S = Q K^T of the current tile is in tensor memory
-    __shared__ __align__(8) uint64_t bar_o;   // O += P V of the previous tile is done
+    auto sK = [&](int x) { return base + (1 + x) * kTileBytes; };   // K tiles of even / odd tiles
+    auto sV = [&](int x) { return base + (3 + x) * kTileBytes; };   // V tiles of even / odd tiles
+    __shared__ __align__(8) uint64_t bar_s[2];   // S of an even / odd tile is in tensor memory
+    __shared__ __align__(8) uint64_t bar_o;      // O += P V of the last issued tile is done
     __shared__ uint32_t s_tmem;
     __shared__ int s_lim_max;
-    __shared__ float s_xch[kTcThreads];       // the two halves of a row trade their maxima / sums
+    __shared__ float s_xch[kTcThreads];          // the two halves of a row trade their maxima / sums
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int lrow = tid & (kTcRows - 1);     // query row within the tile = tensor-memory lane
-    const int half = tid >> 7;                // this thread's 64 keys of each tile and 64 dims of O
+    const int lrow = tid & (kTcRows - 1);        // query row within the tile = tensor-memory lane
+    const int half = tid >> 7;                   // this thread's 64 keys of each tile and 64 dims of O
     const int col0 = half * 64;
     const int h = blockIdx.y;
     const int rows_total = p.Br * p.R;
@@ -207,7 +220,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     }
     if (tid == 0) {
         s_lim_max = 0;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s[0])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s[1])));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_o)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -232,155 +246,133 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     atomicMax(&s_lim_max, lim);
     publish_to_tensor_core();
     const uint32_t tmem = s_tmem;
-    const uint32_t tmem_s = tmem + col0;          // this thread's S columns (S: columns 0..127)
-    const uint32_t tmem_o = tmem + 128 + col0;    // this thread's O columns (O: columns 128..255)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int ntiles = (s_lim_max + kTcKeys - 1) / kTcKeys;
     const uint16_t* kb = p.pk + (int64_t)h * p.p_sh;
     const uint16_t* vb = p.pv + (int64_t)h * p.p_sh;
 
-    // K rows into the swizzled K tile, V rows into the staging rows; keys past P are zero
-    auto load_k = [&](int j0) {
-        for (int e = tid; e < kTcKeys * 16; e += kTcThreads) {
-            const int key = e >> 4;
-            const int c = e & 15;
-            unsigned char* dst = sK + sw128(key, 8 * c, kTcKeys);
-            if (j0 + key < p.P)
-                cp16(smem_addr(dst), kb + (int64_t)(j0 + key) * p.p_st + 8 * c);
-            else
-                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    auto load_v = [&](int j0) {
-        for (int e = tid; e < kTcKeys * 16; e += kTcThreads) {
-            const int key = e >> 4;
-            const int c = e & 15;
-            unsigned char* dst = sVs + key * kVsPitch + 16 * c;
-            if (j0 + key < p.P)
-                cp16(smem_addr(dst), vb + (int64_t)(j0 + key) * p.p_st + 8 * c);
-            else
-                *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-
-    // One pass over the prefix with an online softmax.  A row's running maximum m moves only when a
-    // tile's maximum exceeds it by more than kMaxSlack (log2 units): O in tensor memory is then rescaled
-    // by the row's own threads (read, scale, write back), which happens a few times per row at most, and
-    // P = exp2(s - m) stays below 2^kMaxSlack.  The next tile's K and V rows are in flight while this
-    // tile's softmax and P V run.
-    float m = -INFINITY;
-    float l = 0.f;   // this half's share of the row sum
-    unsigned ph_s = 0, ph_o = 0;
-    if (ntiles > 0) {
-        load_k(0);
-        load_v(0);
-    }
-    for (int t = 0; t < ntiles; ++t) {
-        const int j0 = t * kTcKeys;
-        asm volatile("cp.async.wait_group 1;" ::: "memory");   // K of this tile landed
-        publish_to_tensor_core();
-        if (tid == 0) {
-            mma_tile(tmem, smem_addr(sQ), smem_addr(sK), false);
-            mma_commit(&bar_s);
-        }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");   // V of this tile landed
-        if (t > 0) mma_wait(&bar_o, ph_o, p.err);               // previous P V done: V^T, P tiles and O free
-        __syncthreads();
-        // V (keys x dims, staged row-major) -> V^T (dims x keys) in the swizzled K-major layout:
-        // 8 x 8 blocks through ldmatrix and stmatrix.trans; warp w owns keys 16w .. 16w+15
-        {
-            const int j = lane >> 3;
-            const int i = lane & 7;
-#pragma unroll
-            for (int kg = 0; kg < 2; ++kg) {
-                const int k0 = warp * 16 + kg * 8;
-#pragma unroll
-                for (int dq = 0; dq < 4; ++dq) {
-                    const int d0 = dq * 32;
-                    uint32_t x0, x1, x2, x3;
-                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                                 : "r"(smem_addr(sVs + (k0 + i) * kVsPitch + (d0 + 8 * j) * 2)));
-                    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     smem_addr(sVt + sw128(d0 + 8 * j + i, k0, kHeadDim))),
-                                 "r"(x0), "r"(x1), "r"(x2), "r"(x3)
-                                 : "memory");
-                }
+    // Rows j0 .. j0+127 of a prefix head (K or V) into a swizzled tile, keys past P zero; one commit
+    // group per call, empty when the tile does not exist, so the group counts below stay fixed.
+    auto load_tile = [&](unsigned char* dst, const uint16_t* src, int t) {
+        if (t < ntiles) {
+            const int j0 = t * kTcKeys;
+            for (int e = tid; e < kTcKeys * 16; e += kTcThreads) {
+                const int key = e >> 4;
+                const int c = e & 15;
+                unsigned char* d = dst + sw128(key, 8 * c, kTcKeys);
+                if (j0 + key < p.P)
+                    cp16(smem_addr(d), src + (int64_t)(j0 + key) * p.p_st + 8 * c);
+                else
+                    *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        mma_wait(&bar_s, ph_s, p.err);   // S of this tile in tensor memory; the K tile is consumed
-        __syncthreads();                 // and every warp is done with the V staging rows
-        if (t + 1 < ntiles) {
-            load_k(j0 + kTcKeys);
-            load_v(j0 + kTcKeys);
-        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
 
-        // this half's 64 scaled logits, the row's maximum over the tile, and the rescale of O when the
-        // running maximum moves
+    // Pipeline over the prefix tiles t = 0 .. ntiles-1 (x = t & 1 picks the buffers): K(t) -> sK(x),
+    // V(t) -> sV(x), S(t) = Q K(t)^T -> tensor-memory S[x], P(t) -> the P columns, O += P(t) V(t).
+    // S(t+1) runs on the tensor cores while the threads turn S(t) into P(t); K(t+2) is copied as soon as
+    // S(t) is done, V(t+1) as soon as P(t-1) V(t-1) is done.  Commit groups: K(0), V(0), K(1) before the
+    // loop, then K(t+2) and V(t+1) per tile (empty past the end), so the waits below count fixed groups.
+    // Online softmax: a row's running maximum m moves only when a tile's maximum exceeds it by more than
+    // kMaxSlack (log2 units); O in tensor memory is then rescaled by the row's threads, and
+    // P = exp2(s - m) stays below 2^kMaxSlack.
+    float m = -INFINITY;
+    float l = 0.f;   // this half's share of the row sum
+    if (ntiles > 0) {
+        load_tile(sK(0), kb, 0);
+        load_tile(sV(0), vb, 0);
+        load_tile(sK(1), kb, 1);
+        asm volatile("cp.async.wait_group 2;" ::: "memory");   // K(0)
+        publish_to_tensor_core();
+        if (tid == 0) {
+            mma_qk(tmem + kColS0, smem_addr(sQ), smem_addr(sK(0)));
+            mma_commit(&bar_s[0]);
+        }
+    }
+    for (int t = 0; t < ntiles; ++t) {
+        const int x = t & 1;
+        const int j0 = t * kTcKeys;
+        const uint32_t col_s = x ? kColS1 : kColS0;
+        // (a) S(t+1) onto the tensor cores; its S columns held S(t-1), which every thread has read
+        if (t + 1 < ntiles) {
+            if (t == 0)
+                asm volatile("cp.async.wait_group 0;" ::: "memory");   // K(1)
+            else
+                asm volatile("cp.async.wait_group 1;" ::: "memory");   // K(t+1); V(t) may be in flight
+            publish_to_tensor_core();
+            if (tid == 0) {
+                mma_qk(tmem + (x ? kColS0 : kColS1), smem_addr(sQ), smem_addr(sK(x ^ 1)));
+                mma_commit(&bar_s[x ^ 1]);
+            }
+        }
+        // (b) this half's 64 logits of S(t); the K buffer of tile t is then free for K(t+2)
+        mma_wait_parity(&bar_s[x], (unsigned)(t >> 1) & 1u, p.err);
         float sv[2][32];
-        tmem_ld32(tmem_s + lane_base, sv[0]);
-        tmem_ld32(tmem_s + lane_base + 32, sv[1]);
+        tmem_ld32(tmem + lane_base + col_s + col0, sv[0]);
+        tmem_ld32(tmem + lane_base + col_s + col0 + 32, sv[1]);
+        load_tile(sK(x), kb, t + 2);
+        // (c) the row's maximum over the tile: the two halves trade theirs
         const int nv = lim - (j0 + col0);   // keys of this half that the row sees
         float mt = -INFINITY;
 #pragma unroll
         for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-                const float x = sv[u][jj] * p.qscale;
-                sv[u][jj] = x;
-                if (32 * u + jj < nv) mt = fmaxf(mt, x);
+                const float xs = sv[u][jj] * p.qscale;
+                sv[u][jj] = xs;
+                if (32 * u + jj < nv) mt = fmaxf(mt, xs);
             }
         s_xch[tid] = mt;
         __syncthreads();
         mt = fmaxf(mt, s_xch[tid ^ kTcRows]);
         const bool grow = mt > m + kMaxSlack;   // also when m is still -inf and the tile has keys
         const float mnew = grow ? mt : m;
+        // (d) P(t-1) V(t-1) is done: O may be rescaled, the P columns rewritten, V(t+1) copied into the
+        // V buffer of tile t-1
+        if (t > 0) mma_wait_parity(&bar_o, (unsigned)(t - 1) & 1u, p.err);
+        load_tile(sV(x ^ 1), vb, t + 1);
         if (t > 0 && __any_sync(0xffffffffu, grow)) {   // tensor-memory access is warp-wide
             const float a = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_approx(m - mnew));
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 float v[32];
-                tmem_ld32(tmem_o + lane_base + 32 * u, v);
+                uint32_t w[32];
+                tmem_ld32(tmem + lane_base + kColO + col0 + 32 * u, v);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) v[c] *= a;
-                tmem_st32(tmem_o + lane_base + 32 * u, v);
+                for (int c = 0; c < 32; ++c) w[c] = __float_as_uint(v[c] * a);
+                tmem_st32(tmem + lane_base + kColO + col0 + 32 * u, w);
             }
             l *= a;
         }
         m = mnew;
         const float ms = (m == -INFINITY) ? 0.f : m;
-
-        // P = exp2(s - m) as bf16 hi + lo into the two P tiles, l += sum P
+        // (e) P(t) = exp2(s - m) as bf16 pairs (key 2i in the low half), hi and lo parts, l += sum P
+        {
+            uint32_t ph[32], pl[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {   // 8 keys = one 16-byte chunk of the P tiles
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float pv[2];
-#pragma unroll
-                for (int w2 = 0; w2 < 2; ++w2) {
-                    const int e = 8 * q + 2 * u + w2;
-                    pv[w2] = (e < nv) ? exp2_approx(sv[e >> 5][e & 31] - ms) : 0.f;
-                    l += pv[w2];
-                }
-                __nv_bfloat162 hv = __floats2bfloat162_rn(pv[0], pv[1]);
-                hi[u] = *reinterpret_cast<uint32_t*>(&hv);
-                lo[u] = pack2_bf16(pv[0] - __low2float(hv), pv[1] - __high2float(hv));
+            for (int k2 = 0; k2 < 32; ++k2) {
+                const int e0 = 2 * k2;
+                const float p0 = (e0 < nv) ? exp2_approx(sv[e0 >> 5][e0 & 31] - ms) : 0.f;
+                const float p1 = (e0 + 1 < nv) ? exp2_approx(sv[(e0 + 1) >> 5][(e0 + 1) & 31] - ms) : 0.f;
+                l += p0 + p1;
+                __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
+                ph[k2] = *reinterpret_cast<uint32_t*>(&hv);
+                pl[k2] = pack2_bf16(p0 - __low2float(hv), p1 - __high2float(hv));
             }
-            const uint32_t off = sw128(lrow, col0 + 8 * q, kTcRows);
-            *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            tmem_st32(tmem + lane_base + kColPh + half * 32, ph);
+            tmem_st32(tmem + lane_base + kColPl + half * 32, pl);
         }
-        publish_to_tensor_core();   // also: every thread has read S before the next tile overwrites it
+        // (f) V(t) has landed; O += P_hi V(t) + P_lo V(t) on the tensor cores
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+        publish_to_tensor_core();
         if (tid == 0) {
-            mma_tile(tmem + 128, smem_addr(sPh), smem_addr(sVt), t > 0);
-            mma_tile(tmem + 128, smem_addr(sPl), smem_addr(sVt), true);
+            mma_pv(tmem + kColO, tmem + kColPh, smem_addr(sV(x)), t > 0);
+            mma_pv(tmem + kColO, tmem + kColPl, smem_addr(sV(x)), true);
             mma_commit(&bar_o);
         }
     }
-    if (ntiles > 0) mma_wait(&bar_o, ph_o, p.err);
+    if (ntiles > 0) mma_wait_parity(&bar_o, (unsigned)(ntiles - 1) & 1u, p.err);
 
     // ---- the partial of this row over the prefix (the loads are warp-wide: every lane takes part) -----
     s_xch[tid] = l;
@@ -391,7 +383,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     for (int u = 0; u < 2; ++u) {
         float v[32];
         if (ntiles > 0) {
-            tmem_ld32(tmem_o + lane_base + 32 * u, v);
+            tmem_ld32(tmem + lane_base + kColO + col0 + 32 * u, v);
         } else {
 #pragma unroll
             for (int c = 0; c < 32; ++c) v[c] = 0.f;
