@@ -253,17 +253,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
 
     // Rows j0 .. j0+127 of a prefix head (K or V) into a swizzled tile, keys past P zero; one commit
     // group per call, empty when the tile does not exist, so the group counts below stay fixed.
+    // Thread tid copies 16-byte chunk (tid & 15) of keys key0 + 16 i (i = 0..7) of every tile: the
+    // swizzled offsets of those rows are 2048 i apart, the source rows 16 i * p_st elements apart.
+    const int key0 = tid >> 4;
+    const int chunk = tid & 15;
+    const uint32_t soff0 = sw128(key0, 8 * chunk, kTcKeys);
+    const int64_t goff0 = (int64_t)key0 * p.p_st + 8 * chunk;
+    const int64_t gstep = (int64_t)16 * p.p_st;
     auto load_tile = [&](unsigned char* dst, const uint16_t* src, int t) {
         if (t < ntiles) {
             const int j0 = t * kTcKeys;
-            for (int e = tid; e < kTcKeys * 16; e += kTcThreads) {
-                const int key = e >> 4;
-                const int c = e & 15;
-                unsigned char* d = dst + sw128(key, 8 * c, kTcKeys);
-                if (j0 + key < p.P)
-                    cp16(smem_addr(d), src + (int64_t)(j0 + key) * p.p_st + 8 * c);
-                else
-                    *reinterpret_cast<uint4*>(d) = make_uint4(0u, 0u, 0u, 0u);
+            const uint16_t* g = src + (int64_t)j0 * p.p_st + goff0;
+            const uint32_t d0 = smem_addr(dst) + soff0;
+            if (j0 + kTcKeys <= p.P) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cp16(d0 + 2048 * i, g + i * gstep);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (j0 + key0 + 16 * i < p.P)
+                        cp16(d0 + 2048 * i, g + i * gstep);
+                    else
+                        *reinterpret_cast<uint4*>(dst + soff0 + 2048 * i) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
@@ -314,15 +326,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         load_tile(sK(x), kb, t + 2);
         // (c) the row's maximum over the tile: the two halves trade theirs
         const int nv = lim - (j0 + col0);   // keys of this half that the row sees
+        const bool full = nv >= 64;
         float mt = -INFINITY;
+        if (full && p.qscale > 0.f) {   // max of the raw logits, scaled once
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const float xs = sv[u][jj] * p.qscale;
-                sv[u][jj] = xs;
-                if (32 * u + jj < nv) mt = fmaxf(mt, xs);
-            }
+                for (int jj = 0; jj < 32; ++jj) mt = fmaxf(mt, sv[u][jj]);
+            mt *= p.qscale;
+        } else {
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    if (32 * u + jj < nv) mt = fmaxf(mt, sv[u][jj] * p.qscale);
+        }
         s_xch[tid] = mt;
         __syncthreads();
         mt = fmaxf(mt, s_xch[tid ^ kTcRows]);
@@ -350,15 +368,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         // (e) P(t) = exp2(s - m) as bf16 pairs (key 2i in the low half), hi and lo parts, l += sum P
         {
             uint32_t ph[32], pl[32];
-#pragma unroll
-            for (int k2 = 0; k2 < 32; ++k2) {
-                const int e0 = 2 * k2;
-                const float p0 = (e0 < nv) ? exp2_approx(sv[e0 >> 5][e0 & 31] - ms) : 0.f;
-                const float p1 = (e0 + 1 < nv) ? exp2_approx(sv[(e0 + 1) >> 5][(e0 + 1) & 31] - ms) : 0.f;
+            auto pair = [&](int k2, float p0, float p1) {
                 l += p0 + p1;
                 __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
                 ph[k2] = *reinterpret_cast<uint32_t*>(&hv);
                 pl[k2] = pack2_bf16(p0 - __low2float(hv), p1 - __high2float(hv));
+            };
+            const float qs = p.qscale;
+            if (full) {
+#pragma unroll
+                for (int k2 = 0; k2 < 32; ++k2) {
+                    const int e0 = 2 * k2;
+                    pair(k2, exp2_approx(fmaf(sv[e0 >> 5][e0 & 31], qs, -ms)),
+                         exp2_approx(fmaf(sv[e0 >> 5][(e0 & 31) + 1], qs, -ms)));
+                }
+            } else {
+#pragma unroll
+                for (int k2 = 0; k2 < 32; ++k2) {
+                    const int e0 = 2 * k2;
+                    pair(k2, e0 < nv ? exp2_approx(fmaf(sv[e0 >> 5][e0 & 31], qs, -ms)) : 0.f,
+                         e0 + 1 < nv ? exp2_approx(fmaf(sv[e0 >> 5][(e0 & 31) + 1], qs, -ms)) : 0.f);
+                }
             }
             tmem_st32(tmem + lane_base + kColPh + half * 32, ph);
             tmem_st32(tmem + lane_base + kColPl + half * 32, pl);
