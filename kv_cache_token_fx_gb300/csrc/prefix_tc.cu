@@ -162,6 +162,41 @@ __device__ __forceinline__ float exp2_approx(float x)
     return y;
 }
 
+// Paired fp32 arithmetic (one instruction for two lanes of a pair) and a three-input maximum.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float a, float b)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -332,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) mt = fmaxf(mt, sv[u][jj]);
+                for (int jj = 0; jj < 32; jj += 2) mt = max3(mt, sv[u][jj], sv[u][jj + 1]);
             mt *= p.qscale;
         } else {
 #pragma unroll
@@ -368,28 +403,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         // (e) P(t) = exp2(s - m) as bf16 pairs (key 2i in the low half), hi and lo parts, l += sum P
         {
             uint32_t ph[32], pl[32];
+            float2 l2 = make_float2(0.f, 0.f);
             auto pair = [&](int k2, float p0, float p1) {
-                l += p0 + p1;
+                const float2 pp = make_float2(p0, p1);
+                l2 = add2(l2, pp);
                 __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
                 ph[k2] = *reinterpret_cast<uint32_t*>(&hv);
-                pl[k2] = pack2_bf16(p0 - __low2float(hv), p1 - __high2float(hv));
+                const float2 lo = sub2(pp, make_float2(__low2float(hv), __high2float(hv)));
+                pl[k2] = pack2_bf16(lo.x, lo.y);
             };
-            const float qs = p.qscale;
+            const float2 qs2 = make_float2(p.qscale, p.qscale);
+            const float2 nms2 = make_float2(-ms, -ms);
             if (full) {
 #pragma unroll
                 for (int k2 = 0; k2 < 32; ++k2) {
                     const int e0 = 2 * k2;
-                    pair(k2, exp2_approx(fmaf(sv[e0 >> 5][e0 & 31], qs, -ms)),
-                         exp2_approx(fmaf(sv[e0 >> 5][(e0 & 31) + 1], qs, -ms)));
+                    const float2 x2 = fma2(make_float2(sv[e0 >> 5][e0 & 31], sv[e0 >> 5][(e0 & 31) + 1]), qs2, nms2);
+                    pair(k2, exp2_approx(x2.x), exp2_approx(x2.y));
                 }
             } else {
 #pragma unroll
                 for (int k2 = 0; k2 < 32; ++k2) {
                     const int e0 = 2 * k2;
-                    pair(k2, e0 < nv ? exp2_approx(fmaf(sv[e0 >> 5][e0 & 31], qs, -ms)) : 0.f,
-                         e0 + 1 < nv ? exp2_approx(fmaf(sv[e0 >> 5][(e0 & 31) + 1], qs, -ms)) : 0.f);
+                    const float2 x2 = fma2(make_float2(sv[e0 >> 5][e0 & 31], sv[e0 >> 5][(e0 & 31) + 1]), qs2, nms2);
+                    pair(k2, e0 < nv ? exp2_approx(x2.x) : 0.f, e0 + 1 < nv ? exp2_approx(x2.y) : 0.f);
                 }
             }
+            l += l2.x + l2.y;
             tmem_st32(tmem + lane_base + kColPh + half * 32, ph);
             tmem_st32(tmem + lane_base + kColPl + half * 32, pl);
         }
