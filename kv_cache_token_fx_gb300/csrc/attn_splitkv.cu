@@ -823,59 +823,65 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     __shared__ float c_m[kMaxRowsPerCta];
     __shared__ float c_l[kMaxRowsPerCta];
     float* c_o = sm_o;   // [16][128]: combined in place over warp 0's slice (each element by its own thread)
-    if (!need_v) {
-        // scores only: the row maxima and sums are all that is merged
-        for (int r = tid; r < nr; r += kThreads) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][r]);
-            const float Ms = (M == -INFINITY) ? 0.f : M;
-            float Ls = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) Ls = fmaf(sm_l[w][r], fast_exp2(sm_m[w][r] - Ms), Ls);
-            c_m[r] = M;
-            c_l[r] = Ls;
-        }
-    } else
-    for (int e = tid; e < nr * kHeadDim; e += kThreads) {
-        const int r = e >> 7;
-        const int c = e & (kHeadDim - 1);
+    // merge weights, in the (now free) stage buffers after the warp partials: per row, each warp's
+    // weight, each cluster peer's, the external partial's, and the output row offset
+    float* s_f = sm_o + kWarps * kRowsPerCta * kHeadDim;   // [kWarps][kMaxRowsPerCta]
+    float* s_fp = s_f + kWarps * kMaxRowsPerCta;           // [kMaxClusterSplits][kMaxRowsPerCta]
+    float* s_fe = s_fp + kMaxClusterSplits * kMaxRowsPerCta;
+    int64_t* s_orow = reinterpret_cast<int64_t*>(s_fe + kMaxRowsPerCta);
+    static_assert((kWarps * kRowsPerCta * kHeadDim + (kWarps + kMaxClusterSplits + 1) * kMaxRowsPerCta) * 4 +
+                          kMaxRowsPerCta * 8 <= kWarps * kWarpBytes,
+                  "merge scratch fits the stage buffers");
+    // per row, once: the CTA's maximum and sum, and each warp's weight 2^(m_w - M)
+    if (tid < nr) {
+        const int r = tid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][r]);
         const float Ms = (M == -INFINITY) ? 0.f : M;
-        float O = 0.f, Ls = 0.f;
+        float Ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float sc = fast_exp2(sm_m[w][r] - Ms);
-            O = fmaf(sm_o[(w * kRowsPerCta + r) * kHeadDim + c], sc, O);
-            Ls = fmaf(sm_l[w][r], sc, Ls);
+            const float f = fast_exp2(sm_m[w][r] - Ms);
+            Ls = fmaf(sm_l[w][r], f, Ls);
+            s_f[w * kMaxRowsPerCta + r] = f;
         }
-        c_o[r * kHeadDim + c] = O;
-        if (c == 0) {
-            c_m[r] = M;
-            c_l[r] = Ls;
-        }
+        c_m[r] = M;
+        c_l[r] = Ls;
     }
+    __syncthreads();
+    // the CTA's combined partial O, relative to its own row maxima
+    auto combined4 = [&](int r, int c) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float f = s_f[w * kMaxRowsPerCta + r];
+            const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * kRowsPerCta + r) * kHeadDim + c);
+            o.x = fmaf(v.x, f, o.x);
+            o.y = fmaf(v.y, f, o.y);
+            o.z = fmaf(v.z, f, o.z);
+            o.w = fmaf(v.w, f, o.w);
+        }
+        return o;
+    };
 
     if constexpr (MERGE == kMergePush) {
         static_assert(NR != 32, "scoring-only tiles merge through the workspace");
-        // CTAs 1 .. cs-1 send their partial into CTA 0's receive area with asynchronous remote stores
-        // that count their bytes on CTA 0's barrier, and exit at once; CTA 0 announces the bytes it
-        // expects, waits for them and merges alone.
+        // CTAs 1 .. cs-1 send their combined partial into CTA 0's receive area with asynchronous remote
+        // stores that count their bytes on CTA 0's barrier, and exit at once; CTA 0 announces the bytes
+        // it expects, waits for them and merges alone.
         __shared__ __align__(16) float s_recv[kRecvFloats];   // [cs-1][nr][128] O, [cs-1][nr] m, [cs-1][nr] l
         const unsigned cs = cluster_size();
         const unsigned me = cluster_rank();
         const int npeer = (int)cs - 1;
         float* recv_m = s_recv + npeer * nr * kHeadDim;
         float* recv_l = recv_m + npeer * nr;
-        __syncthreads();          // the combined partial (written by all threads) is complete
         cluster_wait_acquire();   // CTA 0's barrier is initialised
         if (me != 0) {
             const uint32_t rbar = cluster_map(&s_merge_bar, 0);
             const uint32_t dst = cluster_map(s_recv + (me - 1) * nr * kHeadDim, 0);
             for (int e = tid; e < nr * (kHeadDim / 4); e += kThreads)
-                st_async_v4(dst + 16 * e, *reinterpret_cast<const float4*>(c_o + 4 * e), rbar);
+                st_async_v4(dst + 16 * e, combined4(e >> 5, 4 * (e & 31)), rbar);
             if (tid < nr) {
                 st_async_f32(cluster_map(recv_m + (me - 1) * nr + tid, 0), c_m[tid], rbar);
                 st_async_f32(cluster_map(recv_l + (me - 1) * nr + tid, 0), c_l[tid], rbar);
@@ -892,28 +898,52 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 }
             }
         }
+        // per row, once: the weights of this CTA's warps, of each peer and of the external partial,
+        // with the normalisation 1 / L folded in, and the output row's offset
+        if (tid < nr) {
+            const int r = tid;
+            const float me_ = s_ext_m[r];
+            float M = fmaxf(c_m[r], me_);
+            for (int q = 0; q < npeer; ++q) M = fmaxf(M, recv_m[q * nr + r]);
+            const float Ms = (M == -INFINITY) ? 0.f : M;
+            const float a0 = fast_exp2(c_m[r] - Ms);
+            const float ae = fast_exp2(me_ - Ms);
+            float Ls = fmaf(c_l[r], a0, s_ext_l[r] * ae);
+            for (int q = 0; q < npeer; ++q) {
+                const float aq = fast_exp2(recv_m[q * nr + r] - Ms);
+                Ls = fmaf(recv_l[q * nr + r], aq, Ls);
+                s_fp[q * kMaxRowsPerCta + r] = aq;
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) s_f[w * kMaxRowsPerCta + r] *= a0 * inv;
+            for (int q = 0; q < npeer; ++q) s_fp[q * kMaxRowsPerCta + r] *= inv;
+            s_fe[r] = ae * inv;
+            const int row = r0 + r;
+            const int gi = row / p.Mq;
+            const int i = row - gi * p.Mq;
+            s_orow[r] = (((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7;
+        }
+        __syncthreads();
         const int c = tid;
 #pragma unroll
         for (int r = 0; r < kExtRows; ++r) {
             if (r >= nr) break;
-            float M = c_m[r];
-            for (int q = 0; q < npeer; ++q) M = fmaxf(M, recv_m[q * nr + r]);
-            const float Ms = (M == -INFINITY) ? 0.f : M;
-            float w = fast_exp2(c_m[r] - Ms);
-            float Ls = c_l[r] * w;
-            float O = c_o[r * kHeadDim + c] * w;
-            for (int q = 0; q < npeer; ++q) {
-                w = fast_exp2(recv_m[q * nr + r] - Ms);
-                Ls = fmaf(recv_l[q * nr + r], w, Ls);
-                O = fmaf(s_recv[(q * nr + r) * kHeadDim + c], w, O);
-            }
-            const int row = r0 + r;
-            const int gi = row / p.Mq;
-            const int i = row - gi * p.Mq;
-            p.out[((((int64_t)b * p.Hq + h * p.G + gi) * p.Mq + i) << 7) + c] =
-                finish_row(s_ext_m[r], s_ext_l[r], ext_oc[r], M, Ms, Ls, O);
+            float O = ext_oc[r] * s_fe[r];
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) O = fmaf(sm_o[(w * kRowsPerCta + r) * kHeadDim + c], s_f[w * kMaxRowsPerCta + r], O);
+            for (int q = 0; q < npeer; ++q) O = fmaf(s_recv[(q * nr + r) * kHeadDim + c], s_fp[q * kMaxRowsPerCta + r], O);
+            p.out[s_orow[r] + c] = O;
         }
         return;
+    }
+
+    // pull and workspace merges start from the CTA's combined partial
+    if (need_v) {
+        for (int e = tid; e < nr * (kHeadDim / 4); e += kThreads) {
+            const float4 o = combined4(e >> 5, 4 * (e & 31));
+            *reinterpret_cast<float4*>(c_o + 4 * e) = o;   // each element is read above by its own thread only
+        }
     }
 
     if constexpr (MERGE == kMergePull) {
