@@ -64,6 +64,14 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
 }
+// Byte offset of 16-byte chunk `chunk` (0..15) of row `row` in a staged K or V sub-tile: rows are
+// 256 bytes apart and the chunk index is XORed with (row % 8), so the 8 rows an ldmatrix reads at one
+// column fall on 8 distinct bank groups without padding.
+__device__ __forceinline__ uint32_t kv_off(int row, int chunk)
+{
+    return (uint32_t)(row * kKvPitch + ((chunk ^ (row & 7)) << 4));
+}
+
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -365,8 +373,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 const uint16_t* kp = src.kb + __shfl_sync(kFull, mko, r);
                 const uint16_t* vp = src.vb + (MODE == kModePrefix ? __shfl_sync(kFull, mvo, r)
                                                                    : __shfl_sync(kFull, mko, r));
-                unsigned char* dk = stage + (size_t)r * kPitch + 16 * c16;
-                unsigned char* dv = dk + kSub * kPitch;
+                unsigned char* dk = stage + kv_off(r, c16);
+                unsigned char* dv = dk + kSub * kKvPitch;
                 if ((vmask >> r) & 1u) {
                     cp_async16(smem_addr(dk), kp + 8 * c16);
                     if (need_v) cp_async16(smem_addr(dv), vp + 8 * c16);
@@ -489,7 +497,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         cp_async_wait_stages();
         __syncwarp();
         const unsigned char* sk = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
-        const unsigned char* sv = sk + kSub * kPitch;
+        const unsigned char* sv = sk + kSub * kKvPitch;
         const uint32_t vmask = s_vmask[warp][j % kWarpStages];
 
         if constexpr (NR == 32) {
@@ -505,7 +513,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(smem_addr(sk + krow * kPitch + (16 * ks + kcol) * 2), a0, a1, a2, a3);
+                    ldsm_x4(smem_addr(sk + kv_off(krow, (16 * ks + kcol) >> 3)), a0, a1, a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < kNT; ++nt) mma_bf16(acc[nt], a0, a1, a2, a3, qf[ks][2 * nt], qf[ks][2 * nt + 1]);
                 }
@@ -553,8 +561,8 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
                 for (int ks = 0; ks < 8; ks += 2) {
                     uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-                    ldsm_x4(smem_addr(sk + krow * kPitch + (16 * ks + kcol) * 2), a0, a1, a2, a3);
-                    ldsm_x4(smem_addr(sk + krow * kPitch + (16 * ks + 16 + kcol) * 2), c0, c1, c2, c3);
+                    ldsm_x4(smem_addr(sk + kv_off(krow, (16 * ks + kcol) >> 3)), a0, a1, a2, a3);
+                    ldsm_x4(smem_addr(sk + kv_off(krow, (16 * ks + 16 + kcol) >> 3)), c0, c1, c2, c3);
                     mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
                     mma_bf16(sb, c0, c1, c2, c3, qf[ks + 1][0], qf[ks + 1][1]);
                 }
@@ -616,7 +624,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * mt + vcol) * 2), a0, a1, a2, a3);
+                    ldsm_x4_t(smem_addr(sv + kv_off(vrow, (16 * mt + vcol) >> 3)), a0, a1, a2, a3);
                     mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
                     mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
                 }
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
                 for (int kp = 0; kp < 4; ++kp) {     // pairs of k-steps
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(smem_addr(sk + krow * kPitch + (32 * kp + kcol) * 2), b0, b1, b2, b3);
+                    ldsm_x4(smem_addr(sk + kv_off(krow, (32 * kp + kcol) >> 3)), b0, b1, b2, b3);
                     mma_bf16(s[nt], qf[2 * kp][0], qf[2 * kp][1], qf[2 * kp][2], qf[2 * kp][3], b0, b1);
                     mma_bf16(s[nt], qf[2 * kp + 1][0], qf[2 * kp + 1][1], qf[2 * kp + 1][2], qf[2 * kp + 1][3], b2, b3);
                 }
@@ -715,7 +723,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
                 for (int np2 = 0; np2 < 8; ++np2) {   // pairs of 8-dim n-tiles
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_addr(sv + vrow * kPitch + (16 * np2 + vcol) * 2), b0, b1, b2, b3);
+                    ldsm_x4_t(smem_addr(sv + kv_off(vrow, (16 * np2 + vcol) >> 3)), b0, b1, b2, b3);
                     mma_bf16(o[2 * np2], ph[0], ph[1], ph[2], ph[3], b0, b1);
                     mma_bf16(o[2 * np2], pl[0], pl[1], pl[2], pl[3], b0, b1);
                     mma_bf16(o[2 * np2 + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);

@@ -19,9 +19,10 @@ constexpr int kSub = 16;                                // keys per warp sub-til
 constexpr float kMaxSlack = 8.f;                       // online-softmax maximum slack (log2 units)
 constexpr int kWarpStages = 3;                          // sub-tiles in flight per warp
 constexpr int kRowsPerCta = 16;                         // query rows per CTA: one m16 MMA tile
-constexpr int kPitch = kRowBytes + 16;                  // staged row pitch: the 16-byte pad puts the 8
+constexpr int kPitch = kRowBytes + 16;                  // query tile row pitch: the 16-byte pad puts the 8
                                                         // rows of an ldmatrix on 8 distinct bank groups
-constexpr int kSubBytes = 2 * kSub * kPitch;            // K and V rows of one sub-tile (8.5 KB)
+constexpr int kKvPitch = kRowBytes;                     // staged K / V rows: unpadded, chunk-swizzled
+constexpr int kSubBytes = 2 * kSub * kKvPitch;          // K and V rows of one sub-tile (8 KB)
 constexpr int kWarpBytes = kWarpStages * kSubBytes;     // one warp's ring of sub-tile buffers
 constexpr int kTile = kWarps * kSub;                    // split lengths are multiples of this (whole sub-tiles per warp)
 constexpr int kMaxSplitTokens = 4096;                   // gathered rows longer than 16 such splits merge in the workspace
