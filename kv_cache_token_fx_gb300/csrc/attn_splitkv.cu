@@ -5,11 +5,12 @@
 // the split and walks it on its own:
 //   * Data movement: the warp stages its sub-tiles (16 K rows + 16 V rows of 256 bytes; contiguous
 //     rows for the focal mode, gathered rows for the sparse/prefix modes) into a private ring of
-//     kWarpStages buffers with 16-byte cp.async, each warp instruction moving two whole rows, one
-//     commit group per sub-tile, so no CTA-wide barrier is needed in the loop.  Lane l resolves the
-//     token of row l & 15 (one index load per lane); the copies take the row addresses by warp
-//     shuffle and a ballot records which rows are valid.  Rows are padded to 272 bytes so that the
-//     8-row ldmatrix reads hit 8 different bank groups; invalid rows are zero-filled.  (Per-row
+//     2 or 3 buffers (attn_stages) with 16-byte cp.async, each warp instruction moving two whole
+//     rows, one commit group per sub-tile, so no CTA-wide barrier is needed in the loop.  Lane l
+//     resolves the token of row l & 15 (one index load per lane); the copies take the row addresses
+//     by warp shuffle and a ballot records which rows are valid.  Within a row the 16-byte chunk index
+//     is XORed with (row % 8), so the 8-row ldmatrix reads hit 8 different bank groups without
+//     padding; invalid rows are zero-filled.  (Per-row
 //     cp.async.bulk TMA copies were measured slower here: 256-byte requests keep the TMA engine, not
 //     HBM, busy.)
 //   * Math: mma.sync m16n8k16 (bf16 in, fp32 accumulate), online softmax on the accumulator
@@ -51,10 +52,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-// all of this thread's commit groups but the newest kWarpStages-1 have completed
+// all of this thread's commit groups but the newest WS-1 have completed
+template <int WS>
 __device__ __forceinline__ void cp_async_wait_stages()
 {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(kWarpStages - 1) : "memory");
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(WS - 1) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all_groups() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
@@ -243,8 +245,10 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* sQ = smem + 128;                                      // [16][kPitch] bf16
-    unsigned char* sKV = sQ + attn_q_rows(NR) * kPitch;                  // [kWarps][kWarpStages][K, V]
-    __shared__ uint32_t s_vmask[kWarps][kWarpStages];   // valid-row bits of each staged sub-tile
+    constexpr int WS = attn_stages(MODE);                               // sub-tiles in flight per warp
+    constexpr int kWarpBytes = WS * kSubBytes;                          // one warp's ring of sub-tile buffers
+    unsigned char* sKV = sQ + attn_q_rows(NR) * kPitch;                  // [kWarps][WS][K, V]
+    __shared__ uint32_t s_vmask[kWarps][WS];   // valid-row bits of each staged sub-tile
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -289,9 +293,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     const int s0 = split * p.split_len;
     int wl = p.split_len / kWarps;
     int ws = s0 + warp * wl;
-    int tpre[kWarpStages];
+    int tpre[WS];
 #pragma unroll
-    for (int j = 0; j < kWarpStages; ++j) tpre[j] = MODE == kModePrefix ? 0 : src.token(ws + j * kSub + (lane & 15));
+    for (int j = 0; j < WS; ++j) tpre[j] = MODE == kModePrefix ? 0 : src.token(ws + j * kSub + (lane & 15));
 
     if (MODE == kModeFocal || MODE == kModeSparse) {
         int l = p.len[b];
@@ -342,14 +346,14 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         wl = share;
         ws = s0 + warp * share;
 #pragma unroll
-        for (int j = 0; j < kWarpStages; ++j) tpre[j] = src.token(ws + j * kSub + (lane & 15));
+        for (int j = 0; j < WS; ++j) tpre[j] = src.token(ws + j * kSub + (lane & 15));
     }
     const int we = min(s1, ws + wl);
     const int nsub = we > ws ? (we - ws + kSub - 1) / kSub : 0;
 
     // Each warp stages its own sub-tiles (16 K rows + 16 V rows) with 16-byte cp.async operations --
-    // every warp instruction moves two whole rows -- into its private ring of kWarpStages buffers.  One
-    // commit group per sub-tile (empty past the end), so "all but kWarpStages-1 groups done" always
+    // every warp instruction moves two whole rows -- into its private ring of WS buffers.  One
+    // commit group per sub-tile (empty past the end), so "all but WS-1 groups done" always
     // means "the oldest sub-tile has landed".  No CTA-wide barrier is needed inside the loop.
     unsigned char* wbuf = sKV + (size_t)warp * kWarpBytes;
     // a focal call that only scores (no output rows) needs no V rows and no P V products
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     auto issue = [&](int j, int mytok) {
         if (j < nsub) {
             const int c16 = lane & 15;
-            unsigned char* stage = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
+            unsigned char* stage = wbuf + (size_t)(j % WS) * kSubBytes;
             // lane l resolves the token row of key (l & 15) of the sub-tile (one index load per lane);
             // the copies then take each row's address from the lane that resolved it
             const int mypos = ws + j * kSub + (lane & 15);
@@ -383,13 +387,13 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                     if (need_v) *reinterpret_cast<uint4*>(dv) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            if (lane == 0) s_vmask[warp][j % kWarpStages] = vmask;
+            if (lane == 0) s_vmask[warp][j % WS] = vmask;
         }
         cp_async_commit();
     };
 
 #pragma unroll
-    for (int j = 0; j < kWarpStages; ++j) issue(j, tpre[j]);
+    for (int j = 0; j < WS; ++j) issue(j, tpre[j]);
 
     // The query rows may be written by the preceding kernel, so they are read only after the wait
     // below; a prefetch into L2 is only a hint (L2 stays coherent with later writes) and shortens that
@@ -493,12 +497,12 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     }
     for (int j = 0; j < nsub; ++j) {
         const int base = ws + j * kSub;   // first key of this sub-tile
-        const int tnext = src.token(base + kWarpStages * kSub + (lane & 15));   // for the refill below
-        cp_async_wait_stages();
+        const int tnext = src.token(base + WS * kSub + (lane & 15));   // for the refill below
+        cp_async_wait_stages<WS>();
         __syncwarp();
-        const unsigned char* sk = wbuf + (size_t)(j % kWarpStages) * kSubBytes;
+        const unsigned char* sk = wbuf + (size_t)(j % WS) * kSubBytes;
         const unsigned char* sv = sk + kSub * kKvPitch;
-        const uint32_t vmask = s_vmask[warp][j % kWarpStages];
+        const uint32_t vmask = s_vmask[warp][j % WS];
 
         if constexpr (NR == 32) {
             // S^T = K Q^T for 4 n-tiles of 8 query rows; each K fragment serves all four
@@ -733,7 +737,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         }
 
         __syncwarp();      // every lane is done with this buffer before it is refilled
-        issue(j + kWarpStages, tnext);
+        issue(j + WS, tnext);
     }
     // the external partial of these rows (column tid of each; kThreads == kHeadDim), loaded now so its
     // latency overlaps the combine below
@@ -838,7 +842,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     float* s_fe = s_fp + kMaxClusterSplits * kMaxRowsPerCta;
     int64_t* s_orow = reinterpret_cast<int64_t*>(s_fe + kMaxRowsPerCta);
     static_assert((kWarps * kRowsPerCta * kHeadDim + (kWarps + kMaxClusterSplits + 1) * kMaxRowsPerCta) * 4 +
-                          kMaxRowsPerCta * 8 <= kWarps * kWarpBytes,
+                          kMaxRowsPerCta * 8 <= kWarps * 2 * kSubBytes,
                   "merge scratch fits the stage buffers");
     // per row, once: the CTA's maximum and sum, and each warp's weight 2^(m_w - M)
     if (tid < nr) {
@@ -1115,7 +1119,7 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
     const bool cluster = MERGE != kMergeWorkspace;
     if (configured != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_smem_bytes(NR));
+                                             (int)attn_smem_bytes(NR, MODE));
         if (e != cudaSuccess) return e;
         if (cluster) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1123,7 +1127,7 @@ cudaError_t launch_one(const AttnParams& p, bool pdl, cudaStream_t s)
         }
         configured = dev;
     }
-    const size_t smem = attn_smem_bytes(NR);
+    const size_t smem = attn_smem_bytes(NR, MODE);
     dim3 grid(p.nrg, p.nsplit, p.B * p.Hkv);
     // merged in a cluster: every split of one (b, h, row group) is one CTA of a (1, nsplit, 1) cluster
     return launch_kernel(kern, grid, dim3(kThreads), smem, s, pdl, cluster ? (unsigned)p.nsplit : 0u, p);
