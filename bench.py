@@ -563,10 +563,34 @@ def run_reference(args, rank, local, ws):
     print(json.dumps(line), flush=True)
 
 
+def run_hpd_case(args):
+    """The dense shared-prefix verify call of one hpd_branch layer (1.14 GB of inputs: tensor-core prefix
+    kernel, then the verify kernel), `--reps` times, for profiler captures."""
+    import kv_cache_token_fx_gb300 as fx
+    from synth.workloads import HpdBranch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = HpdBranch()
+    d = w.layer_inputs(0, device=dev)
+    out = torch.empty((w.Br, w.Hq, w.Mq, D), dtype=torch.float32, device=dev)
+    ws = fx.Workspace(dev, fx.fx_shared_prefix_workspace_bytes(w.Br, w.Hkv, w.Hq, w.Mq, w.P, w.max_suffix))
+    for _ in range(args.reps):
+        fx.fx_shared_prefix_decode(d["pk"], d["pv"], d["sk"], d["sv"], d["off"], d["dk"], d["dv"], d["q"],
+                                   max_suffix=w.max_suffix, out=out, ws=ws)
+    torch.cuda.synchronize()
+    bits = fx.fx_device_errors()
+    print(json.dumps({"kernel_case": "hpd", "reps": args.reps, "device_errors": bits}))
+    if bits:
+        raise SystemExit(1)
+
+
 def run_kernel_case(args):
     """A small, fixed case of one kernel for profiler captures: the decode-shaped call on `--layers`
     distinct layers (each layer's KV is 160 MB, so even one layer exceeds L2), `--reps` passes."""
     import kv_cache_token_fx_gb300 as fx
+    if args.kernel_case == "hpd":
+        run_hpd_case(args)
+        return
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     w = OcrDecode()
@@ -819,7 +843,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk"], default=None,
+    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk", "hpd"], default=None,
                     help="run a small fixed case of one kernel (for profiler captures) instead of the bench")
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--reps", type=int, default=2)
