@@ -768,7 +768,10 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     const int nr = min(NR, p.R - r0);   // rows of this group that exist
     __shared__ float sm_m[kWarps][kMaxRowsPerCta];
     __shared__ float sm_l[kWarps][kMaxRowsPerCta];
-    float* sm_o = reinterpret_cast<float*>(sKV);   // [kWarps][16][128]
+    // [kWarps][16][kOPitch]: rows padded by 8 floats, so the row-strided fragment stores of the
+    // 16-row path spread over all banks
+    constexpr int kOPitch = kHeadDim + 8;
+    float* sm_o = reinterpret_cast<float*>(sKV);
     if constexpr (NR == 32) {
 #pragma unroll
         for (int i = 0; i < 2 * kNT; ++i) {   // sums over the 16 keys: the 8 lanes of this t4
@@ -797,7 +800,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
         for (int qc = 0; qc < 2; ++qc) {
             const int r = 2 * t4 + qc;
             if (r < nr) {
-                float* dst = sm_o + (warp * kRowsPerCta + r) * kHeadDim + g;
+                float* dst = sm_o + (warp * kRowsPerCta + r) * kOPitch + g;
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     dst[16 * mt] = o[mt][qc];
@@ -819,9 +822,9 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
         for (int n = 0; n < 16; ++n) {   // only the rows that exist
             const int c = 8 * n + 2 * t4;
-            if (g < nr) *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kHeadDim + c) = make_float2(o[n][0], o[n][1]);
+            if (g < nr) *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g) * kOPitch + c) = make_float2(o[n][0], o[n][1]);
             if (g + 8 < nr)
-                *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kHeadDim + c) = make_float2(o[n][2], o[n][3]);
+                *reinterpret_cast<float2*>(sm_o + (warp * kRowsPerCta + g + 8) * kOPitch + c) = make_float2(o[n][2], o[n][3]);
         }
         if (t4 == 0) {
             sm_m[warp][g] = m_run[0];
@@ -834,14 +837,14 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 
     __shared__ float c_m[kMaxRowsPerCta];
     __shared__ float c_l[kMaxRowsPerCta];
-    float* c_o = sm_o;   // [16][128]: combined in place over warp 0's slice (each element by its own thread)
+    float* c_o = sm_o;   // [16][kOPitch]: combined in place over warp 0's slice (each element by its own thread)
     // merge weights, in the (now free) stage buffers after the warp partials: per row, each warp's
     // weight, each cluster peer's, the external partial's, and the output row offset
-    float* s_f = sm_o + kWarps * kRowsPerCta * kHeadDim;   // [kWarps][kMaxRowsPerCta]
+    float* s_f = sm_o + kWarps * kRowsPerCta * kOPitch;    // [kWarps][kMaxRowsPerCta]
     float* s_fp = s_f + kWarps * kMaxRowsPerCta;           // [kMaxClusterSplits][kMaxRowsPerCta]
     float* s_fe = s_fp + kMaxClusterSplits * kMaxRowsPerCta;
     int64_t* s_orow = reinterpret_cast<int64_t*>(s_fe + kMaxRowsPerCta);
-    static_assert((kWarps * kRowsPerCta * kHeadDim + (kWarps + kMaxClusterSplits + 1) * kMaxRowsPerCta) * 4 +
+    static_assert((kWarps * kRowsPerCta * kOPitch + (kWarps + kMaxClusterSplits + 1) * kMaxRowsPerCta) * 4 +
                           kMaxRowsPerCta * 8 <= kWarps * 2 * kSubBytes,
                   "merge scratch fits the stage buffers");
     // per row, once: the CTA's maximum and sum, and each warp's weight 2^(m_w - M)
@@ -868,7 +871,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float f = s_f[w * kMaxRowsPerCta + r];
-            const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * kRowsPerCta + r) * kHeadDim + c);
+            const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * kRowsPerCta + r) * kOPitch + c);
             o.x = fmaf(v.x, f, o.x);
             o.y = fmaf(v.y, f, o.y);
             o.z = fmaf(v.z, f, o.z);
@@ -943,7 +946,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
             if (r >= nr) break;
             float O = ext_oc[r] * s_fe[r];
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) O = fmaf(sm_o[(w * kRowsPerCta + r) * kHeadDim + c], s_f[w * kMaxRowsPerCta + r], O);
+            for (int w = 0; w < kWarps; ++w) O = fmaf(sm_o[(w * kRowsPerCta + r) * kOPitch + c], s_f[w * kMaxRowsPerCta + r], O);
             for (int q = 0; q < npeer; ++q) O = fmaf(s_recv[(q * nr + r) * kHeadDim + c], s_fp[q * kMaxRowsPerCta + r], O);
             p.out[s_orow[r] + c] = O;
         }
@@ -954,7 +957,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     if (need_v) {
         for (int e = tid; e < nr * (kHeadDim / 4); e += kThreads) {
             const float4 o = combined4(e >> 5, 4 * (e & 31));
-            *reinterpret_cast<float4*>(c_o + 4 * e) = o;   // each element is read above by its own thread only
+            *reinterpret_cast<float4*>(c_o + (e >> 5) * kOPitch + 4 * (e & 31)) = o;   // read above by this thread only
         }
     }
 
@@ -979,7 +982,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
                 if ((unsigned)q < cs) {
                     mq[q] = ld_cluster(cluster_map(&c_m[r], q));
                     lq[q] = ld_cluster(cluster_map(&c_l[r], q));
-                    oq[q] = ld_cluster(cluster_map(&c_o[r * kHeadDim + c], q));
+                    oq[q] = ld_cluster(cluster_map(&c_o[r * kOPitch + c], q));
                 } else {
                     mq[q] = -INFINITY;
                     lq[q] = 0.f;
@@ -1011,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads) attn_tile_kernel(const AttnParams p)
     for (int r = 0; r < nr; ++r) {
         const int64_t pi = (int64_t)(bh * p.R + r0 + r) * p.nsplit + split;
         if (need_v)
-            for (int c = tid; c < kHeadDim; c += kThreads) p.part_o[pi * kHeadDim + c] = c_o[r * kHeadDim + c];
+            for (int c = tid; c < kHeadDim; c += kThreads) p.part_o[pi * kHeadDim + c] = c_o[r * kOPitch + c];
         if (tid == 0) {
             p.part_m[pi] = c_m[r];
             p.part_l[pi] = c_l[r];
