@@ -10,11 +10,11 @@
 // more than a fixed slack, so O is rescaled rarely), P split into bf16 hi + lo parts (two products) so
 // the probabilities keep about 16 bits.  Two threads own one query row, each for half of the keys of a
 // tile and half of O: they read their S columns from tensor memory, trade the row maximum, and write
-// P back into tensor memory, where the P V product takes it as its A operand.  Q and K tiles are
+// P back into tensor memory (two buffers), where the P V product takes it as its A operand.  Q and K tiles are
 // K-major operands with the 128-byte swizzle; V tiles are copied as they are stored (keys x dims) into
-// the same swizzled layout and used as an MN-major operand, so nothing is transposed.  S is double
-// buffered in tensor memory and K, V in shared memory: the next tile's Q K^T runs on the tensor cores
-// while this tile's softmax runs on the threads.
+// the same swizzled layout and used as an MN-major operand, so nothing is transposed.  P is double
+// buffered in tensor memory and K, V in shared memory: the next tile's Q K^T and the previous tile's
+// P V run on the tensor cores while this tile's softmax runs on the threads.
 // The result per row is a partial (m, l, O) over the prefix, which the verify kernel folds into its
 // merge of the suffix and draft keys.
 #include <cuda_bf16.h>
@@ -29,9 +29,9 @@ constexpr int kTcRows = 128;                       // query rows per CTA (one te
 constexpr int kTcKeys = 128;                       // prefix keys per tile
 constexpr int kTcThreads = 256;                    // two threads per query row
 constexpr int kTileBytes = kTcRows * kHeadDim * 2;  // one 128 x 128 bf16 operand tile
-// tensor-memory columns: S of even and odd tiles, O, and P (bf16 pairs: hi then lo)
+// tensor-memory columns: S, O, and P of even and odd tiles (bf16 pairs: 64 columns hi, then 64 lo)
 constexpr int kTmemCols = 512;
-constexpr int kColS0 = 0, kColS1 = 128, kColO = 256, kColPh = 384, kColPl = 448;
+constexpr int kColS = 0, kColO = 128, kColP0 = 256, kColP1 = 384;
 // [Q | K even | K odd | V even | V odd] swizzled tiles and slack to align to 1024 bytes
 constexpr size_t kTcSmem = 5 * (size_t)kTileBytes + 1024;
 
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     unsigned char* sQ = base;
     auto sK = [&](int x) { return base + (1 + x) * kTileBytes; };   // K tiles of even / odd tiles
     auto sV = [&](int x) { return base + (3 + x) * kTileBytes; };   // V tiles of even / odd tiles
-    __shared__ __align__(8) uint64_t bar_s[2];   // S of an even / odd tile is in tensor memory
+    __shared__ __align__(8) uint64_t bar_s;      // S of the current tile is in tensor memory
     __shared__ __align__(8) uint64_t bar_o;      // O += P V of the last issued tile is done
     __shared__ uint32_t s_tmem;
     __shared__ int s_lim_max;
@@ -255,8 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     }
     if (tid == 0) {
         s_lim_max = 0;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s[0])));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s[1])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_s)));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_o)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -316,11 +315,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
 
-    // Pipeline over the prefix tiles t = 0 .. ntiles-1 (x = t & 1 picks the buffers): K(t) -> sK(x),
-    // V(t) -> sV(x), S(t) = Q K(t)^T -> tensor-memory S[x], P(t) -> the P columns, O += P(t) V(t).
-    // S(t+1) runs on the tensor cores while the threads turn S(t) into P(t); K(t+2) is copied as soon as
-    // S(t) is done, V(t+1) as soon as P(t-1) V(t-1) is done.  Commit groups: K(0), V(0), K(1) before the
-    // loop, then K(t+2) and V(t+1) per tile (empty past the end), so the waits below count fixed groups.
+    // Pipeline over the prefix tiles t = 0 .. ntiles-1 (x = t & 1 picks the K, V and P buffers):
+    // K(t) -> sK(x), V(t) -> sV(x), S(t) = Q K(t)^T -> tensor-memory S, P(t) -> tensor-memory P[x],
+    // O += P(t) V(t).  Per tile the threads (b) read S(t), (c) trade row maxima -- after which S(t+1) is
+    // issued into the same S columns --, (d) rescale O if the maximum moved, (e) write P(t), and (f)
+    // issue P(t) V(t).  With P double buffered nothing waits for the previous P V product except a
+    // rescale (rare) and the reuse of a V buffer, a whole tile later; the tensor cores run S(t+1) and
+    // P(t-1) V(t-1) while the threads work on tile t.  K(t+2) is copied as soon as S(t) is done, V(t+1)
+    // as soon as P(t-1) V(t-1) is.  Commit groups: K(0), V(0), K(1) before the loop, then K(t+2) and
+    // V(t+1) per tile (empty past the end), so the waits below count fixed groups.
     // Online softmax: a row's running maximum m moves only when a tile's maximum exceeds it by more than
     // kMaxSlack (log2 units); O in tensor memory is then rescaled by the row's threads, and
     // P = exp2(s - m) stays below 2^kMaxSlack.
@@ -333,33 +336,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         asm volatile("cp.async.wait_group 2;" ::: "memory");   // K(0)
         publish_to_tensor_core();
         if (tid == 0) {
-            mma_qk(tmem + kColS0, smem_addr(sQ), smem_addr(sK(0)));
-            mma_commit(&bar_s[0]);
+            mma_qk(tmem + kColS, smem_addr(sQ), smem_addr(sK(0)));
+            mma_commit(&bar_s);
         }
     }
     for (int t = 0; t < ntiles; ++t) {
         const int x = t & 1;
         const int j0 = t * kTcKeys;
-        const uint32_t col_s = x ? kColS1 : kColS0;
-        // (a) S(t+1) onto the tensor cores; its S columns held S(t-1), which every thread has read
-        if (t + 1 < ntiles) {
-            if (t == 0)
-                asm volatile("cp.async.wait_group 0;" ::: "memory");   // K(1)
-            else
-                asm volatile("cp.async.wait_group 1;" ::: "memory");   // K(t+1); V(t) may be in flight
-            publish_to_tensor_core();
-            if (tid == 0) {
-                mma_qk(tmem + (x ? kColS0 : kColS1), smem_addr(sQ), smem_addr(sK(x ^ 1)));
-                mma_commit(&bar_s[x ^ 1]);
-            }
-        }
+        const uint32_t col_p = x ? kColP1 : kColP0;
         // (b) this half's 64 logits of S(t); the K buffer of tile t is then free for K(t+2)
-        mma_wait_parity(&bar_s[x], (unsigned)(t >> 1) & 1u, p.err);
+        mma_wait_parity(&bar_s, (unsigned)t & 1u, p.err);
         float sv[2][32];
-        tmem_ld32(tmem + lane_base + col_s + col0, sv[0]);
-        tmem_ld32(tmem + lane_base + col_s + col0 + 32, sv[1]);
+        tmem_ld32(tmem + lane_base + kColS + col0, sv[0]);
+        tmem_ld32(tmem + lane_base + kColS + col0 + 32, sv[1]);
         load_tile(sK(x), kb, t + 2);
-        // (c) the row's maximum over the tile: the two halves trade theirs
+        // (c) the row's maximum over the tile: the two halves trade theirs.  The same barrier publishes
+        // K(t+1) to the tensor cores and closes every thread's reads of S(t), so S(t+1) follows it.
         const int nv = lim - (j0 + col0);   // keys of this half that the row sees
         const bool full = nv >= 64;
         float mt = -INFINITY;
@@ -377,15 +369,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
                     if (32 * u + jj < nv) mt = fmaxf(mt, sv[u][jj] * p.qscale);
         }
         s_xch[tid] = mt;
-        __syncthreads();
+        if (t == 0)
+            asm volatile("cp.async.wait_group 1;" ::: "memory");   // K(1)
+        else
+            asm volatile("cp.async.wait_group 2;" ::: "memory");   // K(t+1); V(t) and K(t+2) may fly
+        publish_to_tensor_core();
+        if (tid == 0 && t + 1 < ntiles) {
+            mma_qk(tmem + kColS, smem_addr(sQ), smem_addr(sK(x ^ 1)));
+            mma_commit(&bar_s);
+        }
         mt = fmaxf(mt, s_xch[tid ^ kTcRows]);
         const bool grow = mt > m + kMaxSlack;   // also when m is still -inf and the tile has keys
         const float mnew = grow ? mt : m;
-        // (d) P(t-1) V(t-1) is done: O may be rescaled, the P columns rewritten, V(t+1) copied into the
-        // V buffer of tile t-1
-        if (t > 0) mma_wait_parity(&bar_o, (unsigned)(t - 1) & 1u, p.err);
-        load_tile(sV(x ^ 1), vb, t + 1);
+        // (d) a moved maximum rescales O, once P(t-1) V(t-1) is done
         if (t > 0 && __any_sync(0xffffffffu, grow)) {   // tensor-memory access is warp-wide
+            mma_wait_parity(&bar_o, (unsigned)(t - 1) & 1u, p.err);
             const float a = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2_approx(m - mnew));
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -400,7 +398,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
         }
         m = mnew;
         const float ms = (m == -INFINITY) ? 0.f : m;
-        // (e) P(t) = exp2(s - m) as bf16 pairs (key 2i in the low half), hi and lo parts, l += sum P
+        // (e) P(t) = exp2(s - m) as bf16 pairs (key 2i in the low half), hi and lo parts, l += sum P; the
+        // P buffer of tile t was last read by P(t-2) V(t-2), finished before (f) of tile t-1
         {
             uint32_t ph[32], pl[32];
             float2 l2 = make_float2(0.f, 0.f);
@@ -430,15 +429,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
                 }
             }
             l += l2.x + l2.y;
-            tmem_st32(tmem + lane_base + kColPh + half * 32, ph);
-            tmem_st32(tmem + lane_base + kColPl + half * 32, pl);
+            tmem_st32(tmem + lane_base + col_p + half * 32, ph);
+            tmem_st32(tmem + lane_base + col_p + 64 + half * 32, pl);
         }
-        // (f) V(t) has landed; O += P_hi V(t) + P_lo V(t) on the tensor cores
-        asm volatile("cp.async.wait_group 2;" ::: "memory");
+        // (f) P(t-1) V(t-1) done (issued a whole tile ago): its V buffer takes V(t+1); V(t) has landed;
+        // O += P_hi(t) V(t) + P_lo(t) V(t) on the tensor cores
+        if (t > 0) mma_wait_parity(&bar_o, (unsigned)(t - 1) & 1u, p.err);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");   // V(t); K(t+2) may fly
+        load_tile(sV(x ^ 1), vb, t + 1);
         publish_to_tensor_core();
         if (tid == 0) {
-            mma_pv(tmem + kColO, tmem + kColPh, smem_addr(sV(x)), t > 0);
-            mma_pv(tmem + kColO, tmem + kColPl, smem_addr(sV(x)), true);
+            mma_pv(tmem + kColO, tmem + col_p, smem_addr(sV(x)), t > 0);
+            mma_pv(tmem + kColO, tmem + col_p + 64, smem_addr(sV(x)), true);
             mma_commit(&bar_o);
         }
     }
