@@ -463,6 +463,30 @@ def test_dense_prefix_on_tensor_cores_matches_oracle(fx, fork):
     pu.assert_out_close(out, ref, vmax)
 
 
+@pytest.mark.parametrize("G,Mq,Br,P", [(4, 3, 11, 128), (1, 8, 17, 129), (2, 7, 10, 256), (8, 2, 9, 383)])
+def test_dense_prefix_tile_edges_on_tensor_cores(fx, G, Mq, Br, P):
+    """Tensor-core prefix route at tile edges: one full key tile (128), one key past it (129), two full
+    tiles (256), a ragged third (383); 132 to 144 query rows (a second, nearly empty row tile) with
+    group sizes 1 to 8 and 2 to 8 draft positions."""
+    Hkv = 2
+    lens = [(3 * b) % 11 for b in range(Br)]
+    off = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    S = max(1, int(off[-1]))
+    seed = 300 + P
+    pk, pv = rnd((Hkv, P, D), seed, 1), rnd((Hkv, P, D), seed, 2)
+    sk, sv = rnd((Hkv, S, D), seed, 3), rnd((Hkv, S, D), seed, 4)
+    dk, dv = rnd((Br, Mq, Hkv, D), seed, 5), rnd((Br, Mq, Hkv, D), seed, 6)
+    q = rnd((Br, Hkv * G, Mq, D), seed, 7)
+    assert Br * G * Mq >= 128
+    ref = oracle.shared_prefix(pk, pv, sk, sv, off, dk, dv, q, None)
+    out = fx.fx_shared_prefix_decode(dev(pk), dev(pv), dev(sk), dev(sv), dev(off), dev(dk), dev(dv), dev(q),
+                                     max_suffix=16)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    vmax = max(float(t.float().abs().max()) for t in (pv, sv, dv))
+    pu.assert_out_close(out, ref, vmax)
+
+
 def test_sparse_long_dense_tail_uses_global_merge(fx):
     """More than 16 x 4096 keys in one row: the splits are merged through the workspace (not inside a
     thread-block cluster)."""
