@@ -219,6 +219,8 @@ class OcrDecodeRun:
                                       vnew.reshape(w.steps, -1)], dim=1).cpu().pin_memory()
             del knew, vnew
             self.O_host = torch.empty(self.O.shape, dtype=torch.float32).pin_memory()
+            self.KVnew = torch.empty(2 * self.nkv, dtype=torch.bfloat16, device=device)
+            self.app_pos = (self.lens - 1).contiguous()   # the new token's row of every sequence per step
         self.rt = _cudart()
         self.graphs, self.graphs_e2e, self.graphs_sparse, self.sparse_bytes = {}, {}, {}, {}
         self.launches_per_step = 0
@@ -229,14 +231,16 @@ class OcrDecodeRun:
     # the dominant kernel on its own); `nbytes_out` collects the algorithmic bytes of each sparse launch.
     # Every call is a programmatic dependent launch; a call whose lengths / indices / K-V rows were
     # written two or more launches earlier also prefetches them before the previous kernel ends.
-    def step(self, t: int, only_sparse: bool = False, nbytes_out=None):
+    def step(self, t: int, only_sparse: bool = False, nbytes_out=None, after_writer: bool = False):
+        """after_writer: the kernel just before the step wrote rows that its first call reads (the
+        end-to-end step's append), so that call does not read its inputs early."""
         fx, w = self.fx, self.w
         pdl = fx.FX_LAUNCH_PDL if self.pdl else 0
         ready = fx.FX_LAUNCH_INPUTS_READY if self.pdl else 0
         p = t % 2
         ln = self.lens[t]
         launches = 0
-        after_topk = False
+        after_topk = after_writer
         for l in range(w.n_layers):
             if l in w.focal_layers:
                 if only_sparse:
@@ -271,22 +275,16 @@ class OcrDecodeRun:
             self.launches_estimate = launches
 
     def e2e_inputs(self, t: int):
-        """Copy step t's inputs from pinned host memory into device memory: the queries of all layers in
-        one copy, and the new K and V rows in one strided 2-D copy each (28*8*8 rows of 256 bytes; the
-        device pitch is one (layer, b, h) cache)."""
+        """Copy step t's inputs from pinned host memory into device memory -- the queries of all layers,
+        and the new K and V rows of all layers (one contiguous copy each) -- and append the new rows to
+        the caches (fx_kv_append: row len-1 of every (layer, b, h) cache)."""
         w = self.w
         nq, nkv = self.nq, self.nkv
         self.Q[t].copy_(self.In_host[t, :nq].view(self.Q[t].shape), non_blocking=True)
-        pos = w.n_vis + w.n_text + t
-        rows = w.n_layers * w.B * w.Hkv
-        for dst, off in ((self.K, nq), (self.V, nq + nkv)):
-            err = self.rt.cudaMemcpy2DAsync(ctypes.c_void_p(dst.data_ptr() + pos * D * 2),
-                                            ctypes.c_size_t(w.tcap * D * 2),
-                                            ctypes.c_void_p(self.In_host[t].data_ptr() + off * 2),
-                                            ctypes.c_size_t(D * 2), ctypes.c_size_t(D * 2), ctypes.c_size_t(rows),
-                                            ctypes.c_int(1), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-            if err != 0:
-                raise RuntimeError(f"cudaMemcpy2DAsync failed ({err})")
+        self.KVnew.copy_(self.In_host[t, nq:], non_blocking=True)
+        shape = (w.n_layers, w.B, w.Hkv, D)
+        self.fx.fx_kv_append(self.K, self.V, self.KVnew[:nkv].view(shape), self.KVnew[nkv:].view(shape),
+                             self.app_pos[t])
 
     def count_kernel_nodes(self, t: int):
         """Kernel launches of one step, counted as the kernel nodes of a captured graph of it (None when
@@ -335,7 +333,7 @@ class OcrDecodeRun:
                 g2 = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g2, stream=s):
                     self.e2e_inputs(t)
-                    self.step(t)
+                    self.step(t, after_writer=True)
                     self.O_host.copy_(self.O, non_blocking=True)
                 self.graphs_e2e[t] = g2
 

@@ -231,6 +231,25 @@ FX_API fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, 
                         int64_t idx_stride_layer, int k, int tail_lo, const fx_kv_out_desc* dst,
                         int64_t dst_stride_layer, int n_layers, unsigned flags, void* stream);
 
+/*
+ * Decode-step append: the new token's key and value rows of every layer join that layer's cache.
+ * [FastKV] 3.2 decodes over the compacted cache and [FastOCR] decodes over the visual + text cache;
+ * in both, every decoding step adds one row per (layer, sequence, KV head).
+ *
+ * For every layer l < n_layers, b < cache->B and h < cache->Hkv:
+ *   K_l[b, h, pos[b], :] = k_new[l, b, h, :]   and   V_l[b, h, pos[b], :] = v_new[l, b, h, :]
+ * as bit-exact copies, where layer l of the cache starts at element offset l*stride_layer from
+ * cache->k / cache->v.
+ *   k_new, v_new  bf16 [n_layers, B, Hkv, 128], contiguous (device).
+ *   pos           int32 [B] (device): the row each sequence writes, normally its current length.  A
+ *                 position outside [0, cache->Tcap) sets FX_DEVERR_LEN and that sequence's rows are
+ *                 not written.
+ * cache->len is neither read nor written (lengths stay the caller's).  No workspace.
+ */
+FX_API fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer, int n_layers,
+                              const fx_bf16* k_new, const fx_bf16* v_new, const int32_t* pos, unsigned flags,
+                              void* stream);
+
 /* ------------------------------------------------------------------------------------------- */
 /* fx_kv_retain_per_layer -- FastKV decoupled KV retention with its own selection at every layer.
  * [FastKV] 2.A (saliency: attention of a window of recent queries to all context tokens) and 2.B

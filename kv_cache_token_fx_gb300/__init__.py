@@ -20,8 +20,8 @@ from . import build as _build
 __all__ = [
     "FxError", "load_library", "library_path", "Workspace", "fx_focal_attn_scores", "fx_topk_select",
     "fx_focal_mass", "fx_choose_focal_layers",
-    "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode", "fx_device_errors",
-    "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
+    "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_append", "fx_kv_retain_per_layer", "fx_shared_prefix_decode",
+    "fx_device_errors", "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
     "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
     "FX_LAUNCH_PDL", "FX_LAUNCH_INPUTS_READY", "BranchPool",
 ]
@@ -100,6 +100,7 @@ def load_library():
                                              c_vp, c_vp, c_size, c_uint, c_vp]
         lib.fx_kv_compact.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_vp, c_i64, c_int, c_int,
                                       ctypes.POINTER(KVOutDesc), c_i64, c_int, c_uint, c_vp]
+        lib.fx_kv_append.argtypes = [ctypes.POINTER(KVOutDesc), c_i64, c_int, c_vp, c_vp, c_vp, c_uint, c_vp]
         lib.fx_retain_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_retain_workspace_bytes.restype = c_size
         lib.fx_kv_retain_per_layer.argtypes = [ctypes.POINTER(KVDesc), c_i64, c_int, c_vp, c_int, c_int, c_int,
@@ -121,7 +122,8 @@ def load_library():
                                                 c_vp, c_int, c_float, c_vp, c_vp, c_size, c_uint, c_vp]
         for name in ("fx_device_errors", "fx_workspace_init", "fx_focal_attn_scores", "fx_topk_select",
                      "fx_focal_mass", "fx_choose_focal_layers",
-                     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_retain_per_layer", "fx_shared_prefix_decode"):
+                     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_append", "fx_kv_retain_per_layer",
+                     "fx_shared_prefix_decode"):
             getattr(lib, name).restype = c_int
         _lib = lib
         return lib
@@ -347,6 +349,29 @@ def fx_kv_compact(k, v, length, idx, tail_lo: int, dst_k, dst_v, dst_len, *, str
     _check(lib.fx_kv_compact(ctypes.byref(src), s_layer, _ptr(idx) if kk else None, i_layer, kk, int(tail_lo),
                              ctypes.byref(dst_out), d_layer, n_layers, int(flags), _stream(stream)))
     return dst_k, dst_v, dst_len
+
+
+def fx_kv_append(k, v, k_new, v_new, pos, *, stream=None, flags: int = 0):
+    """Write one new key/value row per (layer, sequence, KV head) into the caches: row pos[b] of
+    k, v ([B, Hkv, T, 128], or [L, B, Hkv, T, 128] for L layers) takes k_new, v_new ([B, Hkv, 128] or
+    [L, B, Hkv, 128], contiguous).  pos: int32 [B] on the device."""
+    lib = load_library()
+    if k.dim() == 5:
+        n_layers, s_layer = k.shape[0], k.stride(0)
+        if v.stride(0) != s_layer:
+            raise FxError(FX_ERR_INVALID_ARG, "k/v layer strides must match")
+        cache = _kv_desc(k[0], v[0], pos)
+    else:
+        n_layers, s_layer = 1, 0
+        cache = _kv_desc(k, v, pos)
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        _need_cuda(t, name, torch.bfloat16)
+        if not t.is_contiguous() or t.numel() != n_layers * cache.B * cache.Hkv * cache.d:
+            raise FxError(FX_ERR_INVALID_ARG, f"{name} must be a contiguous [L, B, Hkv, 128] tensor")
+    out = KVOutDesc(*[getattr(cache, f) for f, _ in KVDesc._fields_])
+    _check(lib.fx_kv_append(ctypes.byref(out), s_layer, n_layers, _ptr(k_new), _ptr(v_new), _ptr(pos), int(flags),
+                            _stream(stream)))
+    return k, v
 
 
 def fx_kv_retain_per_layer(k, v, length, q, keep_k: int, cand_hi: int, tail_lo: int, dst_k, dst_v, dst_len, *,

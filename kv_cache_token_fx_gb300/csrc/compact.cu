@@ -83,7 +83,40 @@ __global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams
     }
 }
 
+// Decode-step append: one warp per (layer, b, h) row pair; lanes 0..15 copy the 16-byte chunks of the
+// new K row, lanes 16..31 those of the V row, into row pos[b] of that layer's cache.
+__global__ void __launch_bounds__(kCpThreads) append_kernel(const AppendParams p)
+{
+    griddep_wait();   // the new rows may come from the kernel just before
+    griddep_launch();
+    const int64_t w = (int64_t)blockIdx.x * (kCpThreads / 32) + (threadIdx.x >> 5);
+    const int64_t rows = (int64_t)p.n_layers * p.B * p.Hkv;
+    if (w >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const int h = (int)(w % p.Hkv);
+    const int64_t lb = w / p.Hkv;
+    const int b = (int)(lb % p.B);
+    const int l = (int)(lb / p.B);
+    const int t = p.pos[b];
+    if (t < 0 || t >= p.Tcap) {
+        if (lane == 0 && h == 0 && l == 0) atomicOr(p.err, FX_DEVERR_LEN);
+        return;
+    }
+    const int c = lane & 15;
+    const uint16_t* src = (lane < 16 ? p.k_new : p.v_new) + (w << 7) + 8 * c;
+    uint16_t* dst = (lane < 16 ? p.k : p.v) + l * p.layer + b * p.sb + h * p.sh + (int64_t)t * p.st + 8 * c;
+    *reinterpret_cast<uint4*>(dst) = ld_nc16(src);
+}
+
 }  // namespace
+
+cudaError_t launch_append(const AppendParams& p, bool pdl, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)p.n_layers * p.B * p.Hkv;
+    const int per_cta = kCpThreads / 32;
+    dim3 grid((unsigned)((rows + per_cta - 1) / per_cta));
+    return launch_kernel(append_kernel, grid, dim3(kCpThreads), 0, s, pdl, 0u, p);
+}
 
 cudaError_t launch_compact(const CompactParams& p, bool pdl, cudaStream_t s)
 {

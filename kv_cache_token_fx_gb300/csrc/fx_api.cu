@@ -506,6 +506,45 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
     return FX_OK;
 }
 
+fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer, int n_layers, const fx_bf16* k_new,
+                       const fx_bf16* v_new, const int32_t* pos, unsigned flags, void* stream)
+{
+    fx_status st;
+    if (!cache) return fail(FX_ERR_INVALID_ARG, "cache is NULL");
+    if (!pos) return fail(FX_ERR_INVALID_ARG, "pos is NULL");
+    fx_kv_desc view = {cache->k, cache->v, pos, cache->stride_b, cache->stride_h, cache->stride_t,
+                       cache->B, cache->Hkv, cache->Tcap, cache->d};
+    if ((st = check_kv(&view, "cache")) != FX_OK) return st;
+    if ((st = check_flags(flags)) != FX_OK) return st;
+    if (n_layers < 1) return fail(FX_ERR_INVALID_ARG, "n_layers must be >= 1");
+    if (!k_new || !v_new) return fail(FX_ERR_INVALID_ARG, "k_new and v_new are required");
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+        return fail(FX_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (!row_stride_ok(stride_layer)) return fail(FX_ERR_INVALID_ARG, "stride_layer must be a non-negative multiple of 8 elements");
+    if ((int64_t)n_layers * cache->B * cache->Hkv > (int64_t)65535 * 8 * 65535)
+        return fail(FX_ERR_UNSUPPORTED, "too many rows");
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
+    AppendParams p;
+    p.k = cache->k;
+    p.v = cache->v;
+    p.sb = cache->stride_b;
+    p.sh = cache->stride_h;
+    p.st = cache->stride_t;
+    p.layer = stride_layer;
+    p.B = cache->B;
+    p.Hkv = cache->Hkv;
+    p.Tcap = cache->Tcap;
+    p.n_layers = n_layers;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.pos = pos;
+    p.err = ds->err;
+    cudaError_t e = launch_append(p, (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return FX_OK;
+}
+
 // ---------------------------------------------------------------------------------------------
 size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi)
 {

@@ -160,6 +160,17 @@ struct CompactParams {
     unsigned* err;
 };
 
+struct AppendParams {
+    uint16_t* k;
+    uint16_t* v;
+    int64_t sb, sh, st, layer;
+    int B, Hkv, Tcap, n_layers;
+    const uint16_t* k_new;   // [n_layers, B, Hkv, 128]
+    const uint16_t* v_new;
+    const int32_t* pos;      // [B]
+    unsigned* err;
+};
+
 // Sets the calling thread's error message (read back by fx_last_error) and returns `st`.
 fx_status set_error(fx_status st, const char* msg);
 
@@ -171,6 +182,7 @@ cudaError_t launch_prefix_tc(const PrefixTcParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_mass(const float* scores, int rows, int n, float inv_r, int accumulate, float* mass,
                               bool pdl, cudaStream_t s);
 cudaError_t launch_compact(const CompactParams& p, bool pdl, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, bool pdl, cudaStream_t s);
 
 // Launch `kern` with optional programmatic stream serialization and a (1, cluster_y, 1) cluster.
 template <typename... KArgs, typename... Args>

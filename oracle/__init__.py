@@ -217,6 +217,21 @@ def kv_compact(k, v, length, idx, tail_lo: int, cap: int, *, lib=None):
     return dk, dv, dl
 
 
+def kv_append(k, v, k_new, v_new, pos):
+    """Decode-step append (FastKV 3.2, decoding over the compacted cache; FastOCR, decoding): every
+    (layer, sequence, KV head) cache gains the new token's row at position pos[b].  k, v [..., B, Hkv,
+    T, d]; k_new, v_new [..., B, Hkv, d]; a position outside [0, T) writes nothing.  Returns new CPU
+    tensors (the inputs are not modified)."""
+    k2, v2 = k.clone().cpu(), v.clone().cpu()
+    kn, vn = k_new.cpu(), v_new.cpu()
+    T = k2.shape[-2]
+    for b, t in enumerate(pos.tolist()):
+        if 0 <= t < T:
+            k2[..., b, :, t, :] = kn[..., b, :, :]
+            v2[..., b, :, t, :] = vn[..., b, :, :]
+    return k2, v2
+
+
 def shared_prefix(pk, pv, sk, sv, off, dk, dv, q, prefix_idx=None, *, pre_len=None, suf_len=None, scale=None,
                   lib=None):
     """Shared-prefix draft verification.

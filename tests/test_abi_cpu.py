@@ -70,6 +70,16 @@ def test_host_argument_checks_without_gpu(lib):
     assert retain(3, 596, 597) == 1 and b"keep_k" in lib.fx_last_error()
     assert retain(3, 596, 37) == 3    # no workspace
     assert lib.fx_retain_workspace_bytes(2, 2, 4, 4, 600, 596) > 2 * 2 * 596 * 4
+    # decode-step append: argument checks before any device work
+    lib.fx_kv_append.restype = ctypes.c_int
+    append = lambda n_layers, knew, pos, flags=0: lib.fx_kv_append(
+        ctypes.byref(dst), ctypes.c_int64(2 * 2 * 64 * 128), n_layers, knew, ctypes.c_void_p(2048), pos,
+        ctypes.c_uint(flags), None)
+    assert append(0, ctypes.c_void_p(256), ctypes.c_void_p(256)) == 1 and b"n_layers" in lib.fx_last_error()
+    assert append(2, ctypes.c_void_p(256), None) == 1 and b"pos" in lib.fx_last_error()
+    assert append(2, None, ctypes.c_void_p(256)) == 1 and b"k_new" in lib.fx_last_error()
+    assert append(2, ctypes.c_void_p(264), ctypes.c_void_p(256)) == 1 and b"aligned" in lib.fx_last_error()
+    assert append(2, ctypes.c_void_p(256), ctypes.c_void_p(256), 0x40) == 1
     # the focal-layer choice is host code: it runs here, and agrees with the oracle's rule
     import oracle
     lib.fx_choose_focal_layers.restype = ctypes.c_int

@@ -365,6 +365,46 @@ def test_focal_layer_profiling_matches_oracle(fx):
     assert fx.fx_choose_focal_layers(ratio, C) == oracle.choose_focal_layers(ref_ratio, C) == [1, 3]
 
 
+def test_kv_append_matches_oracle(fx):
+    """Decode-step append into the caches of 3 layers (strided layer views of one buffer), rows at the
+    first and last capacity positions and in between; then a dense decode over the grown cache equals
+    the oracle's decode over the oracle's appended cache."""
+    L, B, Hkv, T, G = 3, 3, 2, 40, 2
+    full_k, full_v = rnd((L, B, Hkv, T + 8, D), 400, 1), rnd((L, B, Hkv, T + 8, D), 400, 2)
+    buf_k, buf_v = full_k[:, :, :, :T], full_v[:, :, :, :T]   # caches of capacity T in padded rows
+    k_new, v_new = rnd((L, B, Hkv, D), 400, 3), rnd((L, B, Hkv, D), 400, 4)
+    pos = torch.tensor([0, T - 1, 17], dtype=torch.int32)
+    ref_k, ref_v = oracle.kv_append(buf_k, buf_v, k_new, v_new, pos)
+    gk_full, gv_full = dev(full_k), dev(full_v)
+    gk, gv = gk_full[:, :, :, :T], gv_full[:, :, :, :T]
+    fx.fx_kv_append(gk, gv, dev(k_new), dev(v_new), dev(pos))
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert torch.equal(gk.cpu().view(torch.int16), ref_k.view(torch.int16))
+    assert torch.equal(gv.cpu().view(torch.int16), ref_v.view(torch.int16))
+    assert torch.equal(gk_full[:, :, :, T:].cpu().view(torch.int16), full_k[:, :, :, T:].view(torch.int16))
+    # decode over len = pos + 1 on layer 1 of both caches
+    length = pos + 1
+    q = rnd((B, Hkv * G, 1, D), 400, 5)
+    ref = oracle.sparse_decode(ref_k[1], ref_v[1], length, q, None, 0)
+    out = fx.fx_sparse_gqa_decode(gk[1], gv[1], dev(length), dev(q), None, 0)
+    pu.assert_out_close(out, ref, float(ref_v[1].float().abs().max()))
+
+
+def test_kv_append_rejects_positions_past_capacity(fx):
+    B, Hkv, T = 2, 2, 16
+    k, v = kv_case(B, Hkv, T, 401)
+    k_new, v_new = rnd((B, Hkv, D), 401, 3), rnd((B, Hkv, D), 401, 4)
+    gk, gv = dev(k), dev(v)
+    fx.fx_device_errors()
+    fx.fx_kv_append(gk, gv, dev(k_new), dev(v_new), dev(torch.tensor([T, 5], dtype=torch.int32)))
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() & fx.FX_DEVERR_LEN
+    ref_k, ref_v = oracle.kv_append(k, v, k_new, v_new, torch.tensor([-1, 5], dtype=torch.int32))
+    assert torch.equal(gk.cpu().view(torch.int16), ref_k.view(torch.int16))
+    assert torch.equal(gv.cpu().view(torch.int16), ref_v.view(torch.int16))
+
+
 def test_compaction_capacity_is_flagged(fx):
     B, Hkv, T = 1, 1, 50
     k, v = kv_case(B, Hkv, T, 60)
