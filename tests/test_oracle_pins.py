@@ -321,6 +321,69 @@ def test_profile_pins_catch_planted_mistakes(oracle_mod):
             pin_choose_focal_layers_brute_force(choose_fn=fn)
 
 
+# Decode-step append (FastKV 3.2 and FastOCR decoding: the step's new K/V row joins the cache), pinned
+# by rebuilding the expected cache with explicit concatenation and by the attention it feeds.
+
+def pin_append_equals_concatenation(lib=None, append_fn=None):
+    """Row pos[b] of every (layer, b, h) becomes the new row: the result equals the cache cut at pos,
+    the new row, and the rest, concatenated; a position outside [0, T) leaves that sequence as it was."""
+    append_fn = append_fn or oracle.kv_append
+    L, B, Hkv, T = 2, 3, 2, 9
+    k, v = _rand_bf16((L, B, Hkv, T, 128), 41, 1), _rand_bf16((L, B, Hkv, T, 128), 41, 2)
+    kn, vn = _rand_bf16((L, B, Hkv, 128), 41, 3), _rand_bf16((L, B, Hkv, 128), 41, 4)
+    pos = torch.tensor([0, 8, -1], dtype=torch.int32)
+    gk, gv = append_fn(k, v, kn, vn, pos)
+    for src, new, got in ((k, kn, gk), (v, vn, gv)):
+        for b, t in enumerate(pos.tolist()):
+            if 0 <= t < T:
+                want = torch.cat([src[:, b, :, :t], new[:, b, :, None], src[:, b, :, t + 1:]], dim=2)
+            else:
+                want = src[:, b]
+            assert torch.equal(got[:, b].view(torch.int16), want.view(torch.int16)), (b, t)
+
+
+def pin_decode_after_append_sees_the_new_row(lib=None, append_fn=None):
+    """A new key far along the query direction takes almost all of the attention once appended at
+    row len-1 (and the cache's length then covers it): the output is that row's value."""
+    append_fn = append_fn or oracle.kv_append
+    B, Hkv, G, T = 1, 1, 2, 12
+    k, v = _rand_bf16((B, Hkv, T, 128), 42, 1), _rand_bf16((B, Hkv, T, 128), 42, 2)
+    q = _rand_bf16((B, Hkv * G, 1, 128), 42, 3)
+    u = q[0, :, 0].float().sum(dim=0)
+    kn = (u / u.norm() * 60.0).to(torch.bfloat16).view(B, Hkv, 128)
+    vn = _rand_bf16((B, Hkv, 128), 42, 4)
+    pos = torch.tensor([7], dtype=torch.int32)
+    k2, v2 = append_fn(k, v, kn, vn, pos)
+    out = oracle.sparse_decode(k2, v2, pos + 1, q, None, 0, lib=lib)
+    assert np.max(np.abs(np.asarray(out)[0, :, 0] - vn[0, 0].double().numpy())) < 1e-6
+
+
+APPEND_PINS = [pin_append_equals_concatenation, pin_decode_after_append_sees_the_new_row]
+
+
+@pytest.mark.parametrize("pin", APPEND_PINS, ids=[p.__name__ for p in APPEND_PINS])
+def test_append_pin(pin, oracle_mod):
+    pin()
+
+
+def test_append_pins_catch_planted_mistakes(oracle_mod):
+    """Plausible mistakes in the append each fail a pin (planted here, on the CPU)."""
+    def shifted(k, v, kn, vn, pos):            # writes one row later
+        return oracle.kv_append(k, v, kn, vn, pos + 1)
+
+    def k_only(k, v, kn, vn, pos):             # forgets the V row
+        k2, _ = oracle.kv_append(k, v, kn, vn, pos)
+        return k2, v.clone()
+
+    def swapped(k, v, kn, vn, pos):            # K and V rows exchanged
+        return oracle.kv_append(k, v, vn, kn, pos)
+
+    for fn in (shifted, k_only, swapped):
+        with pytest.raises(AssertionError):
+            pin_append_equals_concatenation(append_fn=fn)
+            pin_decode_after_append_sees_the_new_row(append_fn=fn)
+
+
 PINS = [pin_golden_focal, pin_golden_topk, pin_golden_sparse, pin_golden_shared_prefix,
         pin_uniform_keys_give_mean, pin_importance_sums_to_rows, pin_single_key_and_dominant_key,
         pin_topk_brute_force, pin_sparse_full_set_equals_dense, pin_compaction_equals_sparse,
