@@ -8,13 +8,15 @@
 //   O += P V        (M = 128 query rows, N = 128 dims, K = 128 prefix keys)   tensor memory x smem -> tensor memory
 // in one pass with an online softmax (P = exp2(S - m) against a running maximum m that moves only by
 // more than a fixed slack, so O is rescaled rarely), P split into bf16 hi + lo parts (two products) so
-// the probabilities keep about 16 bits.  Two threads own one query row, each for half of the keys of a
-// tile and half of O: they read their S columns from tensor memory, trade the row maximum, and write
-// P back into tensor memory (two buffers), where the P V product takes it as its A operand.  Q and K tiles are
-// K-major operands with the 128-byte swizzle; V tiles are copied as they are stored (keys x dims) into
-// the same swizzled layout and used as an MN-major operand, so nothing is transposed.  P is double
-// buffered in tensor memory and K, V in shared memory: the next tile's Q K^T and the previous tile's
-// P V run on the tensor cores while this tile's softmax runs on the threads.
+// the probabilities keep about 16 bits.  Eight softmax warps own the 128 query rows, two threads per
+// row, each for half of the keys of a tile and half of O: they read their S columns from tensor
+// memory, trade the row maximum with the partner warp, and write P back into tensor memory (two
+// buffers), where the P V product takes it as its A operand.  A ninth warp issues the products when
+// mbarriers say the softmax warps have published their operands.  Q and K tiles are K-major operands
+// with the 128-byte swizzle; V tiles are copied as they are stored (keys x dims) into the same
+// swizzled layout and used as an MN-major operand, so nothing is transposed.  K and V are double
+// buffered in shared memory: the next tile's Q K^T and the previous tile's P V run on the tensor cores
+// while this tile's softmax runs on the softmax warps.
 // The result per row is a partial (m, l, O) over the prefix, which the verify kernel folds into its
 // merge of the suffix and draft keys.
 #include <cuda_bf16.h>
