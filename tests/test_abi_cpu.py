@@ -91,6 +91,14 @@ def test_host_argument_checks_without_gpu(lib):
             assert lib.fx_choose_focal_layers((ctypes.c_float * n)(*ratio), n, C, out) == 0
             assert list(out) == oracle.choose_focal_layers(ratio.tolist(), C)
     assert lib.fx_choose_focal_layers((ctypes.c_float * 2)(0.1, 0.2), 2, 3, (ctypes.c_int32 * 3)()) == 1
+    # shared-prefix workspace: a dense prefix of a full 128 x 128 tile or more (and at least 128 query
+    # rows per KV head) also needs room for the tensor-core prefix partials (O, m, l per row)
+    lib.fx_shared_prefix_workspace_bytes.restype = ctypes.c_size_t
+    sp = lambda Br, Hkv, Hq, Mq, np_, ms: lib.fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np_, ms)
+    assert sp(512, 8, 16, 7, 2304, 1024) >= 8 * 512 * 14 * 130 * 4          # tensor-core route
+    assert sp(512, 8, 16, 7, 2304, 1024) >= sp(512, 8, 16, 7, 0, 1024)
+    assert sp(4, 8, 16, 7, 2304, 1024) > 0                                     # 56 rows: no tensor cores
+    assert sp(0, 8, 16, 7, 2304, 1024) == 0 and sp(4, 8, 4, 7, 2304, 1024) == 0   # Br < 1, Hq < Hkv
     lib.fx_sparse_workspace_bytes.restype = ctypes.c_size_t
     assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) > 0
     assert lib.fx_sparse_workspace_bytes(0, 8, 16, 205, 4096, 4864) == 0
