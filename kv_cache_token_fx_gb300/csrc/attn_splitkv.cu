@@ -1,8 +1,9 @@
 // Split-KV decode / verify attention for sm_103a.
 //
-// One CTA (4 warps) = (group of NR = 8 or 16 query rows of one KV head, one split of that head's key
-// sequence, one (b, KV head)).  Each warp owns a fixed, contiguous range of whole 16-key sub-tiles of
-// the split and walks it on its own:
+// One CTA (4 warps) = (group of NR = 8, 16 or 32 query rows of one KV head, one split of that head's
+// key sequence, one (b, KV head)).  Each warp owns a contiguous range of whole 16-key sub-tiles of the
+// split (a fixed quarter of it; in the prefix mode a quarter of the keys the row actually has) and
+// walks it on its own:
 //   * Data movement: the warp stages its sub-tiles (16 K rows + 16 V rows of 256 bytes; contiguous
 //     rows for the focal mode, gathered rows for the sparse/prefix modes) into a private ring of
 //     2 or 3 buffers (attn_stages) with 16-byte cp.async, each warp instruction moving two whole
@@ -10,20 +11,21 @@
 //     resolves the token of row l & 15 (one index load per lane); the copies take the row addresses
 //     by warp shuffle and a ballot records which rows are valid.  Within a row the 16-byte chunk index
 //     is XORed with (row % 8), so the 8-row ldmatrix reads hit 8 different bank groups without
-//     padding; invalid rows are zero-filled.  (Per-row
-//     cp.async.bulk TMA copies were measured slower here: 256-byte requests keep the TMA engine, not
-//     HBM, busy.)
+//     padding; invalid rows are zero-filled.  (Per-row cp.async.bulk TMA copies were measured slower
+//     here: 256-byte requests keep the TMA engine, not HBM, busy.)
 //   * Math: mma.sync m16n8k16 (bf16 in, fp32 accumulate), online softmax on the accumulator
 //     fragments in base-2 units, P split into bf16 hi + lo parts (two MMAs) so that the
 //     probabilities keep ~16 bits.  With NR = 8 the keys are the M side (S^T = K Q^T, O^T = V^T P^T,
 //     P^T moved into the B operand with movmatrix.trans): half the MMAs of the NR = 16 layout, where
-//     the query rows are the M side (S = Q K^T, O = P V).
-// Partial (max, sum, unnormalised output) triples per split are merged inside a thread-block cluster
-// -- all splits of one (b, h, row group) form one cluster; either the others push their partials
-// into CTA 0 with st.async (completing on CTA 0's mbarrier) and exit, or every CTA reads all
-// partials from distributed shared memory -- or, for the focal call and for very long rows, through
-// the workspace (the focal call's combine kernel also forms the per-token importance from the logits
-// this kernel stores).
+//     the query rows are the M side (S = Q K^T, O = P V).  NR = 32 (scoring-only focal calls) keeps
+//     the keys on M with four query n-tiles sharing each K fragment, and has no P V.
+// The warps' partials are combined with per-row weights computed once.  Partial (max, sum,
+// unnormalised output) triples per split are merged inside a thread-block cluster -- all splits of
+// one (b, h, row group) form one cluster; either the others push their partials into CTA 0 with
+// st.async (completing on CTA 0's mbarrier) and exit, or every CTA reads all partials from
+// distributed shared memory -- or, for the focal call and for very long rows, through the workspace
+// (the focal call's combine kernel also forms the per-token importance from the logits this kernel
+// stores).  A verify call whose dense prefix ran on the tensor cores folds that partial in here.
 //
 // Attention and importance follow FastOCR (Methodology: Focal-Guided Pruning): focal layers attend
 // over the full cache, the rest over the selected set; FastKV (2.A) for the causal query window;
