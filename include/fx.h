@@ -300,6 +300,11 @@ FX_API fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride
  *               FX_DEVERR_INDEX and are skipped)
  * Workspace: fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, np, max_suffix) bytes, where np is
  * P (dense) or kp (sparse).
+ * A dense prefix of at least 128 rows with Br*G*Mq >= 128 query rows per KV head runs on the tensor
+ * cores (128-row x 128-key tiles, bf16 products with fp32 accumulation, the probabilities as bf16
+ * hi + lo parts): two launches, the prefix partials held in the workspace (included in the size
+ * above) and folded into the verify kernel's merge.  The result agrees with the single-kernel route
+ * within the same output tolerance.
  */
 typedef struct {
     const fx_bf16* k;
