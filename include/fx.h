@@ -370,6 +370,19 @@ FX_API int fx_branch_pool_batch(fx_branch_pool* pool, int32_t* ids, int32_t* suf
                          int32_t* prefix_len);
 
 /* ------------------------------------------------------------------------------------------- */
+/* fx_test_stall_wait -- testing hook for the device-side failure path; the pages have no counterpart.
+ *
+ * Every wait of a kernel on an mbarrier (copies landing, pushed partials arriving) gives up after a
+ * fixed number of polls, sets FX_DEVERR_TIMEOUT and lets the kernel finish, so a wait that can never
+ * complete leaves the context usable instead of hanging the GPU.  With polls > 0, every later
+ * decode-shaped fx_sparse_gqa_decode call (G <= 8 query heads per KV head) adds one such wait, of
+ * `polls` polls, on a barrier that nothing arrives on, after its results are complete: the call
+ * returns, its output is still correct, and fx_device_errors() then reports FX_DEVERR_TIMEOUT.
+ * polls = 0 (the default) turns the extra wait off.  Process-wide; not for production use.
+ */
+FX_API void fx_test_stall_wait(unsigned polls);
+
+/* ------------------------------------------------------------------------------------------- */
 /* fx_focal_attn_scores_noalloc -- fx_focal_attn_scores for callers that cannot allocate device
  * memory.  The pages have no counterpart for this call; it is a convenience of this library.
  *

@@ -84,6 +84,8 @@ def load_library():
         lib.fx_last_error.restype = ctypes.c_char_p
         lib.fx_abi_version.restype = c_int
         lib.fx_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint), c_vp]
+        lib.fx_test_stall_wait.argtypes = [ctypes.c_uint]
+        lib.fx_test_stall_wait.restype = None
         lib.fx_workspace_init.argtypes = [c_vp, c_size, c_vp]
         lib.fx_focal_workspace_bytes.argtypes = [c_int] * 5
         lib.fx_focal_workspace_bytes.restype = c_size

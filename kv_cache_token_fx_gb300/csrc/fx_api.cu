@@ -3,6 +3,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 #include <stdarg.h>
 #include <stdio.h>
@@ -19,6 +20,9 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kAlign = 256;
 
 thread_local char g_msg[512] = "";
+
+// Testing hook (fx_test_stall_wait): polls of one extra bounded wait that nothing completes.
+unsigned g_test_stall = 0;
 
 fx_status fail(fx_status st, const char* fmt, ...)
 {
@@ -119,6 +123,46 @@ Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_clust
     return pl;
 }
 
+// Streaming decode plan: about 1.5 CTAs per SM per call (the splits of each (b, h) merged in a
+// cluster) and as many ring slots as fit kStreamSmemMax, so that two CTAs share an SM and most of the
+// next call's CTAs are resident, filling their rings, while this call finishes.  Measured on the
+// FastOCR-shaped decode (64 (b, h) pairs, 718-973 keys): 3 splits beat 2 (fewer bytes in flight) and 4
+// (the next call's CTAs find no room) at the early steps; rings of 8 slots with 3 CTAs per SM were
+// slower than 12 slots with 2.
+struct StreamPlan {
+    int nsplit, slots;
+};
+
+StreamPlan make_stream_plan(int pairs, int R, int max_keys, int sm_count)
+{
+    int ns = pairs >= sm_count ? 1 : std::max(1, (3 * sm_count) / (2 * pairs));
+    ns = std::min(ns, kMaxClusterSplits);
+    ns = std::min(ns, std::max(1, cdiv(max_keys, kSub)));
+    while (ns > 1 && stream_decode_smem_bytes(2 * kStreamProducers, ns, R) > kStreamSmemMax) --ns;
+    int slots = (int)((kStreamSmemMax - stream_decode_smem_bytes(0, ns, R)) / kSubBytes);
+    slots = std::min(slots, kStreamMaxSlots) / kStreamProducers * kStreamProducers;   // whole slots per producer
+    return StreamPlan{ns, slots};
+}
+
+// cuTensorMapEncodeTiled, looked up once in the driver (the library does not link against it).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
 struct Layout {
     size_t part_m, part_l, part_o, logits, counters, total;
 };
@@ -195,6 +239,8 @@ extern "C" {
 const char* fx_last_error(void) { return g_msg; }
 
 int fx_abi_version(void) { return kAbiVersion; }
+
+void fx_test_stall_wait(unsigned polls) { g_test_stall = polls; }
 
 fx_status fx_device_errors(unsigned* bits, void* stream)
 {
@@ -380,6 +426,7 @@ size_t fx_sparse_workspace_bytes(int B, int Hkv, int Hq, int k, int tail_lo, int
 {
     if (B < 1 || Hkv < 1 || Hq < Hkv || k < 0 || tail_lo < 0 || Tcap < 0) return 0;
     const int R = Hq / Hkv;
+    if (R <= kStreamRows) return 0;   // the streaming kernel merges inside a cluster: no scratch
     const int max_keys = k + (Tcap > tail_lo ? Tcap - tail_lo : 0);
     const Plan pl = make_plan(B * Hkv, R, max_keys, sm_count_or_default(), true, k > 0);
     return make_layout(B * Hkv, R, pl, 0, true).total;
@@ -405,6 +452,45 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     const int G = Hq / kv->Hkv;
     const int R = G;
     const int max_keys = k + (kv->Tcap > tail_lo ? kv->Tcap - tail_lo : 0);
+    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+    if (R <= kStreamRows) {
+        // decode shapes: the streaming kernel (producer warp + CTA-wide ring, cluster merge)
+        if (pairs > 65535) return fail(FX_ERR_UNSUPPORTED, "grid too large");
+        const StreamPlan sp = make_stream_plan(pairs, R, max_keys, ds->sm_count);
+        AttnParams p;
+        memset(&p, 0, sizeof p);
+        p.k = kv->k;
+        p.v = kv->v;
+        p.len = kv->len;
+        p.sb = kv->stride_b;
+        p.sh = kv->stride_h;
+        p.st = kv->stride_t;
+        p.B = kv->B;
+        p.Hkv = kv->Hkv;
+        p.Tcap = kv->Tcap;
+        p.q = q;
+        p.Hq = Hq;
+        p.G = G;
+        p.Mq = 1;
+        p.R = R;
+        p.q_pos0 = -1;
+        p.qscale = log2e_scale(scale);
+        p.idx = k > 0 ? idx : nullptr;
+        p.kk = k;
+        p.tail_lo = tail_lo;
+        p.nsplit = sp.nsplit;
+        p.stages = sp.slots;
+        p.out = out;
+        p.err = ds->err;
+        p.spin_limit = kSpinLimit;
+        p.test_stall = g_test_stall;
+        p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
+        CUtensorMap tk, tv;
+        p.tail_tma = encode_kv_tensor_maps(kv, &tk, &tv) ? 1 : 0;
+        cudaError_t e = launch_stream_decode(p, &tk, &tv, pdl, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "sparse decode launch");
+        return FX_OK;
+    }
     const Plan pl = make_plan(pairs, R, max_keys, ds->sm_count, true, k > 0);
     const Layout L = make_layout(pairs, R, pl, 0, true);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
@@ -443,7 +529,7 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
     p.counters = reinterpret_cast<unsigned*>(w + L.counters);
     p.out = out;
     p.err = ds->err;
-    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+    p.spin_limit = kSpinLimit;
     p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
     cudaError_t e = launch_attn_partial(p, kModeSparse, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "sparse decode launch");
@@ -748,3 +834,26 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
 }
 
 }  // extern "C"
+
+// Tensor maps of one layer's K and V for the streaming decode kernel: [B][Hkv][Tcap][128] bf16 with the
+// view's strides, boxes of 16 rows x 64 columns, 128-byte swizzle, rows past Tcap read as zero.
+bool fx::encode_kv_tensor_maps(const fx_kv_desc* kv, CUtensorMap* tk, CUtensorMap* tv)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr || kv->Tcap < 1) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kv->Tcap, (cuuint64_t)kv->Hkv, (cuuint64_t)kv->B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kv->stride_t * 2, (cuuint64_t)kv->stride_h * 2, (cuuint64_t)kv->stride_b * 2};
+    for (int i = 0; i < 3; ++i)
+        if (strides[i] == 0 || (strides[i] & 15u) != 0 || strides[i] >= (1ull << 40)) return false;
+    const cuuint32_t box[4] = {64, (cuuint32_t)kSub, 1, 1};
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    const void* bases[2] = {kv->k, kv->v};
+    CUtensorMap* maps[2] = {tk, tv};
+    for (int i = 0; i < 2; ++i) {
+        if (fn(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(bases[i]), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libfx translation units (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (the driver's encode function is resolved at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,6 +30,14 @@ constexpr unsigned kSpinLimit = 1u << 22;               // bounded mbarrier wait
 constexpr int kMaxClusterSplits = 16;                   // splits merged inside one thread-block cluster
 constexpr int kRecvFloats = 1024;                       // CTA 0's receive area for pushed partials (4 KB)
 constexpr int kResidentPerSm = 2;                       // attention CTAs that fit one SM (shared memory)
+// Streaming decode kernel (decode_stream.cu): kStreamProducers producer warps and kStreamConsumers
+// consumer warps share a ring of at most kStreamMaxSlots sub-tile slots; its dynamic shared memory stays
+// within kStreamSmemMax so that two CTAs (two consecutive calls) share an SM.
+constexpr int kStreamConsumers = 4;
+constexpr int kStreamProducers = 4;
+constexpr int kStreamRows = 8;                          // query rows per KV head it serves (R <= 8)
+constexpr int kStreamMaxSlots = 12;
+constexpr size_t kStreamSmemMax = 110u * 1024u;
 // Arrival counters of the last-CTA merge live in a fixed region at the start of every workspace
 // (one slot per (b, h, row group); grid.z <= 65535 and at most 4 row groups), so no other data of
 // any call ever overlaps them and they stay zero between calls.
@@ -103,6 +112,9 @@ struct AttnParams {
     unsigned* counters;   // [B*Hkv*nrg] arrival counters for the last-CTA merge (sparse/prefix)
     float* out;           // [B, Hq, Mq, 128] fp32 (merged by the last CTA in sparse/prefix mode)
     unsigned* err;        // device error word
+    unsigned spin_limit;  // polls of a bounded mbarrier wait before it gives up (kSpinLimit)
+    unsigned test_stall;  // testing: polls of one extra wait on a barrier nothing arrives on (0: none)
+    int tail_tma;         // streaming decode: contiguous tail rows come by TMA through the tensor maps
 };
 
 struct FocalCombineParams {
@@ -176,6 +188,15 @@ fx_status set_error(fx_status st, const char* msg);
 
 // Launchers.  `pdl`: launch as a programmatic dependent of the preceding kernel on the stream.
 cudaError_t launch_attn_partial(const AttnParams& p, int mode, bool pdl, cudaStream_t s);
+// Decode-shaped sparse calls (one query position, R <= 8): p.stages = ring slots, p.nsplit = splits.
+// tk / tv: 4-D tensor maps of K and V ([B][Hkv][Tcap][128] bf16, boxes of 16 rows x 64 columns, 128-byte
+// swizzle) when p.tail_tma, else unused.
+cudaError_t launch_stream_decode(const AttnParams& p, const CUtensorMap* tk, const CUtensorMap* tv, bool pdl,
+                                 cudaStream_t s);
+// Encodes the tensor maps of a KV cache view for launch_stream_decode; false when the strides do not
+// allow a tensor map (the kernel then copies the tail rows itself).
+bool encode_kv_tensor_maps(const fx_kv_desc* kv, CUtensorMap* tk, CUtensorMap* tv);
+size_t stream_decode_smem_bytes(int slots, int nsplit, int R);
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_prefix_tc(const PrefixTcParams& p, bool pdl, cudaStream_t s);

@@ -100,7 +100,10 @@ def test_host_argument_checks_without_gpu(lib):
     assert sp(4, 8, 16, 7, 2304, 1024) > 0                                     # 56 rows: no tensor cores
     assert sp(0, 8, 16, 7, 2304, 1024) == 0 and sp(4, 8, 4, 7, 2304, 1024) == 0   # Br < 1, Hq < Hkv
     lib.fx_sparse_workspace_bytes.restype = ctypes.c_size_t
-    assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) > 0
+    # decode shapes (at most 8 query heads per KV head) merge their splits inside a cluster: no
+    # workspace; wider groups keep split partials in the workspace
+    assert lib.fx_sparse_workspace_bytes(8, 8, 16, 205, 4096, 4864) == 0
+    assert lib.fx_sparse_workspace_bytes(8, 1, 16, 205, 4096, 4864) > 0
     assert lib.fx_sparse_workspace_bytes(0, 8, 16, 205, 4096, 4864) == 0
     lib.fx_focal_workspace_bytes.restype = ctypes.c_size_t
     assert lib.fx_focal_workspace_bytes(8, 8, 16, 1, 4864) >= 8 * 8 * 2 * 4864 * 4

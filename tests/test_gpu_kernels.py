@@ -168,7 +168,7 @@ def _sorted_subsets(B, Hkv, pool, kk, seed):
 
 
 @pytest.mark.parametrize("G,kk,tail_lo", [(1, 64, 1000), (2, 205, 4096), (4, 2048, 6000), (8, 37, 500), (2, 0, 0),
-                                          (4, 300, 300)])
+                                          (4, 300, 300), (16, 205, 4096)])
 def test_sparse_matches_oracle(fx, G, kk, tail_lo):
     B, Hkv = 3, 2
     T = max(tail_lo + 513, 700)
@@ -527,9 +527,9 @@ def test_dense_prefix_tile_edges_on_tensor_cores(fx, G, Mq, Br, P):
     pu.assert_out_close(out, ref, vmax)
 
 
-def test_sparse_long_dense_tail_uses_global_merge(fx):
-    """More than 16 x 4096 keys in one row: the splits are merged through the workspace (not inside a
-    thread-block cluster)."""
+def test_sparse_long_dense_tail(fx):
+    """70000 keys in one row (one (b, h) pair): 16 splits of about 4400 keys, each CTA's ring cycling
+    hundreds of times, merged inside one cluster."""
     B, Hkv, G, T = 1, 1, 2, 70000
     k, v = kv_case(B, Hkv, T, 81)
     q = rnd((B, Hkv * G, 1, D), 81, 3)
@@ -581,3 +581,52 @@ def test_programmatic_dependent_launch_chain_is_identical(fx):
     assert fx.fx_device_errors() == 0
     ref = oracle.sparse_decode(k, v, length, q3, plain[2].cpu(), 700)
     pu.assert_out_close(plain[4], ref, float(v.float().abs().max()))
+
+
+def test_sparse_pdl_chain_of_layers_is_identical(fx):
+    """Twelve decode layers back to back as programmatic dependent launches that read their lengths,
+    index lists and K/V early (the next layer's CTAs are resident and loading while the previous layer
+    runs) give bit-identical results to plain launches, and match the oracle."""
+    B, Hkv, G, T, kk, L = 8, 8, 2, 1200, 205, 12
+    ks = torch.stack([rnd((B, Hkv, T, D), 120 + l, 1) for l in range(L)]).to("cuda")
+    vs = torch.stack([rnd((B, Hkv, T, D), 120 + l, 2) for l in range(L)]).to("cuda")
+    qs = torch.stack([rnd((B, Hkv * G, 1, D), 140 + l, 3) for l in range(L)]).to("cuda")
+    length = torch.tensor([T - 3 * b for b in range(B)], dtype=torch.int32)
+    idx = _sorted_subsets(B, Hkv, 800, kk, 7)
+    dl, di = dev(length), dev(idx)
+    outs = torch.zeros((2, L, B, Hkv * G, 1, D), dtype=torch.float32, device="cuda")
+    P, R = fx.FX_LAUNCH_PDL, fx.FX_LAUNCH_INPUTS_READY
+    for v_, fl in enumerate((0, P | R)):
+        for l in range(L):
+            fx.fx_sparse_gqa_decode(ks[l], vs[l], dl, qs[l], di, 800, out=outs[v_, l], flags=fl)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert torch.equal(outs[0], outs[1])
+    for l in (0, 5, 11):
+        ref = oracle.sparse_decode(ks[l].cpu(), vs[l].cpu(), length, qs[l].cpu(), idx, 800)
+        pu.assert_out_close(outs[1, l], ref, float(vs[l].float().abs().max()))
+
+
+def test_bounded_wait_runs_out_and_is_reported(fx):
+    """A device-side wait that nothing completes gives up after its poll limit: the call returns, the
+    context stays usable, the result is unaffected and FX_DEVERR_TIMEOUT is reported."""
+    B, Hkv, G, T = 2, 2, 2, 500
+    k, v = kv_case(B, Hkv, T, 61)
+    q = rnd((B, Hkv * G, 1, D), 61, 3)
+    length = torch.tensor([T, 321], dtype=torch.int32)
+    ref = oracle.sparse_decode(k, v, length, q, None, 0)
+    fx.fx_device_errors()
+    lib = fx.load_library()
+    lib.fx_test_stall_wait(2000)
+    try:
+        out = fx.fx_sparse_gqa_decode(dev(k), dev(v), dev(length), dev(q), None, 0)
+        torch.cuda.synchronize()
+        bits = fx.fx_device_errors()
+    finally:
+        lib.fx_test_stall_wait(0)
+    assert bits & fx.FX_DEVERR_TIMEOUT
+    pu.assert_out_close(out, ref, float(v.float().abs().max()))
+    again = fx.fx_sparse_gqa_decode(dev(k), dev(v), dev(length), dev(q), None, 0)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert torch.equal(out, again)
