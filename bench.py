@@ -461,6 +461,11 @@ def run_fx(args, rank, local, ws):
         "gpu_launches": run.launches_per_step * len(steps),
         "gpu_launches_source": run.launches_source,
     }
+    if not args.no_secondary:
+        # the other configurations, after the headline's timed region; they reuse nothing of it
+        del run
+        torch.cuda.empty_cache()
+        line["secondary"] = {name: fn(args, peak, peak_kind) for name, fn in SECONDARY.items()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -622,15 +627,53 @@ def run_kernel_case(args):
         raise SystemExit(1)
 
 
-def run_kv_select(args):
-    """The FastKV-shaped workload (4 sequences of 32768 tokens, 32 layers, 32 q / 8 kv heads): per-layer
-    KV retention once (window scores of every layer, its top 2040 + the 8 window tokens, compaction of
-    every layer with its own set), then decode steps over the compacted caches (one token per sequence
-    per step, 32 dense decode calls over 2048 + t rows).  One JSON line; not the headline workload."""
+# ----------------------------------------------------------------------------------------------
+# Secondary workloads: the other configurations of the scope, nested under "secondary" of the
+# headline line (each with its own metric, roofline of its dominant kernel, an oracle sample on the
+# host cores and an end-to-end leg through the same calls with host buffers).
+def _events_ms(fn, reps):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _graph(fn, dev):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream(dev)):
+        fn()
+    g.replay()                      # the first launch also uploads the graph
+    torch.cuda.synchronize()
+    return g
+
+
+def _roofline(kernel, nbytes, ms_per_launch, peak, peak_kind, **extra):
+    achieved = nbytes / (ms_per_launch / 1e3) / 1e9
+    r = {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+         "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_kind,
+         "avg_launch_us": round(ms_per_launch * 1e3, 3), "avg_bytes_per_launch": int(nbytes)}
+    r.update(extra)
+    return r
+
+
+def _oracle(threads):
+    import oracle as orc
+    orc.build()
+    return orc, orc.set_threads(threads)
+
+
+def secondary_kv_select(args, peak, peak_kind):
+    """FastKV-shaped: 4 sequences x 32768 tokens, 32 layers, 32 q / 8 kv heads.  Per-layer KV retention
+    once (window scores of every layer, its top 2040 + the 8 window tokens, compaction of every layer with
+    its own set), then decode steps over the compacted caches (one token per sequence per step: the new
+    K/V row appended, 32 dense decode calls over 2048 + t rows)."""
+    torch.cuda.empty_cache()
     import kv_cache_token_fx_gb300 as fx
     from synth.workloads import KvSelect
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     w = KvSelect()
     L, B, Hkv, Hq, T, win = w.n_layers, w.B, w.Hkv, w.Hq, w.T, w.window
     K = torch.empty((L, B, Hkv, T, D), dtype=torch.bfloat16, device=dev)
@@ -653,103 +696,245 @@ def run_kv_select(args):
                                                q_pos0=ncand, ws=ws, flags=pdl)
     retain()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 3
-    a.record()
-    for _ in range(reps):
-        retain()
-    b.record()
-    torch.cuda.synchronize()
-    retain_ms = a.elapsed_time(b) / reps
-    # algorithmic bytes: K rows of every layer for the scores (V is not read), the compaction's reads
-    # and writes of the kept rows
+    retain_ms = _events_ms(retain, 3)
+    # algorithmic bytes: K rows of every layer for the scores (V is not read), the compaction's reads and
+    # writes of the kept rows
     retain_bytes = L * B * Hkv * (T * 256 + w.keep * 512 * 2)
     del K, V
-    # decode: step t appends its K/V row at position keep + t of every layer, then attends densely
+    torch.cuda.empty_cache()
+    # decode: step t appends the new K/V row at position keep + t of every layer, then attends densely
+    n_steps = max(3, min(args.sec_steps, w.decode_steps))
+    n_warm = max(3, args.warmup)
+    app = [w.appended_kv(l, dev) for l in range(L)]
+    AK = torch.stack([a[0] for a in app])          # [L, B, Hkv, decode_steps, D]
+    AV = torch.stack([a[1] for a in app])
+    del app
     for l in range(L):
-        ak, av = w.appended_kv(l, dev)
-        CK[l, :, :, w.keep:w.keep + w.decode_steps] = ak
-        CV[l, :, :, w.keep:w.keep + w.decode_steps] = av
-    n_steps = min(args.steps, w.decode_steps)
-    Qd = torch.stack([torch.stack([w.decode_query(t, l, dev) for l in range(L)]) for t in range(n_steps)])
-    lens = torch.tensor([[w.keep + t + 1] * B for t in range(n_steps)], dtype=torch.int32, device=dev)
+        CK[l, :, :, w.keep:w.keep + w.decode_steps] = AK[l]
+        CV[l, :, :, w.keep:w.keep + w.decode_steps] = AV[l]
+    tot = n_warm + n_steps
+    Qd = torch.stack([torch.stack([w.decode_query(t, l, dev) for l in range(L)]) for t in range(tot)])
+    lens = torch.tensor([[w.keep + t + 1] * B for t in range(tot)], dtype=torch.int32, device=dev)
     O = torch.empty((L, B, Hq, 1, D), dtype=torch.float32, device=dev)
-    dws = fx.Workspace(dev, fx.fx_sparse_workspace_bytes(B, Hkv, Hq, 0, 0, cap))
     fl = pdl | (0 if args.no_pdl else fx.FX_LAUNCH_INPUTS_READY)
 
-    def step(t):
+    def step(t, first_flags=fl):
         for l in range(L):
-            fx.fx_sparse_gqa_decode(CK[l], CV[l], lens[t], Qd[t, l], None, 0, out=O[l], ws=dws, flags=fl)
+            fx.fx_sparse_gqa_decode(CK[l], CV[l], lens[t], Qd[t, l], None, 0, out=O[l],
+                                    flags=first_flags if l == 0 else fl)
+
     step(0)
     torch.cuda.synchronize()
-    graphs = []
-    s = torch.cuda.Stream(dev)
-    for t in range(n_steps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            step(t)
-        graphs.append(g)
-    for g in graphs:
-        g.replay()
-    for t in range(max(args.warmup, 3)):
-        graphs[t % n_steps].replay()
+    graphs = [_graph(lambda t=t: step(t), dev) for t in range(tot)]
+    for t in range(n_warm):
+        graphs[t].replay()
     torch.cuda.synchronize()
-    sampler = ClockSampler(0)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with sampler:
-        a.record()
-        for g in graphs:
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    bits = fx.fx_device_errors()
-    if bits:
-        raise RuntimeError(f"device error bits {bits}")
-    # per decode call: K+V rows of (keep + t + 1) positions, q, out
-    dec_bytes = sum(L * (B * Hkv * (w.keep + t + 1) * ROW_BYTES + B * Hq * D * 6) for t in range(n_steps))
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:   # ms: per step
+        ms = _events_ms(lambda it=iter(range(n_warm, tot)): graphs[next(it)].replay(), n_steps)
+    if fx.fx_device_errors():
+        raise RuntimeError("device error flag set (kv_select)")
+    dec_bytes = sum(L * (B * Hkv * (w.keep + t + 1) * ROW_BYTES + B * Hq * D * 6) for t in range(n_warm, tot))
     n_calls = L * n_steps
-    achieved = dec_bytes / (ms / 1e3) / 1e9
-    peak, peak_kind = measured_hbm_peak()
-    line = {
+    # end to end: each step copies its queries and new K/V rows from pinned host memory, appends the rows
+    # (fx_kv_append), decodes, and copies the 32 layers' outputs back
+    nq = Qd[0].numel()
+    knew = torch.stack([AK[:, :, :, t] for t in range(tot)])      # [tot, L, B, Hkv, D]
+    vnew = torch.stack([AV[:, :, :, t] for t in range(tot)])
+    In_host = torch.cat([Qd.reshape(tot, -1), knew.reshape(tot, -1), vnew.reshape(tot, -1)], 1).cpu().pin_memory()
+    nkv = knew[0].numel()
+    del knew, vnew
+    O_host = torch.empty(O.shape, dtype=torch.float32).pin_memory()
+    KVn = torch.empty(2 * nkv, dtype=torch.bfloat16, device=dev)
+    pos = (lens - 1).contiguous()
+
+    def e2e_step(t):
+        Qd[t].copy_(In_host[t, :nq].view(Qd[t].shape), non_blocking=True)
+        KVn.copy_(In_host[t, nq:], non_blocking=True)
+        shp = (L, B, Hkv, D)
+        fx.fx_kv_append(CK, CV, KVn[:nkv].view(shp), KVn[nkv:].view(shp), pos[t])
+        step(t, first_flags=pdl)
+        O_host.copy_(O, non_blocking=True)
+
+    eg = [_graph(lambda t=t: e2e_step(t), dev) for t in range(tot)]
+    for t in range(n_warm):
+        eg[t].replay()
+    torch.cuda.synchronize()
+    ems = _events_ms(lambda it=iter(range(n_warm, tot)): eg[next(it)].replay(), n_steps)
+    e2e = {"value": round(B / (ems / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": int(In_host[0].numel() * 2),
+           "d2h_bytes_per_step": int(O_host.numel() * 4), "ms_per_step": round(ems, 4)}
+    # the oracle on the host cores: decode steps of 1 of the 4 sequences over the same compacted caches
+    cpu = None
+    if not args.no_cpu_baseline:
+        orc, cores = _oracle(min(os.cpu_count() or 1, Hkv))
+        ck_h, cv_h = CK[:, :1].cpu(), CV[:, :1].cpu()
+        qd_h = Qd[:, :, :1].cpu()
+        t0 = time.perf_counter()
+        done = 0
+        for t in range(n_warm, tot):
+            lt = torch.tensor([w.keep + t + 1], dtype=torch.int32)
+            for l in range(L):
+                orc.sparse_decode(ck_h[l], cv_h[l], lt, qd_h[t, l], None, 0)
+            done += 1
+            if time.perf_counter() - t0 > args.cpu_seconds / 3:
+                break
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(done / dt, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{done} decode steps of 1 of the 4 sequences, all 32 layers, over the compacted caches "
+                         f"(fp64 C oracle, {cores} threads over KV heads; retention not in the sample)"}
+    peak_frac = retain_bytes / (retain_ms / 1e3) / 1e9 / peak
+    res = {
         "metric": "kv_select decode tokens/s (FastKV per-layer retention, then dense decode over the kept rows)",
-        "value": round(B * n_steps / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": n_steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": round(ms / n_steps, 4), "higher_is_better": True,
-        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+        "value": round(B / (ms / 1e3), 1), "unit": "tokens/s", "steps": n_steps, "warmup": n_warm,
+        "ms_per_step": round(ms, 4),
         "config": {"workload": "kv_select: 4 sequences x 32768 tokens, 32 layers, 32 q / 8 kv heads, d 128; every "
                                "layer keeps its own top 2040 by the last 8 positions' attention + the 8 window "
                                "tokens; decode over 2048 + t kept rows",
-                   "timing": "per-step CUDA graphs of 32 decode calls, CUDA events"},
-        "roofline": {"kernel": "fx_sparse_gqa_decode (dense over the compacted cache)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "peak_source": peak_kind,
-                     "avg_launch_us": round(ms * 1e3 / n_calls, 3), "avg_bytes_per_launch": int(dec_bytes / n_calls)},
+                   "timing": "per-step CUDA graphs of 32 decode calls, CUDA events",
+                   "l2": "inputs larger than L2 (1.1 GB of kept rows read per step)"},
+        "roofline": _roofline("fx_sparse_gqa_decode (dense over the compacted cache)", dec_bytes / n_calls,
+                              ms / L, peak, peak_kind),
         "retention": {"ms": round(retain_ms, 3), "algorithmic_bytes": int(retain_bytes),
-                      "gbs": round(retain_bytes / (retain_ms / 1e3) / 1e9, 1),
-                      "frac": round(retain_bytes / (retain_ms / 1e3) / 1e9 / peak, 4),
+                      "gbs": round(retain_bytes / (retain_ms / 1e3) / 1e9, 1), "frac": round(peak_frac, 4),
                       "launches": L * 3 + 1, "kept_rows": int(clen[0])},
-        "clocks": sampler.summary(), "gpu_launches": n_calls,
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": sampler.summary(), "gpu_launches": n_calls,
     }
-    print(json.dumps(line), flush=True)
+    return res
 
 
-def run_hpd_branch(args):
-    """The HPD-Parsing-shaped draft verification (512 branches sharing a 2304-token prefix, private
-    suffixes of U[0, 1024] tokens, 7 draft positions, 16 q / 8 kv heads, 28 layers): a step verifies
-    every branch's 7 draft tokens at every layer.  Dense: attention over the whole prefix; sparse: over
-    the 256 prefix tokens per (branch, KV head) chosen at the first layer by the branch's draft queries
-    (prefix scoring + top-k), then every layer.  Layer inputs (1.14 GB each) are cycled over 4 buffers.
-    One JSON line; not the headline workload."""
+def secondary_long_ctx(args, peak, peak_kind):
+    """Long-context: 64 sequences x 131072 tokens, 32 q / 8 kv heads.  A step is one focal pass over the
+    whole cache (attention + importance of every token; 34.4 GB of K/V), the top 2048 tokens per KV head,
+    and 16 layers of sparse decode over them.  The sparse layers read the focal layer's cache (one 34 GB
+    buffer; the 537 MB a sparse layer gathers is still 4x the L2) with their own queries."""
+    torch.cuda.empty_cache()
+    import kv_cache_token_fx_gb300 as fx
+    from synth.workloads import LongCtx
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = LongCtx()
+    B, Hkv, Hq, T, k_sel, NL = w.B, w.Hkv, w.Hq, w.T, w.k, w.n_layers
+    K, V = w.layer_kv(0, device=dev)
+    ln = torch.full((B,), T, dtype=torch.int32, device=dev)
+    Qs = torch.stack([w.query(l, dev) for l in range(NL + 1)])      # [17, B, Hq, 1, D]: focal + 16 sparse
+    scores = torch.empty((B, Hkv, T), dtype=torch.float32, device=dev)
+    idx = torch.empty((B, Hkv, k_sel), dtype=torch.int32, device=dev)
+    O = torch.empty((NL + 1, B, Hq, 1, D), dtype=torch.float32, device=dev)
+    ws = fx.Workspace(dev, max(fx.fx_focal_workspace_bytes(B, Hkv, Hq, 1, T),
+                               fx.fx_sparse_workspace_bytes(B, Hkv, Hq, k_sel, T, T)))
+    pdl = 0 if args.no_pdl else fx.FX_LAUNCH_PDL
+    ready = 0 if args.no_pdl else fx.FX_LAUNCH_INPUTS_READY
+
+    def focal_only(fl=pdl | ready):
+        fx.fx_focal_attn_scores(K, V, ln, Qs[0], out=O[0], scores=scores, ws=ws, flags=fl)
+
+    def focal(fl=pdl | ready):
+        focal_only(fl)
+        fx.fx_topk_select(scores, k_sel, out=idx, flags=pdl)
+
+    def sparse():
+        for l in range(NL):
+            fx.fx_sparse_gqa_decode(K, V, ln, Qs[l + 1], idx, T, out=O[l + 1], ws=ws, flags=pdl | (ready if l else 0))
+
+    def step():
+        focal()
+        sparse()
+
+    step()
+    torch.cuda.synchronize()
+    g_step, g_focal, g_sparse = _graph(step, dev), _graph(focal_only, dev), _graph(sparse, dev)
+    n_steps = max(3, min(args.sec_steps, 8))
+    for _ in range(max(3, args.warmup)):
+        g_step.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        ms = _events_ms(g_step.replay, n_steps)
+    f_ms = _events_ms(g_focal.replay, n_steps)
+    s_ms = _events_ms(g_sparse.replay, n_steps)
+    if fx.fx_device_errors():
+        raise RuntimeError("device error flag set (long_ctx)")
+    kv_all = B * Hkv * T * ROW_BYTES                              # the focal pass reads every row
+    focal_bytes = kv_all + B * Hq * D * 6 + B * Hkv * T * 4        # + q, out, scores
+    sparse_bytes = B * Hkv * k_sel * ROW_BYTES + B * Hq * D * 6 + B * Hkv * k_sel * 4
+    # end to end: each step copies the 17 layers' queries in and their outputs out
+    Q_host = Qs.cpu().pin_memory()
+    O_host = torch.empty(O.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        Qs.copy_(Q_host, non_blocking=True)
+        focal(fl=pdl)
+        sparse()
+        O_host.copy_(O, non_blocking=True)
+
+    g_e2e = _graph(e2e_step, dev)
+    for _ in range(3):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    ems = _events_ms(g_e2e.replay, n_steps)
+    e2e = {"value": round(B / (ems / 1e3), 2), "unit": "tokens/s", "h2d_bytes_per_step": int(Q_host.numel() * 2),
+           "d2h_bytes_per_step": int(O_host.numel() * 4), "ms_per_step": round(ems, 4)}
+    cpu = None
+    if not args.no_cpu_baseline:
+        # the oracle on 1 of the 512 (sequence, KV head) rows, the whole step (focal pass, top-k, 16 sparse
+        # layers); the rate is scaled by 512 rows to a 64-sequence step
+        orc, cores = _oracle(os.cpu_count() or 1)
+        G = Hq // Hkv
+        b, h = 17, 5
+        kr, vr = w.layer_kv_rows(0, b, h)
+        kv1 = (kr.view(1, 1, T, D).contiguous(), vr.view(1, 1, T, D).contiguous())
+        qh = Qs[:, b:b + 1, h * G:(h + 1) * G].cpu().contiguous()
+        lt = torch.tensor([T], dtype=torch.int32)
+        t0 = time.perf_counter()
+        _, sc = orc.focal(kv1[0], kv1[1], lt, qh[0])
+        sel = torch.from_numpy(orc.topk(sc, k_sel))
+        for l in range(NL):
+            orc.sparse_decode(kv1[0], kv1[1], lt, qh[l + 1], sel, T)
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(B / (dt * B * Hkv), 5), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"one whole step (focal pass over 131072 tokens, top-2048, 16 sparse layers) for 1 of the "
+                         f"512 (sequence, KV head) rows in {dt:.2f} s, scaled by 512 rows (fp64 C oracle, {cores} "
+                         f"threads)"}
+    del K, V
+    torch.cuda.empty_cache()
+    return {
+        "metric": "long_ctx decode tokens/s (focal pass over 131072 tokens + top-2048 + 16 sparse layers)",
+        "value": round(B / (ms / 1e3), 2), "unit": "tokens/s", "steps": n_steps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms, 4),
+        "config": {"workload": "long_ctx: 64 sequences x 131072 tokens, 32 q / 8 kv heads, d 128, 64 planted clusters "
+                               "of 16 tokens per (sequence, KV head); focal pass, top 2048 per KV head, 16 sparse "
+                               "layers", "timing": "one CUDA graph per step, CUDA events",
+                   "l2": "inputs larger than L2 (34.4 GB focal stream)"},
+        "focal_scoring": {"ms": round(f_ms, 4), "gbs": round(kv_all / (f_ms / 1e3) / 1e9, 1),
+                          "tokens_scanned_per_s": round(B * T / (f_ms / 1e3), 0),
+                          "note": "focal attention + importance of every token (the top-2048 is in the step only)"},
+        "gathered_sparse": {"ms_per_layer": round(s_ms / NL, 4),
+                            "gbs": round(B * Hkv * k_sel * ROW_BYTES * NL / (s_ms / 1e3) / 1e9, 1),
+                            "tokens_per_s": round(B * NL / (s_ms / 1e3), 1)},
+        "roofline": _roofline("fx_focal_attn_scores (focal pass + combine)", focal_bytes, f_ms, peak, peak_kind,
+                              note="the call's two kernels (split-KV attention with logits, then the combine that "
+                                   "forms the scores); algorithmic bytes exclude the logits' round trip"),
+        "roofline_sparse": _roofline("fx_sparse_gqa_decode (2048 gathered rows per (b, h))", sparse_bytes, s_ms / NL,
+                                     peak, peak_kind),
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": sampler.summary(), "gpu_launches": 2 + 1 + NL,
+    }
+
+
+def secondary_hpd_branch(args, peak, peak_kind):
+    """HPD-Parsing-shaped draft verification (512 branches sharing a 2304-token prefix, private suffixes of
+    U[0, 1024] tokens, 7 draft positions, 16 q / 8 kv heads, 28 layers): a step verifies every branch's 7
+    draft tokens at every layer.  Dense: attention over the whole prefix; sparse: over the 256 prefix tokens
+    per (branch, KV head) chosen at the first layer by the branch's draft queries (prefix scoring + top-k),
+    then every layer.  Layer inputs (1.14 GB each) are cycled over 4 buffers."""
+    torch.cuda.empty_cache()
     import kv_cache_token_fx_gb300 as fx
     from synth.workloads import HpdBranch
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     w = HpdBranch()
     Br, Hkv, Hq, Mq, P, L = w.Br, w.Hkv, w.Hq, w.Mq, w.P, w.n_layers
     NB = 4
     bufs = [w.layer_inputs(l, device=dev) for l in range(NB)]
     S = int(bufs[0]["off"][-1])
-    out = torch.empty((Br, Hq, Mq, D), dtype=torch.float32, device=dev)
+    out = torch.empty((L, Br, Hq, Mq, D), dtype=torch.float32, device=dev)
     ws = fx.Workspace(dev, max(fx.fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, P, w.max_suffix),
                                fx.fx_shared_prefix_workspace_bytes(Br, Hkv, Hq, Mq, w.kp, w.max_suffix),
                                fx.fx_focal_workspace_bytes(Br, Hkv, Hq, Mq, P)))
@@ -759,76 +944,123 @@ def run_hpd_branch(args):
     pdl = 0 if args.no_pdl else fx.FX_LAUNCH_PDL
     ready = 0 if args.no_pdl else fx.FX_LAUNCH_INPUTS_READY
 
-    def dense_step():
+    def dense_step(fl0=pdl | ready):
         for l in range(L):
             d = bufs[l % NB]
             fx.fx_shared_prefix_decode(d["pk"], d["pv"], d["sk"], d["sv"], d["off"], d["dk"], d["dv"], d["q"],
-                                       max_suffix=w.max_suffix, out=out, ws=ws, flags=pdl | ready)
+                                       max_suffix=w.max_suffix, out=out[l], ws=ws,
+                                       flags=fl0 if l == 0 else pdl | ready)
 
     def sparse_step():
         d = bufs[0]
-        # every branch sees the same prefix rows (batch stride 0)
-        pk4 = d["pk"].unsqueeze(0).expand(Br, Hkv, P, D)
+        pk4 = d["pk"].unsqueeze(0).expand(Br, Hkv, P, D)      # every branch sees the same prefix rows
         pv4 = d["pv"].unsqueeze(0).expand(Br, Hkv, P, D)
         fx.fx_focal_attn_scores(pk4, pv4, plen, d["q"], want_out=False, scores=pscores, ws=ws, flags=pdl | ready)
         fx.fx_topk_select(pscores, w.kp, out=pidx, flags=pdl)
         for l in range(L):
             d = bufs[l % NB]
             fx.fx_shared_prefix_decode(d["pk"], d["pv"], d["sk"], d["sv"], d["off"], d["dk"], d["dv"], d["q"],
-                                       max_suffix=w.max_suffix, prefix_idx=pidx, out=out, ws=ws,
+                                       max_suffix=w.max_suffix, prefix_idx=pidx, out=out[l], ws=ws,
                                        flags=pdl | (ready if l > 0 else 0))
 
+    n = max(3, min(args.sec_steps, 16))
     res = {}
     for name, fn in (("dense", dense_step), ("sparse", sparse_step)):
         fn()
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(dev)
-        with torch.cuda.graph(g, stream=s):
-            fn()
+        g = _graph(fn, dev)
         for _ in range(max(args.warmup, 3)):
             g.replay()
         torch.cuda.synchronize()
-        n = max(3, min(args.steps, 16))
-        sampler = ClockSampler(0)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(torch.cuda.current_device())
         with sampler:
-            a.record()
-            for _ in range(n):
-                g.replay()
-            b.record()
-            torch.cuda.synchronize()
-        res[name] = (a.elapsed_time(b) / n, n, sampler.summary())
-    bits = fx.fx_device_errors()
-    if bits:
-        raise RuntimeError(f"device error bits {bits}")
-    # algorithmic bytes per dense layer call: prefix K/V once, every branch's suffix and draft rows, q, out
+            ms = _events_ms(g.replay, n)
+        res[name] = (ms, sampler.summary())
+    if fx.fx_device_errors():
+        raise RuntimeError("device error flag set (hpd_branch)")
+    # algorithmic bytes per layer call: prefix K/V once, every branch's suffix and draft rows, q, out
     row = 2 * D * 2
-    dense_bytes = Hkv * P * row + Hkv * S * row + Br * Mq * Hkv * row + Br * Hq * Mq * D * (2 + 4)
-    sparse_bytes = Hkv * P * row + Hkv * S * row + Br * Mq * Hkv * row + Br * Hq * Mq * D * (2 + 4)
-    peak, peak_kind = measured_hbm_peak()
-    ms_d, n_d, clk = res["dense"]
-    ms_s, n_s, _ = res["sparse"]
+    layer_bytes = Hkv * P * row + Hkv * S * row + Br * Mq * Hkv * row + Br * Hq * Mq * D * (2 + 4)
+    ms_d, clk = res["dense"]
+    ms_s, _ = res["sparse"]
     tokens = Br * Mq
-    line = {
+    # end to end: each step copies every layer's draft queries and draft K/V rows in (from pinned host
+    # memory, cycled like the device buffers) and all 28 layers' outputs out
+    host = [torch.cat([b_["q"].reshape(-1), b_["dk"].reshape(-1), b_["dv"].reshape(-1)]).cpu().pin_memory()
+            for b_ in bufs]
+    nq, nd = bufs[0]["q"].numel(), bufs[0]["dk"].numel()
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    stage = [torch.empty(host[0].numel(), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
+
+    def e2e_step():
+        for l in range(L):
+            st_ = stage[l % NB]
+            st_.copy_(host[l % NB], non_blocking=True)
+            d = bufs[l % NB]
+            fx.fx_shared_prefix_decode(d["pk"], d["pv"], d["sk"], d["sv"], d["off"],
+                                       st_[nq:nq + nd].view(d["dk"].shape), st_[nq + nd:].view(d["dv"].shape),
+                                       st_[:nq].view(d["q"].shape), max_suffix=w.max_suffix, out=out[l], ws=ws,
+                                       flags=pdl)
+        out_host.copy_(out, non_blocking=True)
+
+    g_e2e = _graph(e2e_step, dev)
+    for _ in range(3):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    ems = _events_ms(g_e2e.replay, n)
+    e2e = {"value": round(tokens / (ems / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(L * host[0].numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 4),
+           "ms_per_step": round(ems, 4), "note": "dense variant"}
+    cpu = None
+    if not args.no_cpu_baseline:
+        # the oracle on 16 of the 512 branches for 2 of the 28 layers (dense), scaled to a 28-layer step
+        orc, cores = _oracle(os.cpu_count() or 1)
+        d = w.small_inputs(0, device="cpu")
+        off = w.offsets().tolist()
+        nb_ = 16
+        t0 = time.perf_counter()
+        for layer in range(2):
+            for b in range(nb_):
+                sk, sv = w.suffix_rows(0, b)
+                o1 = torch.tensor([0, off[b + 1] - off[b]], dtype=torch.int32)
+                orc.shared_prefix(d["pk"], d["pv"], sk, sv, o1, d["dk"][b:b + 1], d["dv"][b:b + 1], d["q"][b:b + 1])
+        dt = time.perf_counter() - t0
+        per_branch_layer = dt / (2 * nb_)
+        cpu = {"value": round(Mq / (per_branch_layer * L), 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"dense verification of 16 of the 512 branches for 2 of the 28 layers in {dt:.2f} s "
+                         f"(including the host-side generation of their suffix rows), scaled to one branch's 7 "
+                         f"draft tokens over 28 layers (fp64 C oracle, {cores} threads)"}
+    del bufs, stage
+    torch.cuda.empty_cache()
+    return {
         "metric": "hpd_branch verified draft tokens/s (shared-prefix draft verification, dense prefix)",
-        "value": round(tokens / (ms_d / 1e3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": n_d,
-        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_d, 4), "higher_is_better": True,
-        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic",
+        "value": round(tokens / (ms_d / 1e3), 1), "unit": "tokens/s", "steps": n, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_d, 4),
         "config": {"workload": "hpd_branch: 512 branches, shared prefix 2048 + 256 tokens, suffix U[0,1024] tokens, "
                                "7 draft positions, 16 q / 8 kv heads, d 128, 28 layers (inputs cycled over 4 buffers)",
-                   "suffix_rows": S, "timing": "one CUDA graph per step, CUDA events"},
-        "roofline": {"kernel": "fx_shared_prefix_decode (dense prefix)", "bound": "hbm",
-                     "achieved": round(dense_bytes * L / (ms_d / 1e3) / 1e9, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(dense_bytes * L / (ms_d / 1e3) / 1e9 / peak, 4), "traffic": None,
-                     "peak_source": peak_kind, "avg_launch_us": round(ms_d * 1e3 / L, 3),
-                     "avg_bytes_per_launch": int(dense_bytes)},
+                   "suffix_rows": S, "timing": "one CUDA graph per step, CUDA events",
+                   "l2": "inputs larger than L2 (1.14 GB per layer)"},
+        "roofline": _roofline("fx_shared_prefix_decode (dense prefix)", layer_bytes, ms_d / L, peak, peak_kind),
         "sparse": {"value": round(tokens / (ms_s / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms_s, 4),
                    "note": "prefix scoring + top-256 at the first layer, then 28 sparse-prefix layers",
-                   "layer_bytes": int(sparse_bytes)},
-        "clocks": clk, "gpu_launches": L * n_d,
+                   "roofline": _roofline("fx_shared_prefix_decode (sparse prefix)", layer_bytes, ms_s / L, peak,
+                                         peak_kind, note="same algorithmic bytes as dense: prefix rows come from L2")},
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": clk, "gpu_launches": L * n,
     }
-    print(json.dumps(line), flush=True)
+
+
+SECONDARY = {"kv_select": secondary_kv_select, "long_ctx": secondary_long_ctx, "hpd_branch": secondary_hpd_branch}
+
+
+def run_secondary_alone(args, name):
+    torch.cuda.set_device(0)
+    peak, peak_kind = measured_hbm_peak()
+    res = SECONDARY[name](args, peak, peak_kind)
+    res["n_gpus"] = 1
+    res["higher_is_better"] = True
+    res["dtype"] = "bf16 in, fp32 accumulate"
+    res["data"] = "synthetic"
+    print(json.dumps(res), flush=True)
 
 
 def main():
@@ -845,18 +1077,18 @@ def main():
                     help="run a small fixed case of one kernel (for profiler captures) instead of the bench")
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--reps", type=int, default=2)
-    ap.add_argument("--workload", choices=["ocr_decode", "kv_select", "hpd_branch"], default="ocr_decode",
+    ap.add_argument("--workload", choices=["ocr_decode", "kv_select", "long_ctx", "hpd_branch"], default="ocr_decode",
                     help="ocr_decode: the headline workload; kv_select: FastKV per-layer retention + decode; "
-                         "hpd_branch: shared-prefix draft verification")
+                         "long_ctx: 131072-token focal pass + sparse layers; hpd_branch: shared-prefix draft "
+                         "verification.  The others also run nested under 'secondary' of the headline line.")
+    ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
+    ap.add_argument("--sec-steps", type=int, default=8, help="timed steps of each secondary workload")
     args = ap.parse_args()
     if args.kernel_case:
         run_kernel_case(args)
         return
-    if args.workload == "kv_select" and args.impl == "fx":
-        run_kv_select(args)
-        return
-    if args.workload == "hpd_branch" and args.impl == "fx":
-        run_hpd_branch(args)
+    if args.workload != "ocr_decode" and args.impl == "fx":
+        run_secondary_alone(args, args.workload)
         return
     if args.warmup < 3 and args.impl == "fx":
         args.warmup = 3

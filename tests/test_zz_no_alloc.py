@@ -4,14 +4,15 @@ fx_focal_attn_scores_noalloc exists for callers that cannot allocate device memo
 during CUDA graph capture, real-time loops that allow no allocator calls after start-up, hosts that
 only have the C interface.  It keeps its scratch in a fixed array inside the library instead of a
 caller workspace.  This test calls it through the C ABI, twice in a row with different inputs, and
-checks each result against fx_focal_attn_scores with a caller workspace, within the tolerances used by
-every parity test here.  The file name makes pytest collect it last.
+checks each result against fx_focal_attn_scores with a caller workspace and against the fp64 oracle,
+within the tolerances used by every parity test here.  The file name makes pytest collect it last.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 import synth
 from tests import parity_util as pu
 
@@ -59,8 +60,13 @@ def test_noalloc_focal_matches_workspace_call_twice():
         assert st == 0, lib.fx_last_error()
         torch.cuda.synchronize()
         assert fx.fx_device_errors() == 0
-        pu.assert_out_close(out, ref_out, float(v.float().abs().max()), what=f"call {call} out")
+        vmax = float(v.float().abs().max())
+        pu.assert_out_close(out, ref_out, vmax, what=f"call {call} out")
         pu.assert_scores_close(sc, ref_sc, what=f"call {call} scores")
+        # and against the oracle on the same inputs
+        orc_out, orc_sc = oracle.focal(k.cpu(), v.cpu(), length.cpu(), q.cpu(), cand=(0, T))
+        pu.assert_out_close(out, orc_out, vmax, what=f"call {call} out vs oracle")
+        pu.assert_scores_close(sc, orc_sc, what=f"call {call} scores vs oracle")
 
     # a call needing more scratch than the fixed array is refused before anything is launched
     # (the descriptor claims 64 x 8 x 32768 rows; the call is refused before anything reads them)
