@@ -241,8 +241,10 @@ class OcrDecodeRun:
         ln = self.lens[t]
         launches = 0
         after_topk = after_writer
+        # FastOCR's cross-step fixation reuse: which set each layer attends over (library schedule)
+        kinds, srcs = fx.fx_csfr_schedule(w.n_layers, w.focal_layers, first_step=(t == 0))
         for l in range(w.n_layers):
-            if l in w.focal_layers:
+            if kinds[l] == fx.FX_CSFR_FOCAL:
                 if only_sparse:
                     continue
                 fx.fx_focal_attn_scores(self.K[l], self.V[l], ln, self.Q[t, l], cand=(0, w.n_vis), out=self.O[l],
@@ -254,12 +256,10 @@ class OcrDecodeRun:
                 launches += 2   # attention + top-k (a separate combine kernel, if any, is not counted here)
                 after_topk = True
                 continue
-            if l < w.focal_layers[0]:
-                sel = self.sets[w.focal_layers[-1]][1 - p] if t > 0 else None
-            elif l < w.focal_layers[-1]:
-                sel = self.sets[w.focal_layers[0]][p]
+            if kinds[l] == fx.FX_CSFR_DENSE:
+                sel = None
             else:
-                sel = self.sets[w.focal_layers[-1]][p]
+                sel = self.sets[srcs[l]][p if kinds[l] == fx.FX_CSFR_CURRENT else 1 - p]
             n_keys = (w.k_keep + w.length_at(t) - w.n_vis) if sel is not None else w.length_at(t)
             nbytes = (w.B * w.Hkv * n_keys * ROW_BYTES + w.B * w.Hq * D * (2 + 4) +
                       (w.B * w.Hkv * w.k_keep * 4 if sel is not None else 0))
@@ -475,19 +475,16 @@ def _oracle_step(w, orc, kv_host, q_host, t, prev_sets, B):
     """One decode step of the fp64 oracle for the first B sequences: returns the new focal sets."""
     length = torch.full((B,), w.length_at(t), dtype=torch.int32)
     sets = {}
+    sched = orc.csfr_schedule(w.n_layers, w.focal_layers, first_step=not prev_sets)
     for l in range(w.n_layers):
         k, v = kv_host[l]
         q = q_host[t][l]
-        if l in w.focal_layers:
+        kind, src = sched[l]
+        if kind == "focal":
             _, sc = orc.focal(k, v, length, q, cand=(0, w.n_vis))
             sets[l] = torch.from_numpy(orc.topk(sc, w.k_keep))
             continue
-        if l < w.focal_layers[0]:
-            sel = prev_sets.get(w.focal_layers[-1])
-        elif l < w.focal_layers[-1]:
-            sel = sets[w.focal_layers[0]]
-        else:
-            sel = sets[w.focal_layers[-1]]
+        sel = None if kind == "dense" else (sets[src] if kind == "current" else prev_sets[src])
         if sel is None:
             orc.sparse_decode(k, v, length, q, None, 0)
         else:

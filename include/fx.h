@@ -43,6 +43,10 @@
  *                                loads, before that kernel finishes.  Queries, outputs and workspace
  *                                are still touched only after it finishes.
  *     0 gives ordinary stream-ordered launches.
+ *   - The library keeps a little state per device (the address of its device error word, the SM count,
+ *     and for the no-allocation call the address of its scratch array), looked up on the first call on
+ *     each device.  A cudaDeviceReset invalidates it: make no library call on a device after resetting
+ *     it in the same process.
  *   - Host-side argument errors return a status and set a thread-local message (fx_last_error);
  *     nothing is enqueued then.  Data that only the device can see (lengths, indices, offsets) is
  *     checked by the kernels: a bad value is clamped or skipped -- never dereferenced -- and a bit is
@@ -189,6 +193,28 @@ FX_API fx_status fx_focal_mass(const float* scores, int rows, int n, int R, int 
 FX_API fx_status fx_choose_focal_layers(const float* ratio, int n_layers, int C, int32_t* layers_out);
 
 /* ------------------------------------------------------------------------------------------- */
+/* fx_csfr_schedule -- which index set every layer of one decode step attends over (host only, no GPU).
+ * [FastOCR] Focal-Guided Pruning (a focal layer refreshes the set; the layers after it, down to the next
+ * focal layer, attend only to that set) and Cross-Step Fixation Reuse (the layers before the first
+ * focal layer reuse the previous step's set of the deepest focal layer).
+ *
+ * focal_layers: the C focal layers, strictly ascending, each in [0, n_layers).  first_step != 0: no
+ * previous step exists (its layers before the first focal layer attend densely).  For each layer l:
+ *   kind[l] = FX_CSFR_FOCAL     l is focal: fx_focal_attn_scores + fx_topk_select make its set; src[l] = l
+ *             FX_CSFR_CURRENT   attend over this step's set of focal layer src[l] (the nearest above l)
+ *             FX_CSFR_PREVIOUS  attend over the previous step's set of focal layer src[l] (the deepest)
+ *             FX_CSFR_DENSE     attend over the whole cache (first step, before the first focal layer);
+ *                               src[l] = -1
+ * kind, src: host arrays of n_layers entries.
+ */
+#define FX_CSFR_FOCAL 0
+#define FX_CSFR_CURRENT 1
+#define FX_CSFR_PREVIOUS 2
+#define FX_CSFR_DENSE 3
+FX_API fx_status fx_csfr_schedule(int n_layers, const int32_t* focal_layers, int C, int first_step, int32_t* kind,
+                                  int32_t* src);
+
+/* ------------------------------------------------------------------------------------------- */
 /* fx_sparse_gqa_decode -- a non-focal layer: decode attention over the selected tokens only.
  * [FastOCR] Focal-Guided Pruning (non-focal layers attend only to the pruned set; the full cache
  * stays intact); [FastKV] 2.B (decoding over the retained entries).
@@ -304,7 +330,9 @@ FX_API fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride
  * cores (128-row x 128-key tiles, bf16 products with fp32 accumulation, the probabilities as bf16
  * hi + lo parts): two launches, the prefix partials held in the workspace (included in the size
  * above) and folded into the verify kernel's merge.  The result agrees with the single-kernel route
- * within the same output tolerance.
+ * within the same output tolerance.  Each CTA of that route allocates all 512 columns of its SM's
+ * tensor memory and the allocation waits, without a limit, for them to be free: run no other kernel
+ * that holds tensor memory concurrently on another stream.
  */
 typedef struct {
     const fx_bf16* k;

@@ -19,7 +19,8 @@ from . import build as _build
 
 __all__ = [
     "FxError", "load_library", "library_path", "Workspace", "fx_focal_attn_scores", "fx_topk_select",
-    "fx_focal_mass", "fx_choose_focal_layers",
+    "fx_focal_mass", "fx_choose_focal_layers", "fx_csfr_schedule", "FX_CSFR_FOCAL", "FX_CSFR_CURRENT",
+    "FX_CSFR_PREVIOUS", "FX_CSFR_DENSE",
     "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_append", "fx_kv_retain_per_layer", "fx_shared_prefix_decode",
     "fx_device_errors", "fx_focal_workspace_bytes", "fx_sparse_workspace_bytes", "fx_shared_prefix_workspace_bytes",
     "FX_DEVERR_LEN", "FX_DEVERR_INDEX", "FX_DEVERR_OFFSETS", "FX_DEVERR_CAPACITY", "FX_DEVERR_TIMEOUT",
@@ -29,6 +30,7 @@ __all__ = [
 FX_OK, FX_ERR_INVALID_ARG, FX_ERR_UNSUPPORTED, FX_ERR_WORKSPACE, FX_ERR_CUDA, FX_ERR_DEVICE = range(6)
 FX_DEVERR_LEN, FX_DEVERR_INDEX, FX_DEVERR_OFFSETS, FX_DEVERR_CAPACITY, FX_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 FX_LAUNCH_PDL, FX_LAUNCH_INPUTS_READY = 1, 2
+FX_CSFR_FOCAL, FX_CSFR_CURRENT, FX_CSFR_PREVIOUS, FX_CSFR_DENSE = range(4)
 _STATUS = {0: "FX_OK", 1: "FX_ERR_INVALID_ARG", 2: "FX_ERR_UNSUPPORTED", 3: "FX_ERR_WORKSPACE",
            4: "FX_ERR_CUDA", 5: "FX_ERR_DEVICE"}
 
@@ -96,6 +98,8 @@ def load_library():
         lib.fx_focal_mass.argtypes = [c_vp, c_int, c_int, c_int, c_int, c_vp, c_uint, c_vp]
         lib.fx_choose_focal_layers.argtypes = [ctypes.POINTER(ctypes.c_float), c_int, c_int,
                                                ctypes.POINTER(ctypes.c_int32)]
+        lib.fx_csfr_schedule.argtypes = [c_int, ctypes.POINTER(ctypes.c_int32), c_int, c_int,
+                                         ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         lib.fx_sparse_workspace_bytes.argtypes = [c_int] * 6
         lib.fx_sparse_workspace_bytes.restype = c_size
         lib.fx_sparse_gqa_decode.argtypes = [ctypes.POINTER(KVDesc), c_vp, c_int, c_vp, c_int, c_int, c_float,
@@ -123,7 +127,7 @@ def load_library():
         lib.fx_shared_prefix_decode.argtypes = [ctypes.POINTER(PrefixDesc), ctypes.POINTER(BranchDesc), c_vp, c_int,
                                                 c_vp, c_int, c_float, c_vp, c_vp, c_size, c_uint, c_vp]
         for name in ("fx_device_errors", "fx_workspace_init", "fx_focal_attn_scores", "fx_topk_select",
-                     "fx_focal_mass", "fx_choose_focal_layers",
+                     "fx_focal_mass", "fx_choose_focal_layers", "fx_csfr_schedule",
                      "fx_sparse_gqa_decode", "fx_kv_compact", "fx_kv_append", "fx_kv_retain_per_layer",
                      "fx_shared_prefix_decode"):
             getattr(lib, name).restype = c_int
@@ -291,6 +295,19 @@ def fx_topk_select(scores, k: int, *, prev=None, out=None, stream=None, flags: i
             raise FxError(FX_ERR_INVALID_ARG, "prev must be a contiguous [rows, k] int32 tensor")
     _check(lib.fx_topk_select(_ptr(scores), rows, n, int(k), _ptr(prev), _ptr(out), int(flags), _stream(stream)))
     return out
+
+
+def fx_csfr_schedule(n_layers: int, focal_layers, first_step: bool):
+    """Per layer of one decode step: (kind, src) -- FX_CSFR_FOCAL (src = the layer), FX_CSFR_CURRENT /
+    FX_CSFR_PREVIOUS (attend over this / the previous step's set of focal layer src) or FX_CSFR_DENSE
+    (src = -1).  Host only."""
+    lib = load_library()
+    f = [int(x) for x in focal_layers]
+    kind = (ctypes.c_int32 * n_layers)()
+    src = (ctypes.c_int32 * n_layers)()
+    _check(lib.fx_csfr_schedule(int(n_layers), (ctypes.c_int32 * len(f))(*f), len(f), 1 if first_step else 0,
+                                kind, src))
+    return list(kind), list(src)
 
 
 def fx_sparse_gqa_decode(k, v, length, q, idx, tail_lo: int, *, scale=None, out=None, ws=None, stream=None,

@@ -284,6 +284,7 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
                                float scale, int cand_lo, int cand_hi, float* out, float* scores,
                                void* ws, size_t ws_bytes, unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_focal_attn_scores");
     fx_status st = check_kv(kv, "kv");
     if (st != FX_OK) return st;
     if ((st = check_flags(flags)) != FX_OK) return st;
@@ -369,6 +370,7 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
 fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int32_t* prev_idx,
                          int32_t* idx_out, unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_topk_select");
     if (!scores || !idx_out) return fail(FX_ERR_INVALID_ARG, "scores and idx_out must be non-NULL");
     if (rows < 1) return fail(FX_ERR_INVALID_ARG, "rows must be >= 1");
     if (k < 1 || k > n) return fail(FX_ERR_INVALID_ARG, "need 1 <= k (%d) <= n (%d)", k, n);
@@ -394,6 +396,7 @@ fx_status fx_topk_select(const float* scores, int rows, int n, int k, const int3
 fx_status fx_focal_mass(const float* scores, int rows, int n, int R, int accumulate, float* mass, unsigned flags,
                         void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_focal_mass");
     if (!scores || !mass) return fail(FX_ERR_INVALID_ARG, "scores and mass must be non-NULL");
     if (rows < 1 || n < 1 || R < 1) return fail(FX_ERR_INVALID_ARG, "need rows, n, R >= 1");
     fx_status st = check_flags(flags);
@@ -403,6 +406,38 @@ fx_status fx_focal_mass(const float* scores, int rows, int n, int R, int accumul
     cudaError_t e = launch_focal_mass(scores, rows, n, 1.0f / (float)R, accumulate ? 1 : 0, mass,
                                       (flags & FX_LAUNCH_PDL) != 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "focal mass launch");
+    return FX_OK;
+}
+
+fx_status fx_csfr_schedule(int n_layers, const int32_t* focal_layers, int C, int first_step, int32_t* kind,
+                           int32_t* src)
+{
+    if (!focal_layers || !kind || !src) return fail(FX_ERR_INVALID_ARG, "focal_layers, kind and src must be non-NULL");
+    if (n_layers < 1 || C < 1 || C > n_layers) return fail(FX_ERR_INVALID_ARG, "need 1 <= C <= n_layers");
+    for (int i = 0; i < C; ++i) {
+        if (focal_layers[i] < 0 || focal_layers[i] >= n_layers)
+            return fail(FX_ERR_INVALID_ARG, "focal layer %d out of range", focal_layers[i]);
+        if (i > 0 && focal_layers[i] <= focal_layers[i - 1])
+            return fail(FX_ERR_INVALID_ARG, "focal layers must be strictly ascending");
+    }
+    const int first = focal_layers[0];
+    const int deepest = focal_layers[C - 1];
+    int f = 0;   // focal layers at or before the current layer
+    for (int l = 0; l < n_layers; ++l) {
+        if (f < C && focal_layers[f] == l) {
+            kind[l] = FX_CSFR_FOCAL;
+            src[l] = l;
+            ++f;
+        } else if (l < first) {
+            // before the first focal layer of this step: the deepest focal layer's set of the previous
+            // step, or the whole cache when there is none yet
+            kind[l] = first_step ? FX_CSFR_DENSE : FX_CSFR_PREVIOUS;
+            src[l] = first_step ? -1 : deepest;
+        } else {
+            kind[l] = FX_CSFR_CURRENT;   // the nearest focal layer above, this step
+            src[l] = focal_layers[f - 1];
+        }
+    }
     return FX_OK;
 }
 
@@ -436,6 +471,7 @@ fx_status fx_sparse_gqa_decode(const fx_kv_desc* kv, const fx_bf16* q, int Hq, c
                                int k, int tail_lo, float scale, float* out, void* ws,
                                size_t ws_bytes, unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_sparse_gqa_decode");
     fx_status st = check_kv(kv, "kv");
     if (st != FX_OK) return st;
     if ((st = check_flags(flags)) != FX_OK) return st;
@@ -541,6 +577,7 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
                         int64_t idx_stride_layer, int k, int tail_lo, const fx_kv_out_desc* dst,
                         int64_t dst_stride_layer, int n_layers, unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_kv_compact");
     fx_status st = check_kv(src, "src");
     if (st != FX_OK) return st;
     if ((st = check_flags(flags)) != FX_OK) return st;
@@ -595,6 +632,7 @@ fx_status fx_kv_compact(const fx_kv_desc* src, int64_t src_stride_layer, const i
 fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer, int n_layers, const fx_bf16* k_new,
                        const fx_bf16* v_new, const int32_t* pos, unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_kv_append");
     fx_status st;
     if (!cache) return fail(FX_ERR_INVALID_ARG, "cache is NULL");
     if (!pos) return fail(FX_ERR_INVALID_ARG, "pos is NULL");
@@ -607,7 +645,8 @@ fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer, int n_
     if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
         return fail(FX_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     if (!row_stride_ok(stride_layer)) return fail(FX_ERR_INVALID_ARG, "stride_layer must be a non-negative multiple of 8 elements");
-    if ((int64_t)n_layers * cache->B * cache->Hkv > (int64_t)65535 * 8 * 65535)
+    // the append kernel copies 8 rows per CTA and its grid.x stays below 2^31
+    if ((int64_t)n_layers * cache->B * cache->Hkv > (int64_t)0x7fffffff * 8)
         return fail(FX_ERR_UNSUPPORTED, "too many rows");
     DeviceState* ds = nullptr;
     if ((st = device_state(&ds)) != FX_OK) return st;
@@ -644,6 +683,7 @@ fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer,
                                  int32_t* idx_out, const fx_kv_out_desc* dst, int64_t dst_stride_layer, void* ws,
                                  size_t ws_bytes, unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_kv_retain_per_layer");
     fx_status st = check_kv(kv, "kv");
     if (st != FX_OK) return st;
     if ((st = check_flags(flags)) != FX_OK) return st;
@@ -702,6 +742,7 @@ fx_status fx_shared_prefix_decode(const fx_prefix_desc* prefix, const fx_branch_
                                   float scale, float* out, void* ws, size_t ws_bytes, unsigned flags,
                                   void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_shared_prefix_decode");
     if (!prefix || !br) return fail(FX_ERR_INVALID_ARG, "prefix and branches must be non-NULL");
     if (check_flags(flags) != FX_OK) return FX_ERR_INVALID_ARG;
     if (prefix->d != kHeadDim) return fail(FX_ERR_UNSUPPORTED, "head dim %d (only 128 is implemented)", prefix->d);

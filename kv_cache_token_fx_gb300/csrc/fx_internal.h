@@ -7,6 +7,8 @@
 
 #include <utility>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "fx.h"
 
 namespace fx {
@@ -181,6 +183,15 @@ struct AppendParams {
     const uint16_t* v_new;
     const int32_t* pos;      // [B]
     unsigned* err;
+};
+
+// An NVTX range over one library call, so that profiler timelines show each fx_* call by name (header-only
+// NVTX v3: without a tool attached a push/pop costs a few nanoseconds).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
 // Sets the calling thread's error message (read back by fx_last_error) and returns `st`.

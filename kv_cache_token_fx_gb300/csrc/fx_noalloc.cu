@@ -57,6 +57,7 @@ fx_status fx_focal_attn_scores_noalloc(const fx_kv_desc* kv, const fx_bf16* q, i
                                        float scale, int cand_lo, int cand_hi, float* out, float* scores,
                                        unsigned flags, void* stream)
 {
+    fx::NvtxRange nvtx_range("fx_focal_attn_scores_noalloc");
     if (!kv) return fx::set_error(FX_ERR_INVALID_ARG, "kv is NULL");
     const size_t need = fx_focal_workspace_bytes(kv->B, kv->Hkv, Hq, Mq, kv->Tcap);
     if (need > kStaticScratchBytes)

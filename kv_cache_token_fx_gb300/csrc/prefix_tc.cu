@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefix_tc_kernel(const PrefixTc
     const int r = live ? row - b * p.R : 0;
 
     griddep_wait();   // the queries may come from the kernel just before
+    // The verify kernel launched right after this one reads its lengths, offsets and K/V rows before its
+    // own dependency wait (fx_shared_prefix_decode launches it that way whatever the caller's flags).
+    // That is sound only because this trigger comes after this kernel's wait above: when the verify
+    // kernel starts, everything enqueued before this kernel has finished.  Do not move it earlier.
     griddep_launch();
 
     // visible prefix rows of this row's branch (its fork position)

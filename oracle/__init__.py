@@ -162,6 +162,24 @@ def choose_focal_layers(ratio, C: int) -> list:
     return sorted(order[:C])
 
 
+def csfr_schedule(n_layers: int, focal_layers, first_step: bool) -> list:
+    """FastOCR, Focal-Guided Pruning and Cross-Step Fixation Reuse: where each layer of one decode step
+    takes its attention set from.  A focal layer makes its own ("focal", l).  A layer below a focal layer
+    attends to this step's set of the nearest focal layer above it ("current", f).  A layer above the
+    first focal layer reuses the set the deepest focal layer chose at the previous step ("previous",
+    f_last); at the first step there is none and it attends to the whole cache ("dense", -1)."""
+    focal = sorted(int(f) for f in focal_layers)
+    out = []
+    for l in range(n_layers):
+        if l in focal:
+            out.append(("focal", l))
+        elif l < focal[0]:
+            out.append(("dense", -1) if first_step else ("previous", focal[-1]))
+        else:
+            out.append(("current", max(f for f in focal if f < l)))
+    return out
+
+
 def topk(scores, k: int, *, lib=None) -> np.ndarray:
     """scores [..., n] (any float type, compared in double) -> int32 [..., k]: the k best by
     (score descending, index ascending), written in ascending index order."""

@@ -91,6 +91,21 @@ def test_host_argument_checks_without_gpu(lib):
             assert lib.fx_choose_focal_layers((ctypes.c_float * n)(*ratio), n, C, out) == 0
             assert list(out) == oracle.choose_focal_layers(ratio.tolist(), C)
     assert lib.fx_choose_focal_layers((ctypes.c_float * 2)(0.1, 0.2), 2, 3, (ctypes.c_int32 * 3)()) == 1
+    # the cross-step reuse schedule is host code too: every small configuration against the oracle's rule
+    import itertools
+    lib.fx_csfr_schedule.restype = ctypes.c_int
+    names = {0: "focal", 1: "current", 2: "previous", 3: "dense"}
+    for n in range(1, 7):
+        for C in range(1, n + 1):
+            for focal in itertools.combinations(range(n), C):
+                for first in (0, 1):
+                    kind, src = (ctypes.c_int32 * n)(), (ctypes.c_int32 * n)()
+                    assert lib.fx_csfr_schedule(n, (ctypes.c_int32 * C)(*focal), C, first, kind, src) == 0
+                    got = [(names[k], s_) for k, s_ in zip(kind, src)]
+                    assert got == oracle.csfr_schedule(n, focal, bool(first)), (n, focal, first)
+    bad = (ctypes.c_int32 * 2)(5, 3)
+    assert lib.fx_csfr_schedule(8, bad, 2, 0, (ctypes.c_int32 * 8)(), (ctypes.c_int32 * 8)()) == 1
+    assert b"ascending" in lib.fx_last_error()
     # shared-prefix workspace: a dense prefix of a full 128 x 128 tile or more (and at least 128 query
     # rows per KV head) also needs room for the tensor-core prefix partials (O, m, l per row)
     lib.fx_shared_prefix_workspace_bytes.restype = ctypes.c_size_t

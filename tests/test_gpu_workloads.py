@@ -109,17 +109,16 @@ def test_ocr_decode_full_run_sampled():
                     stats["gapped"] += gp
                     stats["exact"] += ex
                     continue
-                if l < 3:
-                    if t == 0:
-                        ref = oracle.sparse_decode(_as_kv(kr), _as_kv(vr), ln, q, None, 0)
-                        pu.assert_out_close(g_out, ref[0], vmax, f"t{t} l{l} dense")
-                        stats["sparse_checked"] += 1
-                        continue
-                    src_layer, src_t, gpu_set = 14, t - 1, gpu[t]["prev14"][b, h]
-                elif l < 14:
-                    src_layer, src_t, gpu_set = 3, t, gpu[t]["sets"][3][b, h]
+                kind, src = oracle.csfr_schedule(w.n_layers, w.focal_layers, first_step=(t == 0))[l]
+                if kind == "dense":
+                    ref = oracle.sparse_decode(_as_kv(kr), _as_kv(vr), ln, q, None, 0)
+                    pu.assert_out_close(g_out, ref[0], vmax, f"t{t} l{l} dense")
+                    stats["sparse_checked"] += 1
+                    continue
+                if kind == "previous":
+                    src_layer, src_t, gpu_set = src, t - 1, gpu[t]["prev14"][b, h]
                 else:
-                    src_layer, src_t, gpu_set = 14, t, gpu[t]["sets"][14][b, h]
+                    src_layer, src_t, gpu_set = src, t, gpu[t]["sets"][src][b, h]
                 ref_set, ref_sc = own[(src_layer, src_t)][0], own[(src_layer, src_t)][1]
                 use = _validated_set(gpu_set, ref_set, ref_sc, w.k_keep, stats)
                 ref = oracle.sparse_decode(_as_kv(kr), _as_kv(vr), ln, q, torch.from_numpy(use).view(1, 1, -1),

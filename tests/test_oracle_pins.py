@@ -458,3 +458,24 @@ def test_mutations_are_caught(name, mutant_dir, oracle_mod):
     failed = line[-1][len("FAILED:"):].split(",") if line else []
     failed = [f for f in failed if f]
     assert caught_by_crash or failed, f"no pin catches the planted mistake {name}"
+
+
+# ----------------------------------------------------------------------------------------------
+# Cross-step fixation reuse: the layer schedule of a decode step, pinned by the FastOCR configuration
+# written out by hand (28 layers, focal layers 3 and 14) and by small cases.
+def test_csfr_schedule_fastocr_configuration():
+    later = [("previous", 14)] * 3 + [("focal", 3)] + [("current", 3)] * 10 + [("focal", 14)] + [("current", 14)] * 13
+    first = [("dense", -1)] * 3 + later[3:]
+    assert oracle.csfr_schedule(28, (3, 14), first_step=False) == later
+    assert oracle.csfr_schedule(28, (14, 3), first_step=True) == first
+
+
+def test_csfr_schedule_small_cases():
+    # a focal first layer: nothing reuses an older set
+    assert oracle.csfr_schedule(4, (0,), first_step=False) == [("focal", 0), ("current", 0), ("current", 0),
+                                                                ("current", 0)]
+    # every layer focal
+    assert oracle.csfr_schedule(3, (0, 1, 2), first_step=False) == [("focal", 0), ("focal", 1), ("focal", 2)]
+    # the deepest focal layer is the last one: layers before the first reuse it
+    assert oracle.csfr_schedule(5, (2, 4), first_step=False) == [("previous", 4), ("previous", 4), ("focal", 2),
+                                                                 ("current", 2), ("focal", 4)]

@@ -30,23 +30,23 @@ def ocr_decode_run(w: OcrDecode, steps_to_keep, n_steps=None, device="cuda"):
     out = torch.empty((L, B, Hq, 1, D), dtype=torch.float32, device=device)
     ws = fx.Workspace(torch.device(device))
     kept = {}
-    f_first, f_last = w.focal_layers[0], w.focal_layers[-1]
+    f_last = w.focal_layers[-1]
     for t in range(n_steps):
         p = t % 2
         ln = torch.full((B,), w.length_at(t), dtype=torch.int32, device=device)
+        # FastOCR's cross-step fixation reuse, as the library schedules it
+        kinds, srcs = fx.fx_csfr_schedule(L, w.focal_layers, first_step=(t == 0))
         for l in range(L):
             q = w.query(t, l, device=device, table=tables[l])
-            if l in w.focal_layers:
+            if kinds[l] == fx.FX_CSFR_FOCAL:
                 fx.fx_focal_attn_scores(K[l], V[l], ln, q, cand=(0, w.n_vis), out=out[l], scores=scores[l], ws=ws)
                 prev = sets[l][1 - p] if t > 0 else None
                 fx.fx_topk_select(scores[l], w.k_keep, prev=prev, out=sets[l][p])
                 continue
-            if l < f_first:
-                sel = sets[f_last][1 - p] if t > 0 else None
-            elif l < f_last:
-                sel = sets[f_first][p]
+            if kinds[l] == fx.FX_CSFR_DENSE:
+                sel = None
             else:
-                sel = sets[f_last][p]
+                sel = sets[srcs[l]][p if kinds[l] == fx.FX_CSFR_CURRENT else 1 - p]
             fx.fx_sparse_gqa_decode(K[l], V[l], ln, q, sel, w.n_vis if sel is not None else 0, out=out[l], ws=ws)
         if t in steps_to_keep:
             torch.cuda.synchronize()
