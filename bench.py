@@ -154,20 +154,20 @@ def _cudart():
 
 
 def profiled_traffic_ratio():
-    """DRAM bytes per algorithmic byte of the dominant kernel from its committed ncu summary, or None
-    when that summary was taken on a different revision of the kernel source."""
+    """DRAM bytes per algorithmic byte of the dominant kernel from its committed ncu figures
+    (profiles/sparse_gqa_decode_ocr_decode.json, written from the capture's raw counters), or None when
+    that capture was taken on a different revision of the kernel source."""
     import hashlib
-    import re
     try:
-        prof = open(os.path.join(ROOT, "profiles", "sparse_gqa_decode_ocr_decode.md")).read()
-        src = os.path.join(ROOT, "kv_cache_token_fx_gb300", "csrc", "attn_splitkv.cu")
+        with open(os.path.join(ROOT, "profiles", "sparse_gqa_decode_ocr_decode.json")) as f:
+            prof = json.load(f)
+        src = os.path.join(ROOT, prof["kernel_source"])
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    except OSError:
+    except (OSError, KeyError, ValueError):
         return None
-    f = dict(re.findall(r"^\s+(\w+): (\S+)$", prof, flags=re.M))
-    if f.get("kernel_source_sha256") != sha:
+    if prof.get("kernel_source_sha256") != sha:
         return None
-    return float(f["profiled_launch_dram_bytes"]) / float(f["profiled_launch_algorithmic_bytes"])
+    return float(prof["profiled_launch_dram_bytes"]) / float(prof["profiled_launch_algorithmic_bytes"])
 
 
 def measured_hbm_peak():
@@ -403,7 +403,8 @@ def run_fx(args, rank, local, ws):
         traffic = int(ratio * kern_bytes / n_launch) if ratio is not None else None
         roofline = {"kernel": "fx_sparse_gqa_decode", "bound": "hbm", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                    "traffic_note": "ncu dram bytes of a captured last-step launch, scaled by algorithmic bytes",
+                    "traffic_note": "ncu dram bytes (read + write) of a captured last-step launch, scaled by "
+                                    "algorithmic bytes (profiles/sparse_gqa_decode_ocr_decode.json)",
                     "peak_source": peak_kind, "avg_launch_us": round(kern_ms * 1e3 / n_launch, 3),
                     "avg_bytes_per_launch": int(kern_bytes / n_launch), "launches_timed": n_launch,
                     "timing": "CUDA events around graphs of the 26 sparse launches per step"}
