@@ -270,8 +270,8 @@ __global__ void __launch_bounds__(32 * (C + NP), 2)
         // the entries of this warp's first sub-tile are loaded now, later ones a sub-tile ahead
         const int n_loc = n_local();
         auto key_row = [&](int L, int r) { return L < n_loc ? copy_token(L, r) : -1; };
-        int ta = key_row(warp, g);
-        int tb = key_row(warp, g + 8);
+        int tok_a = key_row(warp, g);
+        int tok_b = key_row(warp, g + 8);
         // the query rows of this (b, h) as one bf16 8-row tile (rows past R are zero)
         for (int e = tid; e < kRows * (kHeadDim / 8); e += 32 * C) {
             const int rr = e >> 4;
@@ -302,14 +302,14 @@ __global__ void __launch_bounds__(32 * (C + NP), 2)
         const int vcol = 8 * ((lane >> 3) & 1);
         for (int j = warp; j < n_loc; j += C) {
             const int s = j % S;
-            const bool va = (unsigned)ta < (unsigned)len;
-            const bool vb = (unsigned)tb < (unsigned)len;
+            const bool va = (unsigned)tok_a < (unsigned)len;
+            const bool vb = (unsigned)tok_b < (unsigned)len;
             if (t4 == 0 && j < nG) {   // a listed index outside [0, len) is skipped and reported
                 const int pos = ga + j * kSub + g;
                 if ((pos < gb && !va) || (pos + 8 < gb && !vb)) flag(p.err, FX_DEVERR_INDEX);
             }
-            ta = key_row(j + C, g);                      // the next sub-tile's, one iteration ahead
-            tb = key_row(j + C, g + 8);
+            tok_a = key_row(j + C, g);                   // the next sub-tile's, one iteration ahead
+            tok_b = key_row(j + C, g + 8);
             mbar_wait_bounded(&full_bar[s], (j / S) & 1, p.err, spin_limit);
             const unsigned char* sk = ring + (size_t)s * kSubBytes;
             const unsigned char* sv = sk + 2 * kHalfTile;
