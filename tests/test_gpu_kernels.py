@@ -630,3 +630,24 @@ def test_bounded_wait_runs_out_and_is_reported(fx):
     torch.cuda.synchronize()
     assert fx.fx_device_errors() == 0
     assert torch.equal(out, again)
+
+
+def test_sparse_without_tensor_maps_matches_oracle(fx):
+    """A cache view whose batch stride is 0 (every sequence reads the same rows) cannot be described by a
+    TMA tensor map; the decode kernel then copies the contiguous tail rows with cp.async as well.  Same
+    results as the oracle over the broadcast cache."""
+    B, Hkv, G, T, kk = 4, 2, 2, 900, 61
+    k1, v1 = kv_case(1, Hkv, T, 131)
+    kb = dev(k1).expand(B, Hkv, T, D)
+    vb = dev(v1).expand(B, Hkv, T, D)
+    assert kb.stride(0) == 0
+    q = rnd((B, Hkv * G, 1, D), 131, 3)
+    length = torch.tensor([T, 800, 517, 300], dtype=torch.int32)
+    idx = _sorted_subsets(B, Hkv, 300, kk, 5)
+    out = fx.fx_sparse_gqa_decode(kb, vb, dev(length), dev(q), dev(idx), 300)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    ref = oracle.sparse_decode(k1.expand(B, Hkv, T, D).contiguous(), v1.expand(B, Hkv, T, D).contiguous(), length, q,
+                               idx, 300)
+    pu.assert_out_close(out, ref, float(v1.float().abs().max()))
+
