@@ -123,6 +123,29 @@ Plan make_plan(int pairs, int R, int max_keys, int sm_count, bool merge_in_clust
     return pl;
 }
 
+// Tensor-core scoring plan (scores-only calls with more than 8 rows): key ranges of as many whole
+// 128-key tiles as one of a CTA's four tensor-memory buffers holds, spread evenly; one persistent CTA
+// per SM (or per range, when there are fewer), and at most two ranges per SM per (b, h), so that the
+// ranges of one (b, h) can always be in flight together.
+struct ScoreTcPlan {
+    int nsplit, split_len, grid;
+};
+
+bool make_score_tc_plan(int pairs, int R, int Tcap, int sm_count, ScoreTcPlan* sp)
+{
+    const int N = score_tc_cols(R);
+    if (R > kMaxRows || Tcap < 1 || sm_count < 1) return false;
+    const int cap = score_item_tiles(N) * kScoreKeys;
+    const int ns = cdiv(Tcap, cap);
+    if (ns > 2 * sm_count) return false;
+    sp->split_len = cdiv(cdiv(Tcap, ns), kScoreKeys) * kScoreKeys;
+    sp->nsplit = cdiv(Tcap, sp->split_len);
+    const int64_t items = (int64_t)pairs * sp->nsplit;
+    if (items > 0x7fffffff) return false;
+    sp->grid = (int)std::min<int64_t>(items, sm_count);
+    return true;
+}
+
 // Streaming decode plan: about 1.5 CTAs per SM per call (the splits of each (b, h) merged in a
 // cluster) and as many ring slots as fit kStreamSmemMax, so that two CTAs share an SM and most of the
 // next call's CTAs are resident, filling their rings, while this call finishes.  Measured on the
@@ -301,6 +324,52 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     const int pairs = kv->B * kv->Hkv;
     const int G = Hq / kv->Hkv;
     const int R = G * Mq;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
+
+    // Scores only, more than 8 rows: the tensor-core kernel that keeps the logits on chip (its R fp32
+    // logits per key would otherwise be written and read back), when K admits a tensor map.
+    ScoreTcPlan sp;
+    CUtensorMap tk, tq;
+    int bcast = 0;
+    if (out == nullptr && R > kStreamRows && 4 + pairs + 2 * (int64_t)pairs * R <= (int64_t)kCounterSlots &&
+        make_score_tc_plan(pairs, R, kv->Tcap, ds->sm_count, &sp) &&
+        encode_score_maps(kv, q, Hq, Mq, score_tc_cols(R), &tk, &tq, &bcast)) {
+        const size_t np = (size_t)pairs * sp.nsplit * R;
+        const size_t off_m = kCounterBytes;
+        const size_t off_l = off_m + round_up(np * sizeof(float));
+        if ((st = check_ws(ws, ws_bytes, off_l + round_up(np * sizeof(float)))) != FX_OK) return st;
+        char* w = static_cast<char*>(ws);
+        ScoreParams c;
+        memset(&c, 0, sizeof c);
+        c.len = kv->len;
+        c.B = kv->B;
+        c.Hkv = kv->Hkv;
+        c.Tcap = kv->Tcap;
+        c.k_bcast = bcast;
+        c.q = q;
+        c.Hq = Hq;
+        c.G = G;
+        c.Mq = Mq;
+        c.R = R;
+        c.q_pos0 = q_pos0;
+        c.qscale = log2e_scale(scale);
+        c.pairs = pairs;
+        c.nsplit = sp.nsplit;
+        c.split_len = sp.split_len;
+        c.cand_lo = cand_lo;
+        c.cand_hi = cand_hi;
+        c.part_m = reinterpret_cast<float*>(w + off_m);
+        c.part_l = reinterpret_cast<float*>(w + off_l);
+        c.counters = reinterpret_cast<unsigned*>(w);
+        c.scores = scores;
+        c.err = ds->err;
+        c.spin_limit = kSpinLimit;
+        cudaError_t e = launch_score_tc(c, &tk, &tq, sp.grid, pdl, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core scoring launch");
+        return FX_OK;
+    }
+
     const Plan pl = make_plan(pairs, R, kv->Tcap, ds->sm_count, false, false, out == nullptr);
     const Layout L = make_layout(pairs, R, pl, kv->Tcap, false);
     if ((st = check_ws(ws, ws_bytes, L.total)) != FX_OK) return st;
@@ -336,8 +405,6 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
     p.logits = scores ? reinterpret_cast<float*>(w + L.logits) : nullptr;
     p.no_v = out == nullptr ? 1 : 0;
     p.err = ds->err;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool pdl = (flags & FX_LAUNCH_PDL) != 0;
     p.prefetch = (pdl && (flags & FX_LAUNCH_INPUTS_READY)) ? 1 : 0;
     cudaError_t e = launch_attn_partial(p, kModeFocal, pdl, s);
     if (e != cudaSuccess) return cuda_fail(e, "focal attention launch");
@@ -896,5 +963,38 @@ bool fx::encode_kv_tensor_maps(const fx_kv_desc* kv, CUtensorMap* tk, CUtensorMa
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
+    return true;
+}
+
+bool fx::encode_score_maps(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int n_cols, CUtensorMap* tk,
+                           CUtensorMap* tq, int* bcast)
+{
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (fn == nullptr || kv->Tcap < 1) return false;
+    // a cache shared by every sequence (batch stride 0) is one batch entry of the map
+    const bool bc = kv->stride_b == 0;
+    const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kv->Tcap, (cuuint64_t)kv->Hkv,
+                                (cuuint64_t)(bc ? 1 : kv->B)};
+    const cuuint64_t strides[3] = {(cuuint64_t)kv->stride_t * 2, (cuuint64_t)kv->stride_h * 2,
+                                   bc ? (cuuint64_t)kv->stride_h * 2 * (cuuint64_t)kv->Hkv : (cuuint64_t)kv->stride_b * 2};
+    for (int i = 0; i < 3; ++i)
+        if (strides[i] == 0 || (strides[i] & 15u) != 0 || strides[i] >= (1ull << 40)) return false;
+    const cuuint32_t box[4] = {64, (cuuint32_t)kScoreKeys, 1, 1};
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    if (fn(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(static_cast<const void*>(kv->k)), dims, strides,
+           box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    // q as [B Hq Mq] rows of 128 bf16 (contiguous); the kernel addresses row starts up to 2^31
+    const int64_t qrows = (int64_t)kv->B * Hq * Mq;
+    if (qrows >= 0x7fffffff) return false;
+    const cuuint64_t qdims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)qrows};
+    const cuuint64_t qstrides[1] = {(cuuint64_t)kRowBytes};
+    const cuuint32_t qbox[2] = {64, (cuuint32_t)n_cols};
+    if (fn(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(static_cast<const void*>(q)), qdims, qstrides, qbox,
+           elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    *bcast = bc ? 1 : 0;
     return true;
 }

@@ -119,6 +119,36 @@ struct AttnParams {
     int tail_tma;         // streaming decode: contiguous tail rows come by TMA through the tensor maps
 };
 
+// Scores-only focal calls on the tensor cores (score_tc.cu): one persistent CTA per SM takes key ranges
+// ("items") of score_item_tiles(N) tiles of kScoreKeys keys (N = score_tc_cols(rows), at most 64) and
+// keeps kScoreBufs of them in flight, each range's logits in its own part of the tensor memory.
+constexpr int kScoreKeys = 128;
+constexpr int kScoreTmemCols = 512;   // the whole tensor memory of the SM
+constexpr int kScoreBufs = 3;         // ranges in flight per CTA
+constexpr int kScoreStages = 4;       // 32 KB K tiles in flight per CTA
+__host__ __device__ constexpr int score_item_tiles(int n_cols) { return (kScoreTmemCols / kScoreBufs) / n_cols; }
+// The N of a call with R rows: 16, 32 or 64 (each of the kernel's two row halves a power of two).
+__host__ __device__ constexpr int score_tc_cols(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
+
+struct ScoreParams {
+    const int32_t* len;
+    int B, Hkv, Tcap;
+    int k_bcast;              // the cache has batch stride 0: the tensor map's batch extent is 1
+    const uint16_t* q;        // [B, Hq, Mq, 128]
+    int Hq, G, Mq, R;
+    int q_pos0;
+    float qscale;             // scale * log2(e)
+    int pairs, nsplit, split_len;
+    int cand_lo, cand_hi;
+    float* part_m;            // [pairs][nsplit][R] row maximum of each key range
+    float* part_l;            // [pairs][nsplit][R] row sum of each key range
+    unsigned* counters;       // ticket, exit count, arrivals [pairs], then 8-byte words [pairs][R] of the merged
+                              // c_r with a valid bit (all zero between calls)
+    float* scores;            // [pairs][cand_hi - cand_lo]
+    unsigned* err;
+    unsigned spin_limit;
+};
+
 struct FocalCombineParams {
     const float* part_m;
     const float* part_l;
@@ -209,6 +239,15 @@ cudaError_t launch_stream_decode(const AttnParams& p, const CUtensorMap* tk, con
 bool encode_kv_tensor_maps(const fx_kv_desc* kv, CUtensorMap* tk, CUtensorMap* tv);
 size_t stream_decode_smem_bytes(int slots, int nsplit, int R);
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
+// tk: 4-D tensor map of K ([B or 1][Hkv][Tcap][128] bf16, boxes of kScoreKeys rows x 64 columns); tq: 2-D
+// tensor map of q ([B Hq Mq][128] bf16, boxes of N rows x 64 columns); both with the 128-byte swizzle.
+cudaError_t launch_score_tc(const ScoreParams& p, const CUtensorMap* tk, const CUtensorMap* tq, int grid, bool pdl,
+                            cudaStream_t s);
+size_t score_tc_smem_bytes(int n_cols);
+// Encodes the tensor maps for launch_score_tc (*bcast is set when the batch stride is 0); false when the
+// strides or sizes allow no tensor map.
+bool encode_score_maps(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int n_cols, CUtensorMap* tk,
+                       CUtensorMap* tq, int* bcast);
 cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_prefix_tc(const PrefixTcParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_mass(const float* scores, int rows, int n, float inv_r, int accumulate, float* mass,

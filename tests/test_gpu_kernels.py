@@ -107,6 +107,54 @@ def test_focal_scores_only_matches_oracle(fx, G, Mq, q_pos0):
     pu.assert_scores_close(sc, ref_sc)
 
 
+@pytest.mark.parametrize("G,Mq,T,lens,q_off,cand,scale", [
+    (4, 8, 5000, [5000, 3001, 0, 129], 8, (0, 4992), None),      # 32 rows: 5 ranges of 1024 keys, causal window
+    (8, 8, 4000, [4000, 3999, 513, 1], None, (17, 3333), 1.0),   # 64 rows: 8 ranges of 512, sharp softmax
+    (2, 8, 4500, [4500, 2049, 2047, 4500], 8, (0, 4492), None),  # 16 rows: 3 ranges of 2048 (a boundary at 2048)
+    (3, 16, 3000, [3000, 1280, 641, 640], None, (0, 3000), 0.5),  # 48 rows: 5 ranges of 640
+    (1, 9, 2100, [2100, 7, 2048, 2049], 3, (100, 2090), None),   # 9 rows in a 16-column tile, window past len
+])
+def test_scores_only_on_tensor_cores_matches_oracle(fx, G, Mq, T, lens, q_off, cand, scale):
+    """Scores-only calls with more than 8 rows per KV head keep their logits in tensor memory and merge
+    the per-range row maxima and sums across CTAs: several ranges per (sequence, KV head), ragged and
+    empty sequences, a causal window, a candidate range.  Equal to the oracle, and to the split-KV path
+    (taken when output rows are wanted, which writes its logits out) on the same inputs."""
+    B, Hkv = len(lens), 2
+    k, v = kv_case(B, Hkv, T, 300 + G * Mq)
+    q = rnd((B, Hkv * G, Mq, D), 301 + G * Mq, 3)
+    length = torch.tensor(lens, dtype=torch.int32)
+    q_pos0 = -1 if q_off is None else T - q_off
+    _, ref_sc = oracle.focal(k, v, length, q, q_pos0=q_pos0, cand=cand, want_out=False, scale=scale)
+    dk, dv, dl, dq = dev(k), dev(v), dev(length), dev(q)
+    _, sc = fx.fx_focal_attn_scores(dk, dv, dl, dq, q_pos0=q_pos0, cand=cand, want_out=False, scale=scale)
+    _, sc_split = fx.fx_focal_attn_scores(dk, dv, dl, dq, q_pos0=q_pos0, cand=cand, scale=scale)
+    # back to back on the same workspace, as a programmatic dependent launch: the counters were reset
+    _, sc2 = fx.fx_focal_attn_scores(dk, dv, dl, dq, q_pos0=q_pos0, cand=cand, want_out=False, scale=scale,
+                                     flags=fx.FX_LAUNCH_PDL)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    pu.assert_scores_close(sc, ref_sc)
+    pu.assert_scores_close(sc, sc_split, "tensor-core vs split-KV scores")
+    assert torch.equal(sc, sc2)
+    assert torch.all(sc[lens.index(min(lens))][:, max(0, min(lens) - cand[0]):] == 0)
+
+
+def test_scores_only_on_tensor_cores_shared_cache(fx):
+    """A cache shared by every sequence (batch stride 0, as in shared-prefix scoring) with per-sequence
+    lengths and queries."""
+    B, Hkv, G, Mq, T = 3, 2, 4, 4, 2600
+    k1, v1 = kv_case(1, Hkv, T, 321)
+    q = rnd((B, Hkv * G, Mq, D), 322, 3)
+    length = torch.tensor([2600, 1500, 1024], dtype=torch.int32)
+    k, v = k1.expand(B, -1, -1, -1), v1.expand(B, -1, -1, -1)
+    _, ref_sc = oracle.focal(k.contiguous(), v.contiguous(), length, q, want_out=False)
+    _, sc = fx.fx_focal_attn_scores(dev(k1).expand(B, -1, -1, -1), dev(v1).expand(B, -1, -1, -1), dev(length),
+                                    dev(q), want_out=False)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    pu.assert_scores_close(sc, ref_sc)
+
+
 # ----------------------------------------------------------------------------------------------
 def _quantised_scores(rows, n, seed, levels):
     g = np.random.default_rng(seed)
