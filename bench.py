@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from synth.workloads import OcrDecode  # noqa: E402
+from synth.workloads import KvSelect, OcrDecode  # noqa: E402
 
 METRIC = "sparse-decode attn tokens/s/GPU and KV GB/s as % of GB300 HBM peak"
 UNIT = "tokens/s"
@@ -585,12 +585,39 @@ def run_hpd_case(args):
         raise SystemExit(1)
 
 
+def run_window_case(args):
+    """The FastKV window scoring of one kv_select layer (scores only: 4 sequences x 8 KV heads x 32768
+    tokens, 8 window queries x 4 query heads per KV head, K = 268 MB), `--reps` times, for profiler
+    captures."""
+    import kv_cache_token_fx_gb300 as fx
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = KvSelect()
+    layer = w.switch_layer
+    k, v = w.layer_kv_salient(layer, device=dev)
+    q = w.window_queries_at(layer, device=dev)
+    ln = torch.full((w.B,), w.T, dtype=torch.int32, device=dev)
+    scores = torch.empty((w.B, w.Hkv, w.T - w.window), dtype=torch.float32, device=dev)
+    ws = fx.Workspace(dev, fx.fx_focal_workspace_bytes(w.B, w.Hkv, w.Hq, w.window, w.T))
+    for _ in range(args.reps):
+        fx.fx_focal_attn_scores(k, v, ln, q, q_pos0=w.T - w.window, cand=(0, w.T - w.window), want_out=False,
+                                scores=scores, ws=ws)
+    torch.cuda.synchronize()
+    bits = fx.fx_device_errors()
+    print(json.dumps({"kernel_case": "window", "reps": args.reps, "device_errors": bits}))
+    if bits:
+        raise SystemExit(1)
+
+
 def run_kernel_case(args):
     """A small, fixed case of one kernel for profiler captures: the decode-shaped call on `--layers`
     distinct layers (each layer's KV is 160 MB, so even one layer exceeds L2), `--reps` passes."""
     import kv_cache_token_fx_gb300 as fx
     if args.kernel_case == "hpd":
         run_hpd_case(args)
+        return
+    if args.kernel_case == "window":
+        run_window_case(args)
         return
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -1071,7 +1098,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk", "hpd"], default=None,
+    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk", "hpd", "window"], default=None,
                     help="run a small fixed case of one kernel (for profiler captures) instead of the bench")
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--reps", type=int, default=2)

@@ -149,6 +149,14 @@ FX_API fx_status fx_workspace_init(void* ws, size_t ws_bytes, void* stream);
  *   out     [B, Hq, Mq, 128] fp32 or NULL      scores [B, Hkv, cand_hi - cand_lo] fp32 or NULL
  *   G*Mq must be <= 64.  0 <= cand_lo <= cand_hi <= Tcap.
  * Workspace: fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap) bytes.
+ * A call without output rows (out == NULL) and with G*Mq > 8 runs on the tensor cores when K admits a
+ * tensor map (row strides multiples of 8 elements and nonzero head and token strides; a batch stride
+ * of 0 is allowed), the cache has at most 2 x (SM count) x 128 x floor(170 / N) rows (N = 16, 32 or 64,
+ * the rows rounded up) and B*Hkv*(1 + 2*G*Mq) <= 262140 (its counters live in the workspace's fixed
+ * counter region): the logits stay in tensor memory, so K is read once and no logits are written.
+ * The result agrees with the other route within the score tolerance.  Its persistent CTAs (one per
+ * SM) each allocate all 512 tensor-memory columns of the SM, and the allocation waits, without a limit,
+ * for them to be free: run no other kernel that holds tensor memory concurrently on another stream.
  */
 FX_API size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap);
 FX_API fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,

@@ -156,12 +156,6 @@ __device__ __forceinline__ float warp_max(float x)
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float warp_sum(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-    return x;
-}
 
 // Sums y[c] (c < H, H a power of two <= 32) over the 32 lanes of the warp: after log2(H) halving steps
 // lane l holds the partial of row (l / (32 / H)) % H over the lanes that differ from it in the upper

@@ -294,7 +294,9 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
 {
     extern __shared__ uint32_t skeys[];   // this CTA's chunk
     __shared__ SelectShared sh;
-    __shared__ uint32_t s_tot[256];       // CTA 0: the row's histogram
+    __shared__ uint32_t s_hist[2][256];   // this chunk's histogram, by round parity (read by the whole cluster)
+    __shared__ uint32_t s_part[4][256];   // partial sums over pairs of the cluster's chunks
+    __shared__ uint32_t s_tot[256];       // the row's histogram
     __shared__ uint32_t s_cnt[2];         // (greater, equal) keys of this chunk
     __shared__ uint32_t s_base[2];
     const int row = blockIdx.y / kTkCluster;
@@ -341,13 +343,20 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
         }
     }
 
+    // Radix passes over 8-bit digits.  Each round every CTA counts its chunk into one of two histograms
+    // (the other may still be read by a slower CTA), and after one cluster barrier every CTA adds up the
+    // cluster's histograms in the same order and takes the same decision itself.
     uint32_t prefix = 0u, pmask = 0u;
     uint32_t krem = (uint32_t)k;
-    for (int pass = 0; pass < 4; ++pass) {
+    int round = 0;
+    bool all_taken = false;   // every counted key with the prefix is taken: no further pass is needed
+    for (int pass = 0; pass < 4 && !all_taken; ++pass) {
         const int shift = 24 - 8 * pass;
         uint32_t digit = 0u, gt = 0u;
         for (int attempt = 0; attempt < 2; ++attempt) {
-            for (int i = tid; i < 256; i += kTkThreads) sh.hist[i] = 0u;
+            uint32_t* hist = s_hist[round & 1];
+            ++round;
+            for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
             __syncthreads();
             for (int j0 = 0; j0 < cn; j0 += kTkThreads) {
                 const int j = j0 + tid;   // whole warps iterate together (ballot/match below)
@@ -357,30 +366,28 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
                 if (take) {
                     const uint32_t d = (key >> shift) & 255u;
                     const unsigned peers = __match_any_sync(active, d);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
                 }
             }
-            cluster_sync();   // every chunk's histogram is complete
-            if (me == 0) {
-                for (int i = tid; i < 256; i += kTkThreads) {
-                    uint32_t t = 0u;
-                    for (int q = 0; q < kTkCluster; ++q) t += ld_cluster_u32(cluster_map(&sh.hist[i], q));
-                    s_tot[i] = t;
-                }
-                __syncthreads();
-                if (tid < 32) find_digit(s_tot, krem, &sh.digit, &sh.gt);
-            }
-            cluster_sync();   // CTA 0 has decided; every histogram has been read
-            if (tid == 0) {
-                s_base[0] = ld_cluster_u32(cluster_map(&sh.digit, 0));
-                s_base[1] = ld_cluster_u32(cluster_map(&sh.gt, 0));
+            cluster_sync();   // every chunk's histogram of this round is complete
+            {
+                // bin i, CTAs 2g and 2g + 1 of the cluster (integer sums: the order does not matter)
+                const int i = tid & 255;
+                const int g = tid >> 8;
+                uint32_t t = 0u;
+                for (int q = 2 * g; q < kTkCluster && q < 2 * g + 2; ++q) t += ld_cluster_u32(cluster_map(&hist[i], q));
+                s_part[g][i] = t;
             }
             __syncthreads();
-            digit = s_base[0];
-            gt = s_base[1];
+            for (int i = tid; i < 256; i += kTkThreads) s_tot[i] = s_part[0][i] + s_part[1][i] + s_part[2][i] + s_part[3][i];
             __syncthreads();
+            if (tid < 32) find_digit(s_tot, krem, &sh.digit, &sh.gt);
+            __syncthreads();
+            digit = sh.digit;
+            gt = sh.gt;
             if (digit == 0xffffffffu && thr != 0u) {
                 thr = 0u;   // warm-start threshold from repeated indices: count again without it
+                __syncthreads();
                 continue;
             }
             break;
@@ -394,7 +401,12 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
         prefix |= digit << shift;
         pmask |= 255u << shift;
         krem -= gt;
+        // When the chosen bin holds exactly the keys still needed, all of them are taken (not with a
+        // warm-start threshold, which leaves keys of the bin below it uncounted).
+        all_taken = thr == 0u && s_tot[digit] == krem;
+        __syncthreads();   // s_tot, sh.digit and sh.gt are rewritten in the next round
     }
+    // the selected keys: masked key > prefix, and the first krem (in index order) with masked key == prefix
     const uint32_t kstar = prefix;
     const uint32_t need_eq = krem;
 
@@ -404,7 +416,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
     const int j1 = min(cn, j0 + per);
     uint32_t g = 0u, e = 0u;
     for (int j = j0; j < j1; ++j) {
-        const uint32_t key = skeys[j];
+        const uint32_t key = skeys[j] & pmask;
         g += key > kstar ? 1u : 0u;
         e += key == kstar ? 1u : 0u;
     }
@@ -429,7 +441,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
     uint32_t ec = s_base[1] + (ex >> 16);
     int32_t* orow = p.out + (int64_t)row * k;
     for (int j = j0; j < j1; ++j) {
-        const uint32_t key = skeys[j];
+        const uint32_t key = skeys[j] & pmask;
         if (key > kstar) {
             const uint32_t pos = gc + min(ec, need_eq);
             if (pos < (uint32_t)k) orow[pos] = c0 + j;

@@ -194,6 +194,26 @@ def test_topk_warm_start_is_exact(fx, n, k):
     assert fx.fx_device_errors() == 0
 
 
+def test_topk_cluster_rows_stop_early_or_run_every_pass(fx):
+    """Long rows (one cluster of CTAs per row): the passes stop once the chosen bin holds exactly the keys
+    still needed, and run to the last byte when the k-th key is tied.  Exact against the oracle."""
+    g = np.random.default_rng(11)
+    cases = []
+    cases.append((g.normal(size=(3, 32760)).astype(np.float32), 2040))      # distinct keys
+    cases.append((g.random(size=(2, 20000)).astype(np.float32), 20000))     # k = n: every key
+    two = np.full((2, 32760), 0.5, np.float32)
+    two[:, :5000] = 1.0
+    g.shuffle(two[1])
+    cases.append((two, 5000))    # the bin of 1.0 holds exactly k keys (same top byte as 0.5)
+    cases.append((two, 5001))    # one 0.5 is needed: the lowest index among the tied ones
+    for s, k in cases:
+        ref = oracle.topk(s, k)
+        got = fx.fx_topk_select(dev(torch.from_numpy(s)), k)
+        torch.cuda.synchronize()
+        assert fx.fx_device_errors() == 0
+        assert np.array_equal(got.cpu().numpy(), ref), (s.shape, k)
+
+
 def test_topk_negative_and_signed_zero(fx):
     s = torch.tensor([[-1.0, 0.0, -0.0, 2.0, -3.0, 2.0, -0.5]], dtype=torch.float32)
     for k in range(1, 8):
