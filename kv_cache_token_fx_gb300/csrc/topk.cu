@@ -22,7 +22,7 @@ namespace {
 
 constexpr int kTkThreads = 1024;
 constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kSmemKeys = 48 * 1024;   // 192 KB of keys
+constexpr int kSmemKeys = 44 * 1024;   // 176 KB of keys (plus 21 KB of static histogram rows)
 constexpr int kClusterMinKeys = 16384;  // rows at least this long may be split over a cluster
 constexpr int kClusterMaxCtasPerSm = 152;   // (times 2) cluster CTAs allowed in one launch
 
@@ -115,14 +115,47 @@ struct SelectShared {
     uint32_t digit, gt, thr, bad;
 };
 
+// Radix-digit counting.  Every warp pair counts into its own row of `rows` with plain shared atomics --
+// no warp aggregation (match.any over 32 distinct digits cost more than the atomics it saved) and no
+// contention between pairs -- and the rows are then added up per bin into hist[256].  Counted: keys
+// key_at(j), j = tid, tid + kTkThreads, ... < n, that are >= thr and equal prefix under pmask; the digit
+// is byte `shift` of the key.  All threads call it; it begins and ends with a barrier.
+constexpr int kHistRows = kTkWarps / 2;
+template <typename KeyAt>
+__device__ __forceinline__ void count_digits(KeyAt key_at, int n, uint32_t thr, uint32_t prefix, uint32_t pmask,
+                                             int shift, uint32_t (*rows)[256], uint32_t (*part)[256], uint32_t* hist)
+{
+    const int tid = threadIdx.x;
+    uint32_t* mine = rows[(tid >> 5) >> 1];
+    for (int i = tid; i < kHistRows * 256; i += kTkThreads) (&rows[0][0])[i] = 0u;
+    __syncthreads();
+    for (int j = tid; j < n; j += kTkThreads) {
+        const uint32_t key = key_at(j);
+        if (key >= thr && (key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    {
+        const int b = tid & 255;
+        const int g = tid >> 8;   // 4 groups of kHistRows / 4 rows
+        uint32_t t = 0u;
+#pragma unroll
+        for (int r = 0; r < kHistRows / 4; ++r) t += rows[g * (kHistRows / 4) + r][b];
+        part[g][b] = t;
+    }
+    __syncthreads();
+    for (int b = tid; b < 256; b += kTkThreads) hist[b] = part[0][b] + part[1][b] + part[2][b] + part[3][b];
+    __syncthreads();
+}
+
 // The top-k of one row of n keys (in skeys when SMEM, else read from src), written to orow in
 // ascending index order.  prow: the previous set of this row (warm start) or nullptr.  All threads of
 // the CTA call it; it begins and ends with a barrier.
 constexpr int kNoPre = -2147483647 - 1;   // "prev index of this thread not loaded in advance"
 
 template <bool SMEM>
-__device__ void select_row(SelectShared& sh, const uint32_t* skeys, const float* src, int n, int k,
-                           const int32_t* prow, int32_t* orow, unsigned* err, int pre = kNoPre)
+__device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*hpart)[256], const uint32_t* skeys,
+                           const float* src, int n, int k, const int32_t* prow, int32_t* orow, unsigned* err,
+                           int pre = kNoPre)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -160,20 +193,8 @@ __device__ void select_row(SelectShared& sh, const uint32_t* skeys, const float*
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         for (int attempt = 0; attempt < 2; ++attempt) {
-            for (int i = tid; i < 256; i += kTkThreads) sh.hist[i] = 0u;
-            __syncthreads();
-            for (int j0 = 0; j0 < n; j0 += kTkThreads) {
-                const int j = j0 + tid;   // whole warps iterate together (ballot/match below)
-                const uint32_t key = j < n ? get_key<SMEM>(skeys, src, j) : 0u;
-                const bool take = j < n && key >= thr && (key & pmask) == prefix;
-                const unsigned active = __ballot_sync(0xffffffffu, take);
-                if (take) {
-                    const uint32_t digit = (key >> shift) & 255u;
-                    const unsigned peers = __match_any_sync(active, digit);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
-                }
-            }
-            __syncthreads();
+            count_digits([&](int j) { return get_key<SMEM>(skeys, src, j); }, n, thr, prefix, pmask, shift, hrows, hpart,
+                         sh.hist);
             if (tid < 32) find_digit(sh.hist, krem, &sh.digit, &sh.gt);
             __syncthreads();
             if (sh.digit == 0xffffffffu && thr != 0u) {
@@ -264,10 +285,12 @@ __device__ void select_row(SelectShared& sh, const uint32_t* skeys, const float*
 }
 
 template <bool SMEM>
-__global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
+__global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(const TopkParams p)
 {
     extern __shared__ uint32_t skeys[];
     __shared__ SelectShared sh;
+    __shared__ uint32_t s_rows[kHistRows][256];
+    __shared__ uint32_t s_part[4][256];
 
     const int row = blockIdx.x;
     // this thread's entry of the previous set, read before the wait when the caller allows it
@@ -279,23 +302,23 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p)
     if (SMEM) {
         for (int j = threadIdx.x; j < p.n; j += kTkThreads) skeys[j] = order_key(src[j]);
     }
-    select_row<SMEM>(sh, skeys, src, p.n, p.k, p.prev != nullptr ? p.prev + (int64_t)row * p.k : nullptr,
+    select_row<SMEM>(sh, s_rows, s_part, skeys, src, p.n, p.k, p.prev != nullptr ? p.prev + (int64_t)row * p.k : nullptr,
                      p.out + (int64_t)row * p.k, p.err, pre);
 }
 
 // Few long rows: one cluster of kTkCluster CTAs per row.  CTA r of the cluster holds the contiguous
-// chunk r of the row in shared memory; each radix pass counts the chunks in parallel, CTA 0 adds the
-// histograms through distributed shared memory and decides the digit, which every CTA then reads
-// back.  The ordered output offsets each chunk by the (greater, equal) counts of the chunks before
+// chunk r of the row in shared memory; each radix pass counts the chunks in parallel, and every CTA
+// adds the cluster's histograms through distributed shared memory and takes the same digit decision.  The ordered output offsets each chunk by the (greater, equal) counts of the chunks before
 // it.  Same selection, bit for bit, as select_row.
 constexpr int kTkCluster = 8;
 
-__global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkParams p)
+__global__ void __launch_bounds__(kTkThreads, 2) topk_cluster_kernel(const TopkParams p)
 {
     extern __shared__ uint32_t skeys[];   // this CTA's chunk
     __shared__ SelectShared sh;
     __shared__ uint32_t s_hist[2][256];   // this chunk's histogram, by round parity (read by the whole cluster)
-    __shared__ uint32_t s_part[4][256];   // partial sums over pairs of the cluster's chunks
+    __shared__ uint32_t s_part[4][256];   // partial sums (of histogram rows, then of the cluster's chunks)
+    __shared__ uint32_t s_rows[kHistRows][256];
     __shared__ uint32_t s_tot[256];       // the row's histogram
     __shared__ uint32_t s_cnt[2];         // (greater, equal) keys of this chunk
     __shared__ uint32_t s_base[2];
@@ -356,19 +379,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_cluster_kernel(const TopkPara
         for (int attempt = 0; attempt < 2; ++attempt) {
             uint32_t* hist = s_hist[round & 1];
             ++round;
-            for (int i = tid; i < 256; i += kTkThreads) hist[i] = 0u;
-            __syncthreads();
-            for (int j0 = 0; j0 < cn; j0 += kTkThreads) {
-                const int j = j0 + tid;   // whole warps iterate together (ballot/match below)
-                const uint32_t key = j < cn ? skeys[j] : 0u;
-                const bool take = j < cn && key >= thr && (key & pmask) == prefix;
-                const unsigned active = __ballot_sync(0xffffffffu, take);
-                if (take) {
-                    const uint32_t d = (key >> shift) & 255u;
-                    const unsigned peers = __match_any_sync(active, d);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-                }
-            }
+            count_digits([&](int j) { return skeys[j]; }, cn, thr, prefix, pmask, shift, s_rows, s_part, hist);
             cluster_sync();   // every chunk's histogram of this round is complete
             {
                 // bin i, CTAs 2g and 2g + 1 of the cluster (integer sums: the order does not matter)
