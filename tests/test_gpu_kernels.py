@@ -398,6 +398,55 @@ def test_per_layer_retention_matches_oracle(fx):
             assert torch.equal(dv[l, b, :, :n].cpu().view(torch.int16), rv[b, :, :n].view(torch.int16))
 
 
+def test_retention_on_tensor_cores_matches_calls_and_captures(fx):
+    """FastKV retention with 32 window rows per KV head (the scoring takes the tensor-core route, layer
+    after layer on one workspace, as programmatic dependent launches).  Equal to the individual calls
+    (scores, top-k, compaction) and to the oracle; the same call captured in a CUDA graph and replayed
+    gives the same result."""
+    n_layers, B, Hkv, G, Mq, T, keep = 5, 2, 2, 4, 8, 3000, 300
+    cand = T - Mq
+    ks = torch.stack([rnd((B, Hkv, T, D), 190 + l, 1) for l in range(n_layers)])
+    vs = torch.stack([rnd((B, Hkv, T, D), 190 + l, 2) for l in range(n_layers)])
+    qs = torch.stack([rnd((B, Hkv * G, Mq, D), 190 + l, 3) for l in range(n_layers)])
+    length = torch.tensor([T, 2100], dtype=torch.int32)
+    cap = keep + Mq + 8
+    dks, dvs, dls, dl = dev(ks), dev(vs), dev(length), torch.zeros(B, dtype=torch.int32, device="cuda")
+    dk = torch.zeros((n_layers, B, Hkv, cap, D), dtype=torch.bfloat16, device="cuda")
+    dv = torch.zeros_like(dk)
+    idx = fx.fx_kv_retain_per_layer(dks, dvs, dls, dev(qs), keep, cand, cand, dk, dv, dl, q_pos0=cand,
+                                    flags=fx.FX_LAUNCH_PDL)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    for l in range(n_layers):
+        _, sc = fx.fx_focal_attn_scores(dks[l], dvs[l], dls, dev(qs[l]), q_pos0=cand, cand=(0, cand), want_out=False)
+        ref_gpu = fx.fx_topk_select(sc.reshape(B * Hkv, cand), keep).reshape(B, Hkv, keep)
+        assert torch.equal(idx[l], ref_gpu), l
+        if l in (0, n_layers - 1):
+            _, osc = oracle.focal(ks[l], vs[l], length, qs[l], q_pos0=cand, cand=(0, cand), want_out=False)
+            pu.check_index_sets(idx[l], oracle.topk(osc, keep), osc, keep)
+        rk, rv, rl = oracle.kv_compact(ks[l], vs[l], length, idx[l].cpu(), cand, cap)
+        assert torch.equal(dl.cpu(), rl)
+        for b in range(B):
+            n = int(rl[b])
+            assert torch.equal(dk[l, b, :, :n].cpu().view(torch.int16), rk[b, :, :n].view(torch.int16))
+    # captured in a CUDA graph and replayed
+    idx2 = torch.full_like(idx, -1)
+    dk2, dv2 = torch.zeros_like(dk), torch.zeros_like(dv)
+    dl2 = torch.zeros_like(dl)
+    dq = dev(qs)
+    ws = fx.Workspace(torch.device("cuda", 0),
+                      fx.load_library().fx_retain_workspace_bytes(B, Hkv, Hkv * G, Mq, T, cand))
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fx.fx_kv_retain_per_layer(dks, dvs, dls, dq, keep, cand, cand, dk2, dv2, dl2, q_pos0=cand, idx_out=idx2, ws=ws,
+                                  stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert torch.equal(idx2, idx) and torch.equal(dk2, dk) and torch.equal(dl2, dl)
+
+
 def test_focal_layer_profiling_matches_oracle(fx):
     """Warm-up profiling of the image-attention ratio per layer (fx_focal_mass over each layer's image
     scores, accumulated over the warm-up steps) and the choice of the C focal layers."""
