@@ -151,7 +151,7 @@ FX_API fx_status fx_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * Workspace: fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap) bytes.
  * A call without output rows (out == NULL) and with G*Mq > 8 runs on the tensor cores when K admits a
  * tensor map (row strides multiples of 8 elements and nonzero head and token strides; a batch stride
- * of 0 is allowed), the cache has at most 2 x (SM count) x 128 x floor(170 / N) rows (N = 16, 32 or 64,
+ * of 0 is allowed), the cache has at most 2 x (SM count) x 128 x (128 / N) rows (N = 16, 32 or 64,
  * the rows rounded up) and B*Hkv*(1 + 2*G*Mq) <= 262140 (its counters live in the workspace's fixed
  * counter region): the logits stay in tensor memory, so K is read once and no logits are written.
  * The result agrees with the other route within the score tolerance.  Its persistent CTAs (one per
@@ -300,7 +300,8 @@ FX_API fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer,
  *   idx_out  [n_layers, B, Hkv, keep_k] int32, written (ascending per row)
  *   1 <= keep_k <= cand_hi <= Tcap.  Results equal those of the individual calls.
  * Workspace: fx_retain_workspace_bytes(B, Hkv, Hq, Mq, Tcap, cand_hi) bytes (one layer's focal
- * scratch and scores, reused layer after layer).
+ * scratch, reused layer after layer, and the scores of 8 layers: layers are scored 8 at a time and each
+ * batch is selected by one top-k call over all its rows).
  */
 FX_API size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi);
 FX_API fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer, int n_layers,

@@ -738,11 +738,15 @@ fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer, int n_
 }
 
 // ---------------------------------------------------------------------------------------------
+// Layers are scored kRetainBatch at a time into their own score rows, then selected by one top-k launch
+// over all of them (many rows in flight hide each row's latency; the batch's scores stay in L2).
+constexpr int kRetainBatch = 8;
+
 size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi)
 {
     const size_t f = fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap);
     if (f == 0 || cand_hi < 1) return 0;
-    return round_up(f) + round_up((size_t)B * Hkv * cand_hi * sizeof(float));
+    return round_up(f) + round_up((size_t)kRetainBatch * B * Hkv * cand_hi * sizeof(float));
 }
 
 fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer, int n_layers, const fx_bf16* q,
@@ -766,18 +770,23 @@ fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer,
     float* scores = reinterpret_cast<float*>(static_cast<char*>(ws) + fbytes);
     const int rows = kv->B * kv->Hkv;
     const size_t q_layer = (size_t)kv->B * Hq * Mq * kHeadDim;
+    const size_t layer_scores = (size_t)rows * cand_hi;
     // Every call after the first runs as a programmatic dependent launch when the caller asked for
     // one; the later focal calls read K and lengths that were written before the first call.
     const unsigned pdl = flags & FX_LAUNCH_PDL;
-    for (int l = 0; l < n_layers; ++l) {
-        fx_kv_desc kl = *kv;
-        kl.k = kv->k + (int64_t)l * src_stride_layer;
-        kl.v = kv->v + (int64_t)l * src_stride_layer;
-        const unsigned ff = l == 0 ? flags : (pdl ? (FX_LAUNCH_PDL | FX_LAUNCH_INPUTS_READY) : 0u);
-        st = fx_focal_attn_scores(&kl, q + (size_t)l * q_layer, Hq, Mq, q_pos0, scale, 0, cand_hi, nullptr, scores, ws,
-                                  fbytes, ff, stream);
-        if (st != FX_OK) return st;
-        st = fx_topk_select(scores, rows, cand_hi, keep_k, nullptr, idx_out + (size_t)l * rows * keep_k, pdl, stream);
+    for (int l0 = 0; l0 < n_layers; l0 += kRetainBatch) {
+        const int nb = std::min(kRetainBatch, n_layers - l0);
+        for (int l = l0; l < l0 + nb; ++l) {
+            fx_kv_desc kl = *kv;
+            kl.k = kv->k + (int64_t)l * src_stride_layer;
+            kl.v = kv->v + (int64_t)l * src_stride_layer;
+            const unsigned ff = l == 0 ? flags : (pdl ? (FX_LAUNCH_PDL | FX_LAUNCH_INPUTS_READY) : 0u);
+            st = fx_focal_attn_scores(&kl, q + (size_t)l * q_layer, Hq, Mq, q_pos0, scale, 0, cand_hi, nullptr,
+                                      scores + (size_t)(l - l0) * layer_scores, ws, fbytes, ff, stream);
+            if (st != FX_OK) return st;
+        }
+        // the batch's layers' rows are consecutive in both the score rows and idx_out
+        st = fx_topk_select(scores, nb * rows, cand_hi, keep_k, nullptr, idx_out + (size_t)l0 * rows * keep_k, pdl, stream);
         if (st != FX_OK) return st;
     }
     return fx_kv_compact(kv, src_stride_layer, idx_out, (int64_t)rows * keep_k, keep_k, tail_lo, dst,

@@ -124,7 +124,7 @@ struct AttnParams {
 // keeps kScoreBufs of them in flight, each range's logits in its own part of the tensor memory.
 constexpr int kScoreKeys = 128;
 constexpr int kScoreTmemCols = 512;   // the whole tensor memory of the SM
-constexpr int kScoreBufs = 3;         // ranges in flight per CTA
+constexpr int kScoreBufs = 4;         // ranges in flight per CTA
 constexpr int kScoreStages = 4;       // 32 KB K tiles in flight per CTA
 __host__ __device__ constexpr int score_item_tiles(int n_cols) { return (kScoreTmemCols / kScoreBufs) / n_cols; }
 // The N of a call with R rows: 16, 32 or 64 (each of the kernel's two row halves a power of two).

@@ -9,9 +9,9 @@
 // (R x 4 bytes per key against 256), and writing them out and reading them back doubles the call's
 // traffic.  This kernel keeps them on chip.
 //
-// Work is cut into items: a contiguous range of 128 x floor(170 / N) keys of one (sequence, KV head),
-// N = 16, 32 or 64 (the rows rounded up).  One persistent CTA per SM takes items from a ticket counter
-// and keeps three in flight, each in its own third of the CTA's 512 tensor-memory columns (a "buffer"):
+// Work is cut into items: a contiguous range of 128 x (128 / N) keys of one (sequence, KV head), N = 16,
+// 32 or 64 (the rows rounded up).  One persistent CTA per SM takes items from a ticket counter and keeps
+// four in flight, each in its own quarter of the CTA's 512 tensor-memory columns (a "buffer"):
 //   warp 0       draws the ticket and issues TMA copies of the item's K tiles (128 rows x 64 columns
 //                each, 128-byte swizzle) into a ring of 32 KB slots shared by all items, the item's
 //                query rows (an N-row K-major operand tile per buffer) with its first tile;
@@ -32,10 +32,10 @@
 //
 // Waiting for other items needs their CTAs to make progress.  Publishing an item (group A) waits only
 // for its own products, never for another item, so an item that has been drawn always gets published.
-// Tickets are drawn in order, and a CTA draws one only when a buffer is free, so it holds at most three
+// Tickets are drawn in order, and a CTA draws one only when a buffer is free, so it holds at most four
 // items.  While the lowest incomplete (sequence, KV head) still has an undrawn item, every drawn item
 // belongs to it or to an earlier one (those complete: all their items are drawn and get published); a
-// CTA that cannot draw holds three of its items, so with nsplit <= 3 x (CTAs) some CTA can always draw
+// CTA that cannot draw holds four of its items, so with nsplit <= 4 x (CTAs) some CTA can always draw
 // the next one.  The host keeps nsplit at most twice the SM count.  Every wait is bounded all the same.
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -291,10 +291,8 @@ __global__ void __launch_bounds__(kScThreads, 1) score_tc_kernel(const ScorePara
     const unsigned total = (unsigned)(p.pairs * p.nsplit);
     const unsigned spin = p.spin_limit;
 
-    // Counters, lengths and queries may be written by the preceding kernel on the stream.
-    griddep_wait();
-    griddep_launch();
-
+    // Shared-memory barriers and the tensor memory first: they touch no global memory, so with a
+    // programmatic dependent launch this overlaps the preceding kernel's tail.
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -319,6 +317,10 @@ __global__ void __launch_bounds__(kScThreads, 1) score_tc_kernel(const ScorePara
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_tmem;
+
+    // Counters, lengths and queries may be written by the preceding kernel on the stream.
+    griddep_wait();
+    griddep_launch();
 
     if (warp == 0) {
         // ---- items and copies ---------------------------------------------------------------------
