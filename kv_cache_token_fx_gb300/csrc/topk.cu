@@ -220,15 +220,20 @@ __device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*
         prefix |= sh.digit << shift;
         pmask |= 255u << shift;
         krem -= sh.gt;
+        // When the chosen bin holds exactly the keys still needed, all of them are taken (not with a
+        // warm-start threshold, which leaves keys of the bin below it uncounted).
+        const bool all_taken = thr == 0u && sh.hist[sh.digit] == krem;
         __syncthreads();
+        if (all_taken) break;
     }
+    // the selected keys: masked key > prefix, and the first krem (in index order) with masked key == prefix
     const uint32_t kstar = prefix;
     const uint32_t need_eq = krem;
 
     // ---- ordered output -------------------------------------------------------------------------
     // position of an index j = (# greater before j) + min(# equal before j, need_eq); an equal key is
-    // taken while (# equal before j) < need_eq.  Positions are < k by construction; the bound checks
-    // keep a logic slip from writing past the row.
+    // taken while (# equal before j) < need_eq (keys compared under pmask, the digits decided).
+    // Positions are < k by construction; the bound checks keep a logic slip from writing past the row.
     if (SMEM) {
         // each thread owns a contiguous chunk of the row: one scan for the whole row
         const int per = (n + kTkThreads - 1) / kTkThreads;
@@ -236,7 +241,7 @@ __device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*
         const int j1 = min(n, j0 + per);
         uint32_t g = 0u, e = 0u;
         for (int j = j0; j < j1; ++j) {
-            const uint32_t key = skeys[j];
+            const uint32_t key = skeys[j] & pmask;
             g += key > kstar ? 1u : 0u;
             e += key == kstar ? 1u : 0u;
         }
@@ -245,7 +250,7 @@ __device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*
         uint32_t gc = ex & 0xffffu;
         uint32_t ec = ex >> 16;
         for (int j = j0; j < j1; ++j) {
-            const uint32_t key = skeys[j];
+            const uint32_t key = skeys[j] & pmask;
             if (key > kstar) {
                 const uint32_t pos = gc + min(ec, need_eq);
                 if (pos < (uint32_t)k) orow[pos] = j;
@@ -262,7 +267,7 @@ __device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*
             const int j = t0 + tid;
             uint32_t g = 0u, e = 0u;
             if (j < n) {
-                const uint32_t key = get_key<SMEM>(skeys, src, j);
+                const uint32_t key = get_key<SMEM>(skeys, src, j) & pmask;
                 g = key > kstar ? 1u : 0u;
                 e = key == kstar ? 1u : 0u;
             }

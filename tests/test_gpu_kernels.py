@@ -194,9 +194,10 @@ def test_topk_warm_start_is_exact(fx, n, k):
     assert fx.fx_device_errors() == 0
 
 
-def test_topk_cluster_rows_stop_early_or_run_every_pass(fx):
-    """Long rows (one cluster of CTAs per row): the passes stop once the chosen bin holds exactly the keys
-    still needed, and run to the last byte when the k-th key is tied.  Exact against the oracle."""
+def test_topk_long_rows_stop_early_or_run_every_pass(fx):
+    """Long rows (a cluster of CTAs per row, or one CTA per row when there are many): the passes stop once
+    the chosen bin holds exactly the keys still needed, and run to the last byte when the k-th key is
+    tied.  Exact against the oracle."""
     g = np.random.default_rng(11)
     cases = []
     cases.append((g.normal(size=(3, 32760)).astype(np.float32), 2040))      # distinct keys
@@ -206,6 +207,10 @@ def test_topk_cluster_rows_stop_early_or_run_every_pass(fx):
     g.shuffle(two[1])
     cases.append((two, 5000))    # the bin of 1.0 holds exactly k keys (same top byte as 0.5)
     cases.append((two, 5001))    # one 0.5 is needed: the lowest index among the tied ones
+    many = np.full((40, 20000), 0.25, np.float32)   # 40 long rows: one CTA per row
+    many[:, ::7] = g.normal(size=(40, (20000 + 6) // 7)).astype(np.float32)
+    cases.append((many, 1500))
+    cases.append((many, 2858))   # every key above 0.25 and the first tied 0.25s
     for s, k in cases:
         ref = oracle.topk(s, k)
         got = fx.fx_topk_select(dev(torch.from_numpy(s)), k)
