@@ -137,6 +137,33 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------------------------
+def _kernel_nodes(fn, dev, rt):
+    """Kernel launches made by fn(), counted as the kernel nodes of a CUDA graph captured around it (None
+    when this PyTorch cannot hand out the raw graph)."""
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        return None
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    graph = ctypes.c_void_p(int(g.raw_cuda_graph()))
+    n = ctypes.c_size_t(0)
+    if rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
+        return None
+    nodes = (ctypes.c_void_p * n.value)()
+    if rt.cudaGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
+        return None
+    kernels = 0
+    for i in range(n.value):
+        ty = ctypes.c_int(-1)
+        if rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(ty)) != 0:
+            return None
+        kernels += int(ty.value == 0)   # cudaGraphNodeTypeKernel
+    del g
+    return kernels
+
+
 def _cudart():
     """The CUDA runtime PyTorch already loaded (for external event nodes and 2-D copies)."""
     for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
@@ -289,29 +316,7 @@ class OcrDecodeRun:
     def count_kernel_nodes(self, t: int):
         """Kernel launches of one step, counted as the kernel nodes of a captured graph of it (None when
         this PyTorch cannot hand out the raw graph)."""
-        try:
-            g = torch.cuda.CUDAGraph(keep_graph=True)
-        except TypeError:
-            return None
-        s = torch.cuda.Stream(self.dev)
-        with torch.cuda.graph(g, stream=s):
-            self.step(t)
-        rt = self.rt
-        graph = ctypes.c_void_p(int(g.raw_cuda_graph()))
-        n = ctypes.c_size_t(0)
-        if rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) != 0:
-            return None
-        nodes = (ctypes.c_void_p * n.value)()
-        if rt.cudaGraphGetNodes(graph, nodes, ctypes.byref(n)) != 0:
-            return None
-        kernels = 0
-        for i in range(n.value):
-            ty = ctypes.c_int(-1)
-            if rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(ty)) != 0:
-                return None
-            kernels += int(ty.value == 0)   # cudaGraphNodeTypeKernel
-        del g
-        return kernels
+        return _kernel_nodes(lambda: self.step(t), self.dev, self.rt)
 
     def capture(self):
         counted = self.count_kernel_nodes(self.w.steps - 1)
@@ -722,6 +727,7 @@ def secondary_kv_select(args, peak, peak_kind):
     retain()
     torch.cuda.synchronize()
     retain_ms = _events_ms(retain, 3)
+    retain_launches = _kernel_nodes(retain, dev, _cudart())
     # algorithmic bytes: K rows of every layer for the scores (V is not read), the compaction's reads and
     # writes of the kept rows
     retain_bytes = L * B * Hkv * (T * 256 + w.keep * 512 * 2)
@@ -821,7 +827,7 @@ def secondary_kv_select(args, peak, peak_kind):
                               ms / L, peak, peak_kind),
         "retention": {"ms": round(retain_ms, 3), "algorithmic_bytes": int(retain_bytes),
                       "gbs": round(retain_bytes / (retain_ms / 1e3) / 1e9, 1), "frac": round(peak_frac, 4),
-                      "launches": L * 3 + 1, "kept_rows": int(clen[0])},
+                      "launches": retain_launches, "kept_rows": int(clen[0])},
         "e2e": e2e, "cpu_baseline": cpu, "clocks": sampler.summary(), "gpu_launches": n_calls,
     }
     return res

@@ -303,6 +303,72 @@ size_t fx_focal_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap)
     return std::max(make_layout(B * Hkv, R, pl, Tcap, false).total, make_layout(B * Hkv, R, ps, Tcap, false).total);
 }
 
+// Workspace of the tensor-core scoring kernel over `layers` layers of B x Hkv pairs: the counter region,
+// then the (m, l) partials of every key range; 0 when the kernel does not take the shape.
+size_t score_tc_workspace_bytes(int layers, int B, int Hkv, int R, int Tcap, int sm_count)
+{
+    const int64_t pairs = (int64_t)layers * B * Hkv;
+    ScoreTcPlan sp;
+    if (R <= kStreamRows || pairs > 0x7fffffff || 4 + pairs + 2 * pairs * R > (int64_t)kCounterSlots ||
+        !make_score_tc_plan((int)pairs, R, Tcap, sm_count, &sp))
+        return 0;
+    const size_t np = (size_t)pairs * sp.nsplit * R;
+    return kCounterBytes + 2 * round_up(np * sizeof(float));
+}
+
+// Scores of `layers` consecutive layers (K of layer l at kv->k + l * layer_stride, its queries the l-th
+// block of B Hq Mq rows of q, its scores the l-th block of B Hkv rows of cand_hi - cand_lo) on the
+// tensor cores.  Returns false, launching nothing, when the kernel does not take the shape or K admits
+// no tensor map; otherwise *st is the launch status.
+bool score_tc_route(DeviceState* ds, const fx_kv_desc* kv, int64_t layer_stride, int layers, const fx_bf16* q,
+                    int Hq, int Mq, int q_pos0, float scale, int cand_lo, int cand_hi, float* scores, void* ws,
+                    size_t ws_bytes, bool pdl, cudaStream_t s, fx_status* st)
+{
+    const int G = Hq / kv->Hkv;
+    const int R = G * Mq;
+    const size_t need = score_tc_workspace_bytes(layers, kv->B, kv->Hkv, R, kv->Tcap, ds->sm_count);
+    if (need == 0) return false;
+    const int pairs = layers * kv->B * kv->Hkv;
+    ScoreTcPlan sp;
+    CUtensorMap tk, tq;
+    int bcast = 0;
+    if (!make_score_tc_plan(pairs, R, kv->Tcap, ds->sm_count, &sp) ||
+        !encode_score_maps(kv, layer_stride, layers, q, Hq, Mq, score_tc_cols(R), &tk, &tq, &bcast))
+        return false;
+    if ((*st = check_ws(ws, ws_bytes, need)) != FX_OK) return true;
+    const size_t np = (size_t)pairs * sp.nsplit * R;
+    char* w = static_cast<char*>(ws);
+    ScoreParams c;
+    memset(&c, 0, sizeof c);
+    c.len = kv->len;
+    c.B = kv->B;
+    c.Hkv = kv->Hkv;
+    c.Tcap = kv->Tcap;
+    c.layers = layers;
+    c.k_bcast = bcast;
+    c.q = q;
+    c.Hq = Hq;
+    c.G = G;
+    c.Mq = Mq;
+    c.R = R;
+    c.q_pos0 = q_pos0;
+    c.qscale = log2e_scale(scale);
+    c.pairs = pairs;
+    c.nsplit = sp.nsplit;
+    c.split_len = sp.split_len;
+    c.cand_lo = cand_lo;
+    c.cand_hi = cand_hi;
+    c.part_m = reinterpret_cast<float*>(w + kCounterBytes);
+    c.part_l = reinterpret_cast<float*>(w + kCounterBytes + round_up(np * sizeof(float)));
+    c.counters = reinterpret_cast<unsigned*>(w);
+    c.scores = scores;
+    c.err = ds->err;
+    c.spin_limit = kSpinLimit;
+    cudaError_t e = launch_score_tc(c, &tk, &tq, sp.grid, pdl, s);
+    *st = e == cudaSuccess ? FX_OK : cuda_fail(e, "tensor-core scoring launch");
+    return true;
+}
+
 fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int q_pos0,
                                float scale, int cand_lo, int cand_hi, float* out, float* scores,
                                void* ws, size_t ws_bytes, unsigned flags, void* stream)
@@ -329,46 +395,9 @@ fx_status fx_focal_attn_scores(const fx_kv_desc* kv, const fx_bf16* q, int Hq, i
 
     // Scores only, more than 8 rows: the tensor-core kernel that keeps the logits on chip (its R fp32
     // logits per key would otherwise be written and read back), when K admits a tensor map.
-    ScoreTcPlan sp;
-    CUtensorMap tk, tq;
-    int bcast = 0;
-    if (out == nullptr && R > kStreamRows && 4 + pairs + 2 * (int64_t)pairs * R <= (int64_t)kCounterSlots &&
-        make_score_tc_plan(pairs, R, kv->Tcap, ds->sm_count, &sp) &&
-        encode_score_maps(kv, q, Hq, Mq, score_tc_cols(R), &tk, &tq, &bcast)) {
-        const size_t np = (size_t)pairs * sp.nsplit * R;
-        const size_t off_m = kCounterBytes;
-        const size_t off_l = off_m + round_up(np * sizeof(float));
-        if ((st = check_ws(ws, ws_bytes, off_l + round_up(np * sizeof(float)))) != FX_OK) return st;
-        char* w = static_cast<char*>(ws);
-        ScoreParams c;
-        memset(&c, 0, sizeof c);
-        c.len = kv->len;
-        c.B = kv->B;
-        c.Hkv = kv->Hkv;
-        c.Tcap = kv->Tcap;
-        c.k_bcast = bcast;
-        c.q = q;
-        c.Hq = Hq;
-        c.G = G;
-        c.Mq = Mq;
-        c.R = R;
-        c.q_pos0 = q_pos0;
-        c.qscale = log2e_scale(scale);
-        c.pairs = pairs;
-        c.nsplit = sp.nsplit;
-        c.split_len = sp.split_len;
-        c.cand_lo = cand_lo;
-        c.cand_hi = cand_hi;
-        c.part_m = reinterpret_cast<float*>(w + off_m);
-        c.part_l = reinterpret_cast<float*>(w + off_l);
-        c.counters = reinterpret_cast<unsigned*>(w);
-        c.scores = scores;
-        c.err = ds->err;
-        c.spin_limit = kSpinLimit;
-        cudaError_t e = launch_score_tc(c, &tk, &tq, sp.grid, pdl, s);
-        if (e != cudaSuccess) return cuda_fail(e, "tensor-core scoring launch");
-        return FX_OK;
-    }
+    if (out == nullptr && score_tc_route(ds, kv, 0, 1, q, Hq, Mq, q_pos0, scale, cand_lo, cand_hi, scores, ws, ws_bytes,
+                                         pdl, s, &st))
+        return st;
 
     const Plan pl = make_plan(pairs, R, kv->Tcap, ds->sm_count, false, false, out == nullptr);
     const Layout L = make_layout(pairs, R, pl, kv->Tcap, false);
@@ -738,15 +767,25 @@ fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer, int n_
 }
 
 // ---------------------------------------------------------------------------------------------
-// Layers are scored kRetainBatch at a time into their own score rows, then selected by one top-k launch
-// over all of them (many rows in flight hide each row's latency; the batch's scores stay in L2).
+// Layers are scored kRetainBatch at a time into their own score rows -- by one launch of the tensor-core
+// scoring kernel over all of them when it takes the shape, so that one layer's last key ranges overlap
+// the next layer's stream --, then selected by one top-k launch over all of them (many rows in flight
+// hide each row's latency; the batch's scores stay in L2).
 constexpr int kRetainBatch = 8;
+
+size_t retain_scoring_bytes(int B, int Hkv, int Hq, int Mq, int Tcap)
+{
+    const size_t f = fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap);
+    if (f == 0) return 0;
+    const int R = (Hq / Hkv) * Mq;
+    return round_up(std::max(f, score_tc_workspace_bytes(kRetainBatch, B, Hkv, R, Tcap, sm_count_or_default())));
+}
 
 size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi)
 {
-    const size_t f = fx_focal_workspace_bytes(B, Hkv, Hq, Mq, Tcap);
+    const size_t f = retain_scoring_bytes(B, Hkv, Hq, Mq, Tcap);
     if (f == 0 || cand_hi < 1) return 0;
-    return round_up(f) + round_up((size_t)kRetainBatch * B * Hkv * cand_hi * sizeof(float));
+    return f + round_up((size_t)kRetainBatch * B * Hkv * cand_hi * sizeof(float));
 }
 
 fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer, int n_layers, const fx_bf16* q,
@@ -763,11 +802,17 @@ fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer,
     if (cand_hi < 1 || cand_hi > kv->Tcap) return fail(FX_ERR_INVALID_ARG, "need 1 <= cand_hi <= Tcap");
     if (keep_k < 1 || keep_k > cand_hi) return fail(FX_ERR_INVALID_ARG, "need 1 <= keep_k <= cand_hi");
     if (!row_stride_ok(src_stride_layer)) return fail(FX_ERR_INVALID_ARG, "src_stride_layer must be a multiple of 8");
+    if ((st = check_heads(Hq, kv->Hkv, Mq)) != FX_OK) return st;
+    if (!aligned16(q)) return fail(FX_ERR_INVALID_ARG, "q must be 16-byte aligned");
+    if (q_pos0 < -1) return fail(FX_ERR_INVALID_ARG, "q_pos0 must be -1 or >= 0");
+    if (!isfinite(scale)) return fail(FX_ERR_INVALID_ARG, "scale must be finite");
     const size_t need = fx_retain_workspace_bytes(kv->B, kv->Hkv, Hq, Mq, kv->Tcap, cand_hi);
     if (need == 0) return fail(FX_ERR_INVALID_ARG, "bad shape");
     if ((st = check_ws(ws, ws_bytes, need)) != FX_OK) return st;
-    const size_t fbytes = round_up(fx_focal_workspace_bytes(kv->B, kv->Hkv, Hq, Mq, kv->Tcap));
+    const size_t fbytes = retain_scoring_bytes(kv->B, kv->Hkv, Hq, Mq, kv->Tcap);
     float* scores = reinterpret_cast<float*>(static_cast<char*>(ws) + fbytes);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FX_OK) return st;
     const int rows = kv->B * kv->Hkv;
     const size_t q_layer = (size_t)kv->B * Hq * Mq * kHeadDim;
     const size_t layer_scores = (size_t)rows * cand_hi;
@@ -776,7 +821,12 @@ fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer,
     const unsigned pdl = flags & FX_LAUNCH_PDL;
     for (int l0 = 0; l0 < n_layers; l0 += kRetainBatch) {
         const int nb = std::min(kRetainBatch, n_layers - l0);
-        for (int l = l0; l < l0 + nb; ++l) {
+        fx_kv_desc kb = *kv;
+        kb.k = kv->k + (int64_t)l0 * src_stride_layer;
+        if (nb > 1 && score_tc_route(ds, &kb, src_stride_layer, nb, q + (size_t)l0 * q_layer, Hq, Mq, q_pos0, scale, 0,
+                                     cand_hi, scores, ws, fbytes, pdl != 0, static_cast<cudaStream_t>(stream), &st)) {
+            if (st != FX_OK) return st;
+        } else for (int l = l0; l < l0 + nb; ++l) {
             fx_kv_desc kl = *kv;
             kl.k = kv->k + (int64_t)l * src_stride_layer;
             kl.v = kv->v + (int64_t)l * src_stride_layer;
@@ -975,27 +1025,31 @@ bool fx::encode_kv_tensor_maps(const fx_kv_desc* kv, CUtensorMap* tk, CUtensorMa
     return true;
 }
 
-bool fx::encode_score_maps(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int n_cols, CUtensorMap* tk,
-                           CUtensorMap* tq, int* bcast)
+bool fx::encode_score_maps(const fx_kv_desc* kv, int64_t layer_stride, int layers, const fx_bf16* q, int Hq, int Mq,
+                           int n_cols, CUtensorMap* tk, CUtensorMap* tq, int* bcast)
 {
     EncodeTiledFn fn = encode_tiled_fn();
-    if (fn == nullptr || kv->Tcap < 1) return false;
+    if (fn == nullptr || kv->Tcap < 1 || layers < 1) return false;
     // a cache shared by every sequence (batch stride 0) is one batch entry of the map
     const bool bc = kv->stride_b == 0;
-    const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kv->Tcap, (cuuint64_t)kv->Hkv,
-                                (cuuint64_t)(bc ? 1 : kv->B)};
-    const cuuint64_t strides[3] = {(cuuint64_t)kv->stride_t * 2, (cuuint64_t)kv->stride_h * 2,
-                                   bc ? (cuuint64_t)kv->stride_h * 2 * (cuuint64_t)kv->Hkv : (cuuint64_t)kv->stride_b * 2};
-    for (int i = 0; i < 3; ++i)
+    const cuuint64_t nb = bc ? 1 : (cuuint64_t)kv->B;
+    const cuuint64_t dims[5] = {(cuuint64_t)kHeadDim, (cuuint64_t)kv->Tcap, (cuuint64_t)kv->Hkv, nb,
+                                (cuuint64_t)layers};
+    const cuuint64_t sb = bc ? (cuuint64_t)kv->stride_h * 2 * (cuuint64_t)kv->Hkv : (cuuint64_t)kv->stride_b * 2;
+    // one layer: any stride the encoder accepts (the layer coordinate is always 0)
+    const cuuint64_t sl = layers > 1 ? (cuuint64_t)layer_stride * 2 : sb * nb;
+    if (layers > 1 && layer_stride <= 0) return false;
+    const cuuint64_t strides[4] = {(cuuint64_t)kv->stride_t * 2, (cuuint64_t)kv->stride_h * 2, sb, sl};
+    for (int i = 0; i < 4; ++i)
         if (strides[i] == 0 || (strides[i] & 15u) != 0 || strides[i] >= (1ull << 40)) return false;
-    const cuuint32_t box[4] = {64, (cuuint32_t)kScoreKeys, 1, 1};
-    const cuuint32_t elem[4] = {1, 1, 1, 1};
-    if (fn(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(static_cast<const void*>(kv->k)), dims, strides,
+    const cuuint32_t box[5] = {64, (cuuint32_t)kScoreKeys, 1, 1, 1};
+    const cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+    if (fn(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(static_cast<const void*>(kv->k)), dims, strides,
            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
-    // q as [B Hq Mq] rows of 128 bf16 (contiguous); the kernel addresses row starts up to 2^31
-    const int64_t qrows = (int64_t)kv->B * Hq * Mq;
+    // q as [layers B Hq Mq] rows of 128 bf16 (contiguous); the kernel addresses row starts up to 2^31
+    const int64_t qrows = (int64_t)layers * kv->B * Hq * Mq;
     if (qrows >= 0x7fffffff) return false;
     const cuuint64_t qdims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)qrows};
     const cuuint64_t qstrides[1] = {(cuuint64_t)kRowBytes};

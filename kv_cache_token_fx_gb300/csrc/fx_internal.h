@@ -131,8 +131,9 @@ __host__ __device__ constexpr int score_item_tiles(int n_cols) { return (kScoreT
 __host__ __device__ constexpr int score_tc_cols(int R) { return R <= 16 ? 16 : (R <= 32 ? 32 : 64); }
 
 struct ScoreParams {
-    const int32_t* len;
+    const int32_t* len;       // [B], shared by the layers
     int B, Hkv, Tcap;
+    int layers;               // layers scored in one launch; pairs = layers * B * Hkv
     int k_bcast;              // the cache has batch stride 0: the tensor map's batch extent is 1
     const uint16_t* q;        // [B, Hq, Mq, 128]
     int Hq, G, Mq, R;
@@ -239,15 +240,16 @@ cudaError_t launch_stream_decode(const AttnParams& p, const CUtensorMap* tk, con
 bool encode_kv_tensor_maps(const fx_kv_desc* kv, CUtensorMap* tk, CUtensorMap* tv);
 size_t stream_decode_smem_bytes(int slots, int nsplit, int R);
 cudaError_t launch_focal_combine(const FocalCombineParams& p, bool pdl, cudaStream_t s);
-// tk: 4-D tensor map of K ([B or 1][Hkv][Tcap][128] bf16, boxes of kScoreKeys rows x 64 columns); tq: 2-D
-// tensor map of q ([B Hq Mq][128] bf16, boxes of N rows x 64 columns); both with the 128-byte swizzle.
+// tk: 5-D tensor map of K ([layers][B or 1][Hkv][Tcap][128] bf16, boxes of kScoreKeys rows x 64 columns);
+// tq: 2-D tensor map of q ([layers B Hq Mq][128] bf16, boxes of N rows x 64 columns); both with the
+// 128-byte swizzle.
 cudaError_t launch_score_tc(const ScoreParams& p, const CUtensorMap* tk, const CUtensorMap* tq, int grid, bool pdl,
                             cudaStream_t s);
 size_t score_tc_smem_bytes(int n_cols);
 // Encodes the tensor maps for launch_score_tc (*bcast is set when the batch stride is 0); false when the
 // strides or sizes allow no tensor map.
-bool encode_score_maps(const fx_kv_desc* kv, const fx_bf16* q, int Hq, int Mq, int n_cols, CUtensorMap* tk,
-                       CUtensorMap* tq, int* bcast);
+bool encode_score_maps(const fx_kv_desc* kv, int64_t layer_stride, int layers, const fx_bf16* q, int Hq, int Mq,
+                       int n_cols, CUtensorMap* tk, CUtensorMap* tq, int* bcast);
 cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_prefix_tc(const PrefixTcParams& p, bool pdl, cudaStream_t s);
 cudaError_t launch_focal_mass(const float* scores, int rows, int n, float inv_r, int accumulate, float* mass,

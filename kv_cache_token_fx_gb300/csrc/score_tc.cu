@@ -53,12 +53,12 @@ constexpr int kScThreads = 32 * (kScCoordWarp + 1);                  // + the co
 constexpr int kScTileBytes = kScoreKeys * kRowBytes;   // one 128-key K tile (32 KB)
 constexpr int kScHalf = kScTileBytes / 2;             // its 64-column half (one TMA copy)
 
-__device__ __forceinline__ void tma_load_k(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+__device__ __forceinline__ void tma_load_k(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
                                            uint64_t* bar)
 {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(bar))
         : "memory");
 }
 
@@ -222,9 +222,10 @@ __device__ __forceinline__ void mma_kq(uint32_t d_tmem, uint32_t k_tile, uint32_
     }
 }
 
-// One item: its (sequence, KV head), its key range [ja, jb) and the visible part [ja, jv).
+// One item: its (layer, sequence, KV head) -- the "pair" --, its key range [ja, jb) and the visible part
+// [ja, jv).
 struct Item {
-    int pair, split, b, h, ja, jb, jv, ntile;
+    int pair, split, layer, b, h, ja, jb, jv, ntile;
     bool bad_len;
 };
 
@@ -233,8 +234,11 @@ __device__ __forceinline__ Item decode_item(const ScoreParams& p, int item)
     Item it;
     it.pair = item / p.nsplit;
     it.split = item - it.pair * p.nsplit;
-    it.b = it.pair / p.Hkv;
-    it.h = it.pair - it.b * p.Hkv;
+    const int per_layer = p.B * p.Hkv;
+    it.layer = it.pair / per_layer;
+    const int bh = it.pair - it.layer * per_layer;
+    it.b = bh / p.Hkv;
+    it.h = bh - it.b * p.Hkv;
     int lenb = p.len[it.b];
     it.bad_len = lenb < 0 || lenb > p.Tcap;
     if (it.bad_len) lenb = lenb < 0 ? 0 : p.Tcap;
@@ -363,10 +367,11 @@ __global__ void __launch_bounds__(kScThreads, 1) score_tc_kernel(const ScorePara
             if (lane == 0) {
                 s_item[hf] = (int)tk;
                 mbar_arrive(&item_bar[hf]);   // releases the limits and the item
-                // The item's R query rows are rows (b Hq + h G) Mq .. + R - 1 of q viewed as [B Hq Mq][128]:
+                // The item's R query rows are rows ((layer B + b) Hq + h G) Mq .. + R - 1 of q viewed as
+                // [layers B Hq Mq][128]:
                 // they come with the first K tile, as the N-row K-major B operand of this buffer (the rows
                 // past R belong to other items or lie past the end, and no result reads their columns).
-                const int qrow = (it.b * p.Hq + it.h * p.G) * p.Mq;
+                const int qrow = ((it.layer * p.B + it.b) * p.Hq + it.h * p.G) * p.Mq;
                 const uint32_t dq = smem_addr(sQ0 + hf * N * kRowBytes);
                 for (int t = 0; t < it.ntile; ++t, ++g) {
                     const unsigned s = g % S;
@@ -379,8 +384,8 @@ __global__ void __launch_bounds__(kScThreads, 1) score_tc_kernel(const ScorePara
                     const uint32_t dst = smem_addr(ring + (size_t)s * kScTileBytes);
                     const int j0 = it.ja + t * kScoreKeys;
                     const int cb = p.k_bcast ? 0 : it.b;
-                    tma_load_k(dst, &tm_k, 0, j0, it.h, cb, &full_bar[s]);
-                    tma_load_k(dst + kScHalf, &tm_k, 64, j0, it.h, cb, &full_bar[s]);
+                    tma_load_k(dst, &tm_k, 0, j0, it.h, cb, it.layer, &full_bar[s]);
+                    tma_load_k(dst + kScHalf, &tm_k, 64, j0, it.h, cb, it.layer, &full_bar[s]);
                 }
             }
             __syncwarp();

@@ -404,11 +404,11 @@ def test_per_layer_retention_matches_oracle(fx):
 
 
 def test_retention_on_tensor_cores_matches_calls_and_captures(fx):
-    """FastKV retention with 32 window rows per KV head (the scoring takes the tensor-core route, layer
-    after layer on one workspace, as programmatic dependent launches).  Equal to the individual calls
-    (scores, top-k, compaction) and to the oracle; the same call captured in a CUDA graph and replayed
+    """FastKV retention with 32 window rows per KV head: the scoring takes the tensor-core route, eight
+    layers per launch (11 layers: a batch of 8, then one of 3).  Equal to the individual calls (scores of
+    one layer, top-k, compaction) and to the oracle; the same call captured in a CUDA graph and replayed
     gives the same result."""
-    n_layers, B, Hkv, G, Mq, T, keep = 5, 2, 2, 4, 8, 3000, 300
+    n_layers, B, Hkv, G, Mq, T, keep = 11, 2, 2, 4, 8, 3000, 300
     cand = T - Mq
     ks = torch.stack([rnd((B, Hkv, T, D), 190 + l, 1) for l in range(n_layers)])
     vs = torch.stack([rnd((B, Hkv, T, D), 190 + l, 2) for l in range(n_layers)])
