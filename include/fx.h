@@ -299,9 +299,11 @@ FX_API fx_status fx_kv_append(const fx_kv_out_desc* cache, int64_t stride_layer,
  *   q        [n_layers, B, Hq, Mq, 128] bf16 (contiguous): layer l's window queries
  *   idx_out  [n_layers, B, Hkv, keep_k] int32, written (ascending per row)
  *   1 <= keep_k <= cand_hi <= Tcap.  Results equal those of the individual calls.
- * Workspace: fx_retain_workspace_bytes(B, Hkv, Hq, Mq, Tcap, cand_hi) bytes (one layer's focal
- * scratch, reused layer after layer, and the scores of 8 layers: layers are scored 8 at a time and each
- * batch is selected by one top-k call over all its rows).
+ * Workspace: fx_retain_workspace_bytes(B, Hkv, Hq, Mq, Tcap, cand_hi) bytes: the scoring scratch and
+ * the scores of up to 32 layers.  Layers are taken 32 at a time; with more than 8 query rows per KV
+ * head a batch is scored by one launch of the tensor-core scoring kernel (otherwise by one focal call
+ * per layer), and each batch is selected by one top-k call over all its rows.  A K layout that admits
+ * no tensor map (strides not multiples of 16 bytes) takes the per-layer calls.
  */
 FX_API size_t fx_retain_workspace_bytes(int B, int Hkv, int Hq, int Mq, int Tcap, int cand_hi);
 FX_API fx_status fx_kv_retain_per_layer(const fx_kv_desc* kv, int64_t src_stride_layer, int n_layers,
