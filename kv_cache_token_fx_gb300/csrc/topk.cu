@@ -11,8 +11,9 @@
 // T = min over S_prev of the current scores is exceeded-or-met by at least k entries, so the top-k
 // lies in {score >= T}; the radix passes only count those candidates.  The result is unchanged.
 //
-// Rows up to kSmemKeys long are held in shared memory as keys; longer rows are re-read from global
-// memory (L2) on each pass.
+// Rows up to kSmemKeys long are held in shared memory as keys.  Longer rows are split over a cluster of
+// CTAs when there are few of them; otherwise each CTA reads its row from global memory until the
+// remaining candidates fit in shared memory (rows up to kFilterMaxN), or on every pass (longer rows).
 #include <stdint.h>
 
 #include "fx_internal.h"
@@ -115,31 +116,37 @@ struct SelectShared {
     uint32_t digit, gt, thr, bad;
 };
 
-// Radix-digit counting.  Every warp pair counts into its own row of `rows` with plain shared atomics --
-// no warp aggregation (match.any over 32 distinct digits cost more than the atomics it saved) and no
-// contention between pairs -- and the rows are then added up per bin into hist[256].  Counted: keys
-// key_at(j), j = tid, tid + kTkThreads, ... < n, that are >= thr and equal prefix under pmask; the digit
-// is byte `shift` of the key.  All threads call it; it begins and ends with a barrier.
-constexpr int kHistRows = kTkWarps / 2;
-template <typename KeyAt>
-__device__ __forceinline__ void count_digits(KeyAt key_at, int n, uint32_t thr, uint32_t prefix, uint32_t pmask,
-                                             int shift, uint32_t (*rows)[256], uint32_t (*part)[256], uint32_t* hist)
+// Radix-digit counting.  Each lane counts with plain shared atomics into histogram row (lane mod 16),
+// rows kHistStride = 257 words apart, and the rows are then added up per bin into hist[256].  Scores
+// span few exponents, so most keys of a warp share one or two top-byte digits: with a row per lane
+// pair, at most two lanes update one address, and lanes with the same digit hit different banks
+// (257 = 1 mod 32).  Rows shared by whole warps let up to 32 lanes collide on one address.
+constexpr int kHistRows = 16;
+constexpr int kHistStride = 257;
+constexpr int kHistWords = kHistRows * kHistStride;
+
+__device__ __forceinline__ uint32_t* hist_row_of_lane(uint32_t* rows)
+{
+    return rows + (threadIdx.x & (kHistRows - 1)) * kHistStride;
+}
+
+__device__ __forceinline__ void hist_rows_clear(uint32_t* rows)
+{
+    for (int i = threadIdx.x; i < kHistWords; i += kTkThreads) rows[i] = 0u;
+    __syncthreads();
+}
+
+// hist[b] = the sum of the rows' bin b; begins and ends with a barrier.
+__device__ __forceinline__ void hist_rows_sum(const uint32_t* rows, uint32_t (*part)[256], uint32_t* hist)
 {
     const int tid = threadIdx.x;
-    uint32_t* mine = rows[(tid >> 5) >> 1];
-    for (int i = tid; i < kHistRows * 256; i += kTkThreads) (&rows[0][0])[i] = 0u;
-    __syncthreads();
-    for (int j = tid; j < n; j += kTkThreads) {
-        const uint32_t key = key_at(j);
-        if (key >= thr && (key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1u);
-    }
     __syncthreads();
     {
         const int b = tid & 255;
         const int g = tid >> 8;   // 4 groups of kHistRows / 4 rows
         uint32_t t = 0u;
 #pragma unroll
-        for (int r = 0; r < kHistRows / 4; ++r) t += rows[g * (kHistRows / 4) + r][b];
+        for (int r = 0; r < kHistRows / 4; ++r) t += rows[(g * (kHistRows / 4) + r) * kHistStride + b];
         part[g][b] = t;
     }
     __syncthreads();
@@ -147,18 +154,61 @@ __device__ __forceinline__ void count_digits(KeyAt key_at, int n, uint32_t thr, 
     __syncthreads();
 }
 
+// Counted: keys key_at(j), j = tid, tid + kTkThreads, ... < n, that are >= thr and equal prefix under
+// pmask; the digit is byte `shift` of the key.  All threads call it; it begins and ends with a barrier.
+template <typename KeyAt>
+__device__ __forceinline__ void count_digits(KeyAt key_at, int n, uint32_t thr, uint32_t prefix, uint32_t pmask,
+                                             int shift, uint32_t* rows, uint32_t (*part)[256], uint32_t* hist)
+{
+    const int tid = threadIdx.x;
+    uint32_t* mine = hist_row_of_lane(rows);
+    hist_rows_clear(rows);
+    for (int j = tid; j < n; j += kTkThreads) {
+        const uint32_t key = key_at(j);
+        if (key >= thr && (key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1u);
+    }
+    hist_rows_sum(rows, part, hist);
+}
+
+// The warm-start threshold: the smallest key over the previous set prow[0, k) (thread tid's first entry
+// may have been read early into pre); 0 when an entry is out of [0, n) (reported once through err when
+// report).  sh.thr must be 0xffffffff and sh.bad 0, visible to all threads, on entry; all threads call it.
+constexpr int kNoPre = -2147483647 - 1;   // "prev index of this thread not loaded in advance"
+
+template <typename KeyAt>
+__device__ uint32_t warm_threshold(SelectShared& sh, const int32_t* prow, int pre, int k, int n, KeyAt key_at,
+                                   unsigned* err, bool report)
+{
+    const int tid = threadIdx.x;
+    uint32_t kmin = 0xffffffffu;
+    for (int i = tid; i < k; i += kTkThreads) {
+        const int t = (i == tid && pre != kNoPre) ? pre : prow[i];
+        if (t < 0 || t >= n)
+            sh.bad = 1u;
+        else
+            kmin = min(kmin, key_at(t));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    if ((tid & 31) == 0) atomicMin(&sh.thr, kmin);
+    __syncthreads();
+    if (sh.bad) {
+        if (tid == 0 && report) atomicOr(err, FX_DEVERR_INDEX);
+        return 0u;
+    }
+    return sh.thr;
+}
+
 // The top-k of one row of n keys (in skeys when SMEM, else read from src), written to orow in
 // ascending index order.  prow: the previous set of this row (warm start) or nullptr.  All threads of
 // the CTA call it; it begins and ends with a barrier.
-constexpr int kNoPre = -2147483647 - 1;   // "prev index of this thread not loaded in advance"
 
 template <bool SMEM>
-__device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*hpart)[256], const uint32_t* skeys,
+__device__ void select_row(SelectShared& sh, uint32_t* hrows, uint32_t (*hpart)[256], const uint32_t* skeys,
                            const float* src, int n, int k, const int32_t* prow, int32_t* orow, unsigned* err,
                            int pre = kNoPre)
 {
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
     if (tid == 0) {
         sh.thr = prow != nullptr ? 0xffffffffu : 0u;
         sh.bad = 0u;
@@ -166,26 +216,9 @@ __device__ void select_row(SelectShared& sh, uint32_t (*hrows)[256], uint32_t (*
     __syncthreads();
 
     // ---- warm-start threshold ----------------------------------------------------------------
-    uint32_t thr = 0u;
-    if (prow != nullptr) {
-        uint32_t kmin = 0xffffffffu;
-        for (int i = tid; i < k; i += kTkThreads) {
-            const int t = (i == tid && pre != kNoPre) ? pre : prow[i];
-            if (t < 0 || t >= n)
-                sh.bad = 1u;
-            else
-                kmin = min(kmin, get_key<SMEM>(skeys, src, t));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-        if (lane == 0) atomicMin(&sh.thr, kmin);
-        __syncthreads();
-        if (sh.bad) {
-            if (tid == 0) atomicOr(err, FX_DEVERR_INDEX);
-        } else {
-            thr = sh.thr;
-        }
-    }
+    uint32_t thr = prow != nullptr ? warm_threshold(sh, prow, pre, k, n,
+                                                    [&](int j) { return get_key<SMEM>(skeys, src, j); }, err, true)
+                                   : 0u;
 
     // ---- radix select: K* and the number of equal keys to take --------------------------------
     uint32_t prefix = 0u, pmask = 0u;
@@ -294,7 +327,7 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(const TopkParams p)
 {
     extern __shared__ uint32_t skeys[];
     __shared__ SelectShared sh;
-    __shared__ uint32_t s_rows[kHistRows][256];
+    __shared__ uint32_t s_rows[kHistWords];
     __shared__ uint32_t s_part[4][256];
 
     const int row = blockIdx.x;
@@ -323,14 +356,13 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_cluster_kernel(const TopkP
     __shared__ SelectShared sh;
     __shared__ uint32_t s_hist[2][256];   // this chunk's histogram, by round parity (read by the whole cluster)
     __shared__ uint32_t s_part[4][256];   // partial sums (of histogram rows, then of the cluster's chunks)
-    __shared__ uint32_t s_rows[kHistRows][256];
+    __shared__ uint32_t s_rows[kHistWords];
     __shared__ uint32_t s_tot[256];       // the row's histogram
     __shared__ uint32_t s_cnt[2];         // (greater, equal) keys of this chunk
     __shared__ uint32_t s_base[2];
     const int row = blockIdx.y / kTkCluster;
     const unsigned me = cluster_rank();
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
     const int n = p.n;
     const int k = p.k;
     const int chunk = (n + kTkCluster - 1) / kTkCluster;
@@ -350,26 +382,9 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_cluster_kernel(const TopkP
     __syncthreads();
 
     // warm-start threshold, the same in every CTA (scores read from global memory)
-    uint32_t thr = 0u;
-    if (prow != nullptr) {
-        uint32_t kmin = 0xffffffffu;
-        for (int i = tid; i < k; i += kTkThreads) {
-            const int t = (i == tid && pre != kNoPre) ? pre : prow[i];
-            if (t < 0 || t >= n)
-                sh.bad = 1u;
-            else
-                kmin = min(kmin, order_key(__ldg(src + t)));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-        if (lane == 0) atomicMin(&sh.thr, kmin);
-        __syncthreads();
-        if (sh.bad) {
-            if (tid == 0 && me == 0) atomicOr(p.err, FX_DEVERR_INDEX);
-        } else {
-            thr = sh.thr;
-        }
-    }
+    uint32_t thr = prow != nullptr ? warm_threshold(sh, prow, pre, k, n, [&](int j) { return order_key(__ldg(src + j)); },
+                                                    p.err, me == 0)
+                                   : 0u;
 
     // Radix passes over 8-bit digits.  Each round every CTA counts its chunk into one of two histograms
     // (the other may still be read by a slower CTA), and after one cluster barrier every CTA adds up the
@@ -470,6 +485,289 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_cluster_kernel(const TopkP
     cluster_sync();   // keep every CTA's shared memory alive until all remote reads are done
 }
 
+// Many rows too long for shared memory: one CTA per row reads its scores from global memory (16-byte
+// loads, four in flight per thread) on each radix pass, until the candidates -- the keys that match the
+// digits chosen so far -- fit in shared memory.  The pass that finds them that few (the previous pass's
+// chosen bin) also copies them there, (key, index), while it counts their next digit, and marks the keys
+// above them -- all selected -- in a bitmap of the row; the remaining passes run on the copy.  The selected
+// indices end as two bitmaps of the row (above K*, and equal to K* under the decided digits), and the
+// ordered output is one block scan over them.  Same selection, bit for bit, as select_row.
+constexpr int kFilterDynBytes = 200 * 1024;   // bitmaps + candidates (plus 21 KB of static histogram rows)
+constexpr int kFilterMaxN = 1 << 18;          // two bitmaps of 32 KB at most
+
+__host__ __device__ constexpr int filter_words(int n) { return (n + 31) / 32; }
+__host__ __device__ constexpr int filter_cap(int n) { return (kFilterDynBytes - 8 * filter_words(n)) / 8; }
+
+__device__ __forceinline__ float f4_at(const float4& v, int c) { return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w; }
+
+__device__ __forceinline__ void set_bit(uint32_t* bits, int j) { atomicOr(&bits[j >> 5], 1u << (j & 31)); }
+
+// The 16-byte groups of a row held by one round: group i = r0 + u kTkThreads + tid (u < kRoundGroups)
+// while i < n4; all loads of a round are in flight together.
+constexpr int kRoundGroups = 4;
+
+__device__ __forceinline__ void load_round(const float4* s4, int n4, int r0, float4 (&v)[kRoundGroups])
+{
+#pragma unroll
+    for (int u = 0; u < kRoundGroups; ++u) {
+        const int i = r0 + u * kTkThreads + threadIdx.x;
+        v[u] = i < n4 ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Groups of 16 bytes when the row starts on a 16-byte boundary, else none (single scores only).
+__device__ __forceinline__ int row_groups(const float* src, int n)
+{
+    return (reinterpret_cast<uintptr_t>(src) & 15u) == 0 ? n >> 2 : 0;
+}
+
+// f(key, j, valid) for every position of the row, in rounds that every thread of the CTA runs the same
+// number of times (valid = false past the end), so that f may use warp-wide votes.
+template <typename F>
+__device__ __forceinline__ void for_each_key_global(const float* src, int n, F f)
+{
+    const int tid = threadIdx.x;
+    const int n4 = row_groups(src, n);
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    for (int r0 = 0; r0 < n4; r0 += kRoundGroups * kTkThreads) {
+        float4 v[kRoundGroups];
+        load_round(s4, n4, r0, v);
+#pragma unroll
+        for (int u = 0; u < kRoundGroups; ++u) {
+            const int i = r0 + u * kTkThreads + tid;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) f(order_key(f4_at(v[u], c)), 4 * i + c, i < n4);
+        }
+    }
+    for (int t0 = 4 * n4; t0 < n; t0 += kTkThreads) {
+        const int j = t0 + tid;
+        const bool ok = j < n;
+        f(ok ? order_key(__ldg(src + j)) : 0u, j, ok);
+    }
+}
+
+// The global pass that moves the candidates to shared memory.  Keys >= thr that match prefix under
+// pmask: digit `shift` counted into this lane's histogram row `mine`, (key, index) appended to the
+// candidates; keys >= thr above the prefix (all selected): marked in gt_bits.  Candidate slots are
+// reserved with one shared atomic per warp and round (4 kRoundGroups keys per lane), not one per key.
+__device__ void collect_pass(const float* src, int n, uint32_t thr, uint32_t prefix, uint32_t pmask, int shift,
+                             uint32_t* mine, uint32_t* gt_bits, uint32_t* ckey, int32_t* cidx, int cap,
+                             uint32_t* ncand)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int n4 = row_groups(src, n);
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+    auto visit = [&](uint32_t key, int j, bool ok) -> bool {
+        const bool in = ok && key >= thr;
+        const uint32_t masked = key & pmask;
+        const bool match = in && masked == prefix;
+        if (match) atomicAdd(&mine[(key >> shift) & 255u], 1u);
+        if (in && masked > prefix) set_bit(gt_bits, j);
+        return match;
+    };
+    // cnt slots for this lane: a warp-inclusive scan and one atomic per warp; returns the lane's first slot
+    auto reserve = [&](uint32_t cnt) -> uint32_t {
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t base = 0u;
+        if (lane == 31 && wtot != 0u) base = atomicAdd(ncand, wtot);
+        base = __shfl_sync(0xffffffffu, base, 31);
+        return base + incl - cnt;
+    };
+    static_assert(4 * kRoundGroups <= 32, "one match bit per key of a round");
+    auto put = [&](uint32_t slot, uint32_t key, int j) {
+        if (slot < (uint32_t)cap) {
+            ckey[slot] = key;
+            cidx[slot] = j;
+        }
+    };
+    for (int r0 = 0; r0 < n4; r0 += kRoundGroups * kTkThreads) {
+        float4 v[kRoundGroups];
+        load_round(s4, n4, r0, v);
+        uint32_t m = 0u;
+#pragma unroll
+        for (int u = 0; u < kRoundGroups; ++u) {
+            const int i = r0 + u * kTkThreads + tid;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) m |= (uint32_t)visit(order_key(f4_at(v[u], c)), 4 * i + c, i < n4) << (4 * u + c);
+        }
+        uint32_t slot = reserve(__popc(m));
+#pragma unroll
+        for (int u = 0; u < kRoundGroups; ++u) {
+            const int i = r0 + u * kTkThreads + tid;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if ((m >> (4 * u + c)) & 1u) put(slot++, order_key(f4_at(v[u], c)), 4 * i + c);
+        }
+    }
+    for (int t0 = 4 * n4; t0 < n; t0 += kTkThreads) {
+        const int j = t0 + tid;
+        const bool ok = j < n;
+        const uint32_t key = ok ? order_key(__ldg(src + j)) : 0u;
+        const bool match = visit(key, j, ok);
+        const uint32_t slot = reserve(match ? 1u : 0u);
+        if (match) put(slot, key, j);
+    }
+}
+
+__global__ void __launch_bounds__(kTkThreads, 1) topk_filter_kernel(const TopkParams p)
+{
+    extern __shared__ uint32_t sdyn[];
+    __shared__ SelectShared sh;
+    __shared__ uint32_t s_rows[kHistWords];
+    __shared__ uint32_t s_part[4][256];
+    __shared__ uint32_t s_ncand;
+    const int tid = threadIdx.x;
+    const int row = blockIdx.x;
+    const int n = p.n;
+    const int k = p.k;
+    const int nw = filter_words(n);
+    const int cap = filter_cap(n);
+    uint32_t* gt_bits = sdyn;
+    uint32_t* eq_bits = sdyn + nw;
+    uint32_t* ckey = sdyn + 2 * nw;
+    int32_t* cidx = reinterpret_cast<int32_t*>(ckey + cap);
+    uint32_t* mine = hist_row_of_lane(s_rows);
+    const int32_t* prow = p.prev != nullptr ? p.prev + (int64_t)row * k : nullptr;
+    int pre = kNoPre;
+    if (p.prev_early && prow != nullptr && tid < k) pre = prow[tid];
+    for (int i = tid; i < 2 * nw; i += kTkThreads) sdyn[i] = 0u;
+    if (tid == 0) {
+        sh.thr = prow != nullptr ? 0xffffffffu : 0u;
+        sh.bad = 0u;
+        s_ncand = 0u;
+    }
+    griddep_wait();   // the scores usually come from the kernel just before
+    griddep_launch();
+    const float* src = p.scores + (int64_t)row * n;
+    __syncthreads();
+    uint32_t thr = prow != nullptr ? warm_threshold(sh, prow, pre, k, n, [&](int j) { return order_key(__ldg(src + j)); },
+                                                    p.err, true)
+                                   : 0u;
+
+    uint32_t prefix = 0u, pmask = 0u;
+    uint32_t krem = (uint32_t)k;
+    uint32_t bin = 0xffffffffu;   // counted keys that match the prefix (the last chosen bin)
+    bool in_smem = false;
+    int ncand = 0;
+    bool all_taken = false;
+    for (int pass = 0; pass < 4 && !all_taken; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int attempt = 0; attempt < 2; ++attempt) {
+            if (in_smem) {
+                count_digits([&](int j) { return ckey[j]; }, ncand, 0u, prefix, pmask, shift, s_rows, s_part, sh.hist);
+            } else {
+                const bool collect = pass > 0 && bin <= (uint32_t)cap;
+                hist_rows_clear(s_rows);
+                if (collect) {
+                    collect_pass(src, n, thr, prefix, pmask, shift, mine, gt_bits, ckey, cidx, cap, &s_ncand);
+                } else {
+                    for_each_key_global(src, n, [&](uint32_t key, int, bool ok) {
+                        if (ok && key >= thr && (key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1u);
+                    });
+                }
+                hist_rows_sum(s_rows, s_part, sh.hist);
+                if (collect) {
+                    const uint32_t got = s_ncand;
+                    if (got != bin && tid == 0) atomicOr(p.err, FX_DEVERR_INDEX);   // a logic slip: keep the kernel finite
+                    ncand = (int)min(got, (uint32_t)cap);
+                    in_smem = true;
+                }
+            }
+            if (tid < 32) find_digit(sh.hist, krem, &sh.digit, &sh.gt);
+            __syncthreads();
+            if (sh.digit == 0xffffffffu && thr != 0u) {
+                // only possible in pass 0 with a warm-start threshold built from repeated indices:
+                // drop the threshold and count again
+                thr = 0u;
+                __syncthreads();
+                continue;
+            }
+            break;
+        }
+        uint32_t digit = sh.digit;
+        uint32_t gt = sh.gt;
+        if (digit == 0xffffffffu) {
+            // unreachable for 1 <= k <= n (checked on the host); keep the kernel finite anyway
+            if (tid == 0) atomicOr(p.err, FX_DEVERR_INDEX);
+            digit = 0u;
+            gt = 0u;
+        }
+        prefix |= digit << shift;
+        pmask |= 255u << shift;
+        krem -= gt;
+        bin = sh.hist[digit];
+        // When the chosen bin holds exactly the keys still needed, all of them are taken (not with a
+        // warm-start threshold, which leaves keys of the bin below it uncounted).
+        all_taken = thr == 0u && bin == krem;
+        __syncthreads();   // sh.hist, sh.digit and sh.gt are rewritten in the next pass
+    }
+    // the selected keys: masked key > prefix, and the first krem (in index order) with masked key == prefix
+    const uint32_t kstar = prefix;
+    const uint32_t need_eq = krem;
+    if (in_smem) {
+        for (int c = tid; c < ncand; c += kTkThreads) {
+            const uint32_t key = ckey[c] & pmask;
+            if (key > kstar)
+                set_bit(gt_bits, cidx[c]);
+            else if (key == kstar)
+                set_bit(eq_bits, cidx[c]);
+        }
+    } else {
+        // no pass found few enough candidates (or the first pass decided): mark from the row itself.  A
+        // key equal to K* under the decided digits is >= the warm-start threshold: K* is then a whole key.
+        for_each_key_global(src, n, [&](uint32_t key, int j, bool ok) {
+            const uint32_t masked = key & pmask;
+            if (ok && masked > kstar)
+                set_bit(gt_bits, j);
+            else if (ok && masked == kstar)
+                set_bit(eq_bits, j);
+        });
+    }
+    __syncthreads();
+
+    // ordered output: each thread owns a contiguous run of bitmap words; position of a selected index j =
+    // (# greater before j) + min(# equal before j, need_eq), an equal one taken while (# equal before j) <
+    // need_eq.  Positions are < k by construction; the bound checks keep a logic slip from writing past
+    // the row.
+    const int per = (nw + kTkThreads - 1) / kTkThreads;
+    const int w0 = min(nw, tid * per);
+    const int w1 = min(nw, w0 + per);
+    uint32_t g = 0u, e = 0u;
+    for (int w = w0; w < w1; ++w) {
+        g += __popc(gt_bits[w]);
+        e += __popc(eq_bits[w]);
+    }
+    uint32_t total;
+    uint32_t gc = block_exclusive_scan(g, sh.swarp, &total);
+    uint32_t ec = block_exclusive_scan(e, sh.swarp, &total);
+    int32_t* orow = p.out + (int64_t)row * k;
+    for (int w = w0; w < w1; ++w) {
+        const uint32_t gw = gt_bits[w];
+        const uint32_t ew = eq_bits[w];
+        uint32_t u = gw | ew;
+        while (u != 0u) {
+            const int b = __ffs(u) - 1;
+            u &= u - 1u;
+            const int j = 32 * w + b;
+            if ((gw >> b) & 1u) {
+                const uint32_t pos = gc + min(ec, need_eq);
+                if (pos < (uint32_t)k) orow[pos] = j;
+                ++gc;
+            } else {
+                if (ec < need_eq && gc + ec < (uint32_t)k) orow[gc + ec] = j;
+                ++ec;
+            }
+        }
+    }
+}
+
 // Raise the kernel's dynamic shared memory limit to the largest key array (once per kernel and device).
 template <auto KERN>
 cudaError_t allow_smem_keys()
@@ -501,6 +799,20 @@ cudaError_t launch_topk(const TopkParams& p, bool pdl, cudaStream_t s)
         cudaError_t e = allow_smem_keys<topk_kernel<true>>();
         if (e != cudaSuccess) return e;
         return launch_kernel(topk_kernel<true>, dim3(p.rows), dim3(kTkThreads), smem, s, pdl, 0u, p);
+    }
+    // many long rows: one CTA per row, finishing in shared memory once the candidates fit
+    if (p.n <= kFilterMaxN) {
+        static int configured_device = -1;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (configured_device != dev) {
+            cudaError_t e = cudaFuncSetAttribute(topk_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kFilterDynBytes);
+            if (e != cudaSuccess) return e;
+            configured_device = dev;
+        }
+        const size_t smem = (size_t)8 * filter_words(p.n) + (size_t)8 * filter_cap(p.n);
+        return launch_kernel(topk_filter_kernel, dim3(p.rows), dim3(kTkThreads), smem, s, pdl, 0u, p);
     }
     return launch_kernel(topk_kernel<false>, dim3(p.rows), dim3(kTkThreads), 0, s, pdl, 0u, p);
 }

@@ -219,6 +219,56 @@ def test_topk_long_rows_stop_early_or_run_every_pass(fx):
         assert np.array_equal(got.cpu().numpy(), ref), (s.shape, k)
 
 
+def test_topk_many_rows_too_long_for_shared_memory(fx):
+    """Many rows longer than shared memory (one CTA per row reading global memory): the candidates move
+    to shared memory once a chosen bin fits (after the first or a later pass), or never (every key tied,
+    or k = n); rows not 16-byte aligned; a warm start; rows past the bitmap limit.  Exact against the
+    oracle."""
+    g = np.random.default_rng(12)
+    rows = 40   # more than a cluster launch takes
+    cases = []
+    # long-context shaped importance: lognormal bulk, a few planted high keys (bin fits after pass 1)
+    ln = np.exp(g.normal(size=(rows, 131072))).astype(np.float32) * 1e-5
+    ln[:, g.integers(0, 131072, size=1024)] += 0.01
+    cases.append((ln, 2048))
+    # distinct normal keys: the first chosen bin is too large, a later one fits
+    cases.append((g.normal(size=(rows, 50000)).astype(np.float32) * 1e-3 + 1.0, 2048))
+    # odd row length (rows not 16-byte aligned), ties at the boundary
+    cases.append(((g.integers(0, 300, size=(rows, 50001)) / 300).astype(np.float32), 2048))
+    # every key tied: no bin ever fits, the first need_eq = k indices are taken
+    cases.append((np.full((rows, 60000), 0.75, np.float32), 100))
+    # k = n: the first pass takes every key
+    cases.append((g.random(size=(rows, 45057)).astype(np.float32), 45057))
+    # the bin of 1.0 holds exactly k keys
+    two = np.full((rows, 50000), 0.5, np.float32)
+    two[:, :3000] = 1.0
+    for r in range(1, rows):
+        g.shuffle(two[r])
+    cases.append((two, 3000))
+    cases.append((two, 3001))
+    # k = 1 and a negative row
+    cases.append((-np.abs(g.normal(size=(rows, 46000))).astype(np.float32), 1))
+    # longer than the bitmaps allow: every pass reads global memory
+    cases.append((g.normal(size=(rows, 270000)).astype(np.float32), 1000))
+    for s, k in cases:
+        ref = oracle.topk(s, k)
+        got = fx.fx_topk_select(dev(torch.from_numpy(s)), k)
+        torch.cuda.synchronize()
+        assert fx.fx_device_errors() == 0
+        assert np.array_equal(got.cpu().numpy(), ref), (s.shape, k)
+    # warm start: a previous set from perturbed scores, read early and late
+    s = cases[1][0]
+    prev_scores = s + g.normal(0, 2e-4, size=s.shape).astype(np.float32)
+    prev = torch.from_numpy(oracle.topk(prev_scores, 2048))
+    ref = oracle.topk(s, 2048)
+    got = fx.fx_topk_select(dev(torch.from_numpy(s)), 2048, prev=dev(prev))
+    got_early = fx.fx_topk_select(dev(torch.from_numpy(s)), 2048, prev=dev(prev),
+                                  flags=fx.FX_LAUNCH_PDL | fx.FX_LAUNCH_INPUTS_READY)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert np.array_equal(got.cpu().numpy(), ref) and np.array_equal(got_early.cpu().numpy(), ref)
+
+
 def test_topk_negative_and_signed_zero(fx):
     s = torch.tensor([[-1.0, 0.0, -0.0, 2.0, -3.0, 2.0, -0.5]], dtype=torch.float32)
     for k in range(1, 8):
