@@ -181,6 +181,58 @@ def test_kv_select_full_sampled():
     print("kv_select sampled:", stats)
 
 
+def test_kv_select_per_layer_retention_full_sampled():
+    """FastKV per-layer retention at the full kv_select size, launched as the bench launches it (the 32
+    layers' window scores in one tensor-core launch, one top-k over their 1024 rows, one compaction;
+    programmatic dependent launches).  Sampled (layer, sequence, KV head) rows against the oracle's window
+    scores and top-k; the compaction bit for bit on the validated set."""
+    import kv_cache_token_fx_gb300 as fx
+    w = KvSelect()
+    L, B, Hkv, Hq, T, win = w.n_layers, w.B, w.Hkv, w.Hq, w.T, w.window
+    G, ncand, cap = Hq // Hkv, T - win, w.compact_cap
+    dev = torch.device("cuda", 0)
+    K = torch.empty((L, B, Hkv, T, D), dtype=torch.bfloat16, device=dev)
+    V = torch.empty_like(K)
+    QW = torch.empty((L, B, Hq, win, D), dtype=torch.bfloat16, device=dev)
+    for l in range(L):
+        k, v = w.layer_kv_salient(l, device=dev)
+        K[l].copy_(k)
+        V[l].copy_(v)
+        QW[l].copy_(w.window_queries_at(l, device=dev))
+        del k, v
+    ln = torch.full((B,), T, dtype=torch.int32, device=dev)
+    CK = torch.zeros((L, B, Hkv, cap, D), dtype=torch.bfloat16, device=dev)
+    CV = torch.zeros_like(CK)
+    clen = torch.zeros(B, dtype=torch.int32, device=dev)
+    idx = fx.fx_kv_retain_per_layer(K, V, ln, QW, w.k_select, ncand, ncand, CK, CV, clen, q_pos0=ncand,
+                                    flags=fx.FX_LAUNCH_PDL)
+    torch.cuda.synchronize()
+    assert fx.fx_device_errors() == 0
+    assert clen.tolist() == [w.keep] * B
+    del K, V
+    samples = [(0, 0, 0), (7, 1, 3), (w.switch_layer, 2, 5), (16, 3, 7), (24, 0, 6), (L - 1, 3, 1)]
+    stats = dict(rows=0, gapped=0, compacted=0)
+    lt = torch.tensor([T], dtype=torch.int32)
+    for l, b, h in samples:
+        kr, vr = w.layer_kv_salient_rows(l, b, h)
+        q = w.window_queries_at(l)[b:b + 1, h * G:(h + 1) * G].contiguous()
+        _, sc = oracle.focal(_as_kv(kr), _as_kv(vr), lt, q, q_pos0=ncand, cand=(0, ncand), want_out=False)
+        ref_idx = oracle.topk(sc[0, 0], w.k_select)
+        g_idx = idx[l, b, h].cpu().numpy()
+        _, gp, _ = pu.check_index_sets(g_idx.reshape(1, -1), ref_idx.reshape(1, -1), sc[0, 0].reshape(1, -1),
+                                       w.k_select)
+        stats["rows"] += 1
+        stats["gapped"] += gp
+        use = _validated_set(g_idx, ref_idx, sc[0, 0], w.k_select, stats)
+        ck, cv, cl = oracle.kv_compact(_as_kv(kr), _as_kv(vr), lt, torch.from_numpy(use).view(1, 1, -1), ncand, cap)
+        assert int(cl[0]) == w.keep
+        assert torch.equal(CK[l, b, h, :w.keep].cpu().view(torch.int16), ck[0, 0, :w.keep].view(torch.int16))
+        assert torch.equal(CV[l, b, h, :w.keep].cpu().view(torch.int16), cv[0, 0, :w.keep].view(torch.int16))
+        stats["compacted"] += 1
+    assert stats["rows"] == len(samples) and stats["compacted"] == len(samples), stats
+    print("kv_select per-layer retention sampled:", stats)
+
+
 # ----------------------------------------------------------------------------------------------
 def test_long_ctx_full_sampled():
     from tests.workload_runs import long_ctx_run
