@@ -560,9 +560,11 @@ __device__ __forceinline__ void for_each_key_global(const float* src, int n, F f
 }
 
 // The global pass that moves the candidates to shared memory.  Keys >= thr that match prefix under
-// pmask: digit `shift` counted into this lane's histogram row `mine`, (key, index) appended to the
-// candidates; keys >= thr above the prefix (all selected): marked in gt_bits.  Candidate slots are
-// reserved with one shared atomic per warp and round (4 kRoundGroups keys per lane), not one per key.
+// pmask: (key, index) appended to the candidates and, when COUNT, digit `shift` counted into this lane's
+// histogram row `mine`; keys >= thr above the prefix (all selected): marked in gt_bits.  Without COUNT
+// the prefix must be empty (every key >= thr is copied; mine and gt_bits are not used).  Candidate slots
+// are reserved with one shared atomic per warp and round (4 kRoundGroups keys per lane), not one per key.
+template <bool COUNT>
 __device__ void collect_pass(const float* src, int n, uint32_t thr, uint32_t prefix, uint32_t pmask, int shift,
                              uint32_t* mine, uint32_t* gt_bits, uint32_t* ckey, int32_t* cidx, int cap,
                              uint32_t* ncand)
@@ -573,6 +575,7 @@ __device__ void collect_pass(const float* src, int n, uint32_t thr, uint32_t pre
     const float4* s4 = reinterpret_cast<const float4*>(src);
     auto visit = [&](uint32_t key, int j, bool ok) -> bool {
         const bool in = ok && key >= thr;
+        if (!COUNT) return in;
         const uint32_t masked = key & pmask;
         const bool match = in && masked == prefix;
         if (match) atomicAdd(&mine[(key >> shift) & 255u], 1u);
@@ -629,6 +632,50 @@ __device__ void collect_pass(const float* src, int n, uint32_t thr, uint32_t pre
     }
 }
 
+// A threshold from a sample of the row: kSampleKeys keys at evenly spread positions (four consecutive
+// keys per thread when the row is 16-byte aligned).  m = the expected number of the row's top k in the
+// sample + 4 standard deviations + 8; the result is the lower edge of the 16-bit key bin that holds the
+// sample's m-th largest key, so that with high probability at least k keys of the row reach it, and about
+// m n / kSampleKeys do.  0 when that is not selective (m above half the sample) or the row is shorter than
+// 4 kSampleKeys.  skey: scratch for kSampleKeys keys.  All threads call it; it ends with a barrier.
+constexpr int kSampleKeys = 4 * kTkThreads;
+
+__device__ __noinline__ uint32_t sample_threshold(const float* src, int n, int k, uint32_t* skey, SelectShared& sh, uint32_t* rows,
+                                     uint32_t (*part)[256])
+{
+    const float mu = (float)kSampleKeys * (float)k / (float)n;
+    const float mf = mu + 4.f * sqrtf(mu) + 8.f;
+    if (n < 4 * kSampleKeys || mf > 0.5f * (float)kSampleKeys) return 0u;   // the same in every thread
+    const int tid = threadIdx.x;
+    const int n4 = row_groups(src, n);
+    if (n4 > 0) {
+        const int g = (int)(((int64_t)tid * n4) / kTkThreads);
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src) + g);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) skey[4 * tid + c] = order_key(f4_at(v, c));
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) skey[4 * tid + c] = order_key(__ldg(src + ((int64_t)(4 * tid + c) * n) / kSampleKeys));
+    }
+    __syncthreads();
+    uint32_t prefix = 0u, pmask = 0u;
+    uint32_t krem = (uint32_t)ceilf(mf);
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = 24 - 8 * pass;
+        count_digits([&](int j) { return skey[j]; }, kSampleKeys, 0u, prefix, pmask, shift, rows, part, sh.hist);
+        if (tid < 32) find_digit(sh.hist, krem, &sh.digit, &sh.gt);
+        __syncthreads();
+        const uint32_t d = sh.digit;
+        const uint32_t g = sh.gt;
+        __syncthreads();   // sh.digit and sh.gt are rewritten by the next pass
+        if (d == 0xffffffffu) return 0u;   // not reached: m <= half the sample
+        prefix |= d << shift;
+        pmask |= 255u << shift;
+        krem -= g;
+    }
+    return prefix;
+}
+
 __global__ void __launch_bounds__(kTkThreads, 1) topk_filter_kernel(const TopkParams p)
 {
     extern __shared__ __align__(16) uint32_t sdyn[];
@@ -664,6 +711,11 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_filter_kernel(const TopkPa
                                                     p.err, true)
                                    : 0u;
 
+    // A sampled threshold above the warm-start one lets the first pass copy its keys to shared memory
+    // (when at least k and at most cap keys reach it; otherwise that pass is counted again without it).
+    const uint32_t thr_s = sample_threshold(src, n, k, ckey, sh, s_rows, s_part);
+    bool sampled = thr_s > thr;
+
     uint32_t prefix = 0u, pmask = 0u;
     uint32_t krem = (uint32_t)k;
     uint32_t bin = 0xffffffffu;   // counted keys that match the prefix (the last chosen bin)
@@ -672,29 +724,52 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_filter_kernel(const TopkPa
     bool all_taken = false;
     for (int pass = 0; pass < 4 && !all_taken; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int attempt = 0; attempt < 2; ++attempt) {
+        for (int attempt = 0; attempt < 3; ++attempt) {
+            bool overflow = false;
             if (in_smem) {
                 count_digits([&](int j) { return ckey[j]; }, ncand, 0u, prefix, pmask, shift, s_rows, s_part, sh.hist);
             } else {
-                const bool collect = pass > 0 && bin <= (uint32_t)cap;
-                hist_rows_clear(s_rows);
-                if (collect) {
-                    collect_pass(src, n, thr, prefix, pmask, shift, mine, gt_bits, ckey, cidx, cap, &s_ncand);
-                } else {
-                    for_each_key_global(src, n, [&](uint32_t key, int, bool ok) {
-                        if (ok && key >= thr && (key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1u);
-                    });
-                }
-                hist_rows_sum(s_rows, s_part, sh.hist);
-                if (collect) {
+                if (pass == 0 && sampled) {
+                    // copy the keys that reach the sampled threshold, then count their first digit there
+                    collect_pass<false>(src, n, thr_s, 0u, 0u, shift, nullptr, nullptr, ckey, cidx, cap, &s_ncand);
+                    __syncthreads();
                     const uint32_t got = s_ncand;
-                    if (got != bin && tid == 0) atomicOr(p.err, FX_DEVERR_INDEX);   // a logic slip: keep the kernel finite
+                    overflow = got > (uint32_t)cap;
                     ncand = (int)min(got, (uint32_t)cap);
                     in_smem = true;
+                    count_digits([&](int j) { return ckey[j]; }, ncand, 0u, prefix, pmask, shift, s_rows, s_part,
+                                 sh.hist);
+                } else {
+                    const bool collect = pass > 0 && bin <= (uint32_t)cap;
+                    hist_rows_clear(s_rows);
+                    if (collect) {
+                        collect_pass<true>(src, n, thr, prefix, pmask, shift, mine, gt_bits, ckey, cidx, cap, &s_ncand);
+                    } else {
+                        for_each_key_global(src, n, [&](uint32_t key, int, bool ok) {
+                            if (ok && key >= thr && (key & pmask) == prefix) atomicAdd(&mine[(key >> shift) & 255u], 1u);
+                        });
+                    }
+                    hist_rows_sum(s_rows, s_part, sh.hist);
+                    if (collect) {
+                        const uint32_t got = s_ncand;
+                        if (got != bin && tid == 0) atomicOr(p.err, FX_DEVERR_INDEX);   // a logic slip: keep the kernel finite
+                        ncand = (int)min(got, (uint32_t)cap);
+                        in_smem = true;
+                    }
                 }
             }
             if (tid < 32) find_digit(sh.hist, krem, &sh.digit, &sh.gt);
             __syncthreads();
+            if (sampled && pass == 0 && (overflow || sh.digit == 0xffffffffu)) {
+                // fewer than k keys, or more than the candidates' room, reached the sampled threshold: count
+                // the row again without it (no bitmap bit was set: the prefix was empty)
+                sampled = false;
+                in_smem = false;
+                ncand = 0;
+                if (tid == 0) s_ncand = 0u;
+                __syncthreads();
+                continue;
+            }
             if (sh.digit == 0xffffffffu && thr != 0u) {
                 // only possible in pass 0 with a warm-start threshold built from repeated indices:
                 // drop the threshold and count again
@@ -716,9 +791,10 @@ __global__ void __launch_bounds__(kTkThreads, 1) topk_filter_kernel(const TopkPa
         pmask |= 255u << shift;
         krem -= gt;
         bin = sh.hist[digit];
-        // When the chosen bin holds exactly the keys still needed, all of them are taken (not with a
-        // warm-start threshold, which leaves keys of the bin below it uncounted).
-        all_taken = thr == 0u && bin == krem;
+        // When the chosen bin holds exactly the keys still needed, all of them are taken: the counted ones,
+        // which are exactly the copies in shared memory once the pass has copied them (keys below a
+        // threshold are uncounted; they are below every copy), or every key of the bin without a threshold.
+        all_taken = (thr == 0u || in_smem) && bin == krem;
         __syncthreads();   // sh.hist, sh.digit and sh.gt are rewritten in the next pass
     }
     // the selected keys: masked key > prefix, and the first krem (in index order) with masked key == prefix
