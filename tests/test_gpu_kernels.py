@@ -220,10 +220,10 @@ def test_topk_long_rows_stop_early_or_run_every_pass(fx):
 
 
 def test_topk_many_rows_too_long_for_shared_memory(fx):
-    """Many rows longer than shared memory (one CTA per row reading global memory): the candidates move
-    to shared memory once a chosen bin fits (after the first or a later pass), or never (every key tied,
-    or k = n); rows not 16-byte aligned; a warm start; rows past the bitmap limit.  Exact against the
-    oracle."""
+    """Many long rows (one CTA per row reading global memory): the candidates move to shared memory in
+    the first scan (a sampled threshold), once a chosen bin fits (after the first or a later pass), or
+    never (every key tied, or k = n); a sample that lets too few or too many keys through; rows not
+    16-byte aligned; a warm start; rows past the bitmap limit.  Exact against the oracle."""
     g = np.random.default_rng(12)
     rows = 40   # more than a cluster launch takes
     cases = []
@@ -248,6 +248,17 @@ def test_topk_many_rows_too_long_for_shared_memory(fx):
     cases.append((two, 3001))
     # k = 1 and a negative row
     cases.append((-np.abs(g.normal(size=(rows, 46000))).astype(np.float32), 1))
+    # the row's largest keys sit exactly at the positions the kernel samples (4 keys at each 16-byte group
+    # t * n / 4096, t < 1024), so fewer than k keys reach the sampled threshold and the row is counted
+    # again without it; and the unaligned rows' sampled positions (t * n / 4096, t < 4096)
+    adv = g.random(size=(rows, 65536)).astype(np.float32)
+    pos = (np.arange(1024)[:, None] * 64 + np.arange(4)[None, :]).reshape(-1)
+    adv[:, pos] = 10.0 + 100.0 * g.random(size=(rows, pos.size)).astype(np.float32)
+    cases.append((adv, 100))
+    adv_odd = g.random(size=(rows, 65537)).astype(np.float32)
+    pos_odd = (np.arange(4096, dtype=np.int64) * 65537) // 4096
+    adv_odd[:, pos_odd] = 10.0 + 100.0 * g.random(size=(rows, pos_odd.size)).astype(np.float32)
+    cases.append((adv_odd, 100))
     # longer than the bitmaps allow: every pass reads global memory
     cases.append((g.normal(size=(rows, 270000)).astype(np.float32), 1000))
     for s, k in cases:
