@@ -614,6 +614,30 @@ def run_window_case(args):
         raise SystemExit(1)
 
 
+def run_topk_long_case(args):
+    """The top-k of the long-context shape, `--reps` times, for profiler captures: 512 rows (64 sequences x
+    8 KV heads) of 131072 synthetic importance scores (a lognormal bulk and 1024 planted high keys per row;
+    268 MB, above L2), the top 2048 of each row."""
+    import kv_cache_token_fx_gb300 as fx
+    from synth.workloads import LongCtx
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = LongCtx()
+    rows, n, k = w.B * w.Hkv, w.T, w.k
+    g = torch.Generator(device=dev).manual_seed(131072)
+    s = torch.exp(torch.randn(rows, n, device=dev, generator=g)) * (1.0 / n)
+    hot = torch.randint(0, n, (rows, 1024), device=dev, generator=g)
+    s.scatter_add_(1, hot, torch.full((rows, 1024), 1e3 / n, device=dev))
+    out = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    for _ in range(args.reps):
+        fx.fx_topk_select(s, k, out=out)
+    torch.cuda.synchronize()
+    bits = fx.fx_device_errors()
+    print(json.dumps({"kernel_case": "topk_long", "reps": args.reps, "device_errors": bits}))
+    if bits:
+        raise SystemExit(1)
+
+
 def run_kernel_case(args):
     """A small, fixed case of one kernel for profiler captures: the decode-shaped call on `--layers`
     distinct layers (each layer's KV is 160 MB, so even one layer exceeds L2), `--reps` passes."""
@@ -623,6 +647,9 @@ def run_kernel_case(args):
         return
     if args.kernel_case == "window":
         run_window_case(args)
+        return
+    if args.kernel_case == "topk_long":
+        run_topk_long_case(args)
         return
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -1104,7 +1131,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pdl", action="store_true", help="plain stream-ordered launches (no programmatic dependent launch)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk", "hpd", "window"], default=None,
+    ap.add_argument("--kernel-case", choices=["sparse", "focal", "topk", "hpd", "window", "topk_long"], default=None,
                     help="run a small fixed case of one kernel (for profiler captures) instead of the bench")
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--reps", type=int, default=2)
