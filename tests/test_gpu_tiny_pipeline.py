@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 def enforce_gaps(k, v, length, q, kk, max_iter=60):
     """Make every row's rank-k / rank-(k+1) gap at least 2e-3 (relative) by halving the keys of the
-    near-boundary losers, judged by the oracle's scores.  Halving a bf16 row is exact."""
+    near-boundary losers, as ranked by the oracle's scores.  Halving a bf16 row is exact."""
     k = k.clone()
     for _ in range(max_iter):
         _, sc = oracle.focal(k, v, length, q)
