@@ -69,7 +69,20 @@ def test_host_argument_checks_without_gpu(lib):
     assert retain(3, 601, 37) == 1 and b"cand_hi" in lib.fx_last_error()
     assert retain(3, 596, 597) == 1 and b"keep_k" in lib.fx_last_error()
     assert retain(3, 596, 37) == 3    # no workspace
+    # the window queries and the softmax are checked before any device work too
+    retain_q = lambda hq, q, q_pos0, scale: lib.fx_kv_retain_per_layer(
+        ctypes.byref(kv), ctypes.c_int64(2 * 2 * 600 * 128), 3, q, hq, 4, q_pos0, ctypes.c_float(scale), 596, 37, 596,
+        ctypes.c_void_p(256), ctypes.byref(dst), ctypes.c_int64(0), None, ctypes.c_size_t(0), ctypes.c_uint(0), None)
+    assert retain_q(3, ctypes.c_void_p(256), 596, 1.0) != 0                       # 3 query heads over 2 KV heads
+    assert retain_q(4, ctypes.c_void_p(264), 596, 1.0) == 1 and b"16-byte" in lib.fx_last_error()
+    assert retain_q(4, ctypes.c_void_p(256), -2, 1.0) == 1 and b"q_pos0" in lib.fx_last_error()
+    assert retain_q(4, ctypes.c_void_p(256), 596, float("nan")) == 1 and b"scale" in lib.fx_last_error()
+    assert retain_q(4, ctypes.c_void_p(256), 596, 1.0) == 3                       # valid: only the workspace is missing
+    # the workspace holds the scores of a batch of layers and the scoring scratch of all of them
     assert lib.fx_retain_workspace_bytes(2, 2, 4, 4, 600, 596) > 2 * 2 * 596 * 4
+    lib.fx_focal_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.fx_retain_workspace_bytes(4, 8, 32, 8, 32768, 32760) >= \
+        lib.fx_focal_workspace_bytes(4, 8, 32, 8, 32768) + 32 * 4 * 8 * 32760 * 4
     # decode-step append: argument checks before any device work
     lib.fx_kv_append.restype = ctypes.c_int
     append = lambda n_layers, knew, pos, flags=0: lib.fx_kv_append(
